@@ -1,0 +1,453 @@
+#!/usr/bin/env python
+"""Benchmark of one layer-step of RAG KV-cache fusion on GB300.
+
+Workload: the Qwen3-8B-shaped single layer -- 8 chunks x 512 context tokens
++ 64 query tokens (T = 4160), hidden 4096, 32 query / 8 KV heads, head_dim
+128, RoPE base 1e6, bf16, recompute ratio 0.15 -- with synthetic inputs.
+
+A step is one ``fuse_layer_step``: stitch + re-rotate, deviation score,
+top-k, gathered QKV projection with RoPE and scatter, selected-row causal
+attention.  The metric is fused (context + query) tokens per second per
+layer-step.  Inputs are resident in HBM; consecutive steps cycle through
+several independent input sets whose total exceeds twice the L2, so no step
+reads another step's data from L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+``--impl reference`` times the CPU oracle (fp64 numpy) on the machine's host
+cores on the same workload.  Under torchrun (N > 1) every rank runs its own
+independent copy of the workload (weak scaling, no collective on the data
+path); rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "qwen3_8b_layer"
+METRIC = "cache-fusion fused tokens/s per layer-step"
+UNIT = "fused tokens/s"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), float(j.get("bf16_tflops_sustained", j["bf16_tflops"])), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _config_json(cfg, layouts, n_sets, set_bytes):
+    l = layouts[0]
+    return {
+        "workload": f"{cfg.name}: {len(l.chunk_lens)} chunks x {l.chunk_lens[0]} context + "
+                    f"{l.query_len} query tokens, hidden {cfg.hidden}, {cfg.n_q_heads}/{cfg.n_kv_heads} "
+                    f"heads, head_dim {cfg.head_dim}, RoPE base {cfg.rope_base:g}, ratio {cfg.ratio}",
+        "tokens_per_step": l.n_tok,
+        "context_tokens": l.n_ctx,
+        "recomputed_rows": None,
+        "kv_storage": cfg.kv_storage,
+        "l2": f"inputs rotate over {n_sets} independent sets ({n_sets * set_bytes / 2**20:.0f} MiB > 2x L2)",
+    }
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index=0):
+        self.proc = None
+        self.path = os.path.join("/tmp", f"fusekv_clocks_{os.getpid()}.csv")
+        sel = []
+        try:
+            pr = torch.cuda.get_device_properties(device_index)
+            bus = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0"
+            sel = ["-i", bus]
+        except Exception:
+            sel = []
+        self.cmd = ["nvidia-smi"] + sel + ["--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                                           "-lms", "100"]
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(self.cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    smax.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[4:8]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline object)
+# ---------------------------------------------------------------------------
+
+def _oracle_inputs(cfg):
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import harness  # noqa: E402  (test glue: oracle-made chunk caches)
+    case = harness.make_case(cfg)
+    f = harness.f64
+    return case, f(case.draws.H), f(case.draws.Wq), f(case.draws.Wk), f(case.draws.Wv)
+
+
+def _oracle_step(orc, cfg, case, H, Wq, Wk, Wv, attn_rows):
+    """One oracle layer-step; attention evaluated for ``attn_rows`` (indices
+    into S, or None = all).  Returns (seconds, fixed seconds, attention
+    seconds, S, rows)."""
+    t0 = time.perf_counter()
+    Kc, Vc = orc.stitch_rerotate(case.K_cached, case.V_cached, cfg.rope_base)
+    N = Kc.shape[0]
+    sc = orc.deviation_scores(H[:N], Wv, Vc, cfg.n_kv_heads, cfg.head_dim)
+    idx = orc.select_topk(sc, orc.k_from_ratio(cfg.ratio, N))
+    T = H.shape[0]
+    Kf = np.zeros((T, cfg.n_kv_heads, cfg.head_dim))
+    Vf = np.zeros_like(Kf)
+    Kf[:N], Vf[:N] = Kc, Vc
+    S = orc.selected_rows(idx, N, T)
+    t1 = time.perf_counter()
+    rows = np.arange(len(S)) if attn_rows is None else attn_rows(S)
+    orc.recompute_selected(H, Wq, Wk, Wv, idx, N, Kf, Vf, cfg.n_q_heads, cfg.n_kv_heads,
+                           cfg.head_dim, cfg.rope_base, out_rows=rows)
+    t2 = time.perf_counter()
+    return t2 - t0, t1 - t0, t2 - t1, S, rows
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def _sample_rows(frac):
+    def pick(S):
+        n = len(S)
+        m = max(1, int(round(n * frac)))
+        return np.unique(np.linspace(0, n - 1, m).astype(int))
+    return pick
+
+
+def _scaled_seconds(t_total, t_attn, S, rows):
+    """Full-step time estimated from an attention row sample: attention cost
+    scales with the keys read, sum over rows of (p + 1)."""
+    if len(rows) == len(S):
+        return t_total
+    keys_all = float(np.sum(S + 1))
+    keys_smp = float(np.sum(S[rows] + 1))
+    return (t_total - t_attn) + t_attn * keys_all / keys_smp
+
+
+def cpu_oracle_run(cfg, steps, warmup, budget_s):
+    from oracle import fusion as orc
+    case, H, Wq, Wk, Wv = _oracle_inputs(cfg)
+    T = H.shape[0]
+    # probe one step with a 10% attention sample to size the per-step sample
+    t, tf, ta, S, rows = _oracle_step(orc, cfg, case, H, Wq, Wk, Wv, _sample_rows(0.1))
+    full_est = _scaled_seconds(t, ta, S, rows)
+    per_step = budget_s / max(1, steps + warmup)
+    frac = 1.0 if full_est <= per_step else max(0.02, (per_step - tf) / max(full_est - tf, 1e-9))
+    frac = min(1.0, frac)
+    picker = None if frac >= 1.0 else _sample_rows(frac)
+    for _ in range(warmup):
+        _oracle_step(orc, cfg, case, H, Wq, Wk, Wv, picker)
+    secs = []
+    for _ in range(steps):
+        t, tf, ta, S, rows = _oracle_step(orc, cfg, case, H, Wq, Wk, Wv, picker)
+        secs.append(_scaled_seconds(t, ta, S, rows))
+    mean = float(np.mean(secs))
+    sample = ("full layer-step" if picker is None else
+              f"stitch, deviation, top-k and projections in full; attention for {len(rows)} of "
+              f"{len(S)} recomputed rows, scaled by keys read")
+    return {"value": T / mean, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+            "sample": sample + f" ({cfg.name}, {steps} step(s), fp64 numpy)",
+            "ms_per_step": mean * 1e3}
+
+
+# ---------------------------------------------------------------------------
+# native (CUDA) arm
+# ---------------------------------------------------------------------------
+
+def _make_set(cfg, layouts, layer, fk, workload, synth):
+    d = synth.draw_layer(cfg, layouts, layer=layer, device="cuda")
+    caches = workload.gpu_pic_caches(cfg, layouts, d.H_clean, d.Wk, d.Wv)
+    b = workload.layer_buffers(cfg, layouts, d.H, d.Wq, d.Wk, d.Wv, caches, device="cuda")
+    del d
+    return b
+
+
+def _set_bytes(b):
+    n = 0
+    for t in (b.H, b.Wq, b.Wk, b.Wv, b.Kf, b.Vf, b.O):
+        n += t.numel() * t.element_size()
+    for t in b.storage.values():
+        if isinstance(t, torch.Tensor):
+            n += t.numel() * t.element_size()
+    return n
+
+
+def _step(fk, b):
+    fk.layer_step(b.desc, b.chunks, b.reqs, b.H, b.Wq, b.Wk, b.Wv, True, b.idx, b.Kf, b.Vf, b.O,
+                  b.score, b.ws)
+
+
+def native_run(args, ws, rank, local):
+    from rag_kv_cache_rerotate_gb300 import _build, fusekv as fk, synth, workload
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    if rank == 0:
+        _build.build()
+    if ws > 1:
+        dist.barrier()
+    fk.load()
+    hbm_gbs, bf16_tf, bf16_tf_sus, peak_src = _peaks()
+    cfg = synth.CONFIGS[WORKLOAD]
+    layouts = synth.draw_layouts(cfg)
+    sets = [_make_set(cfg, layouts, i, fk, workload, synth) for i in range(1)]
+    sb = _set_bytes(sets[0])
+    n_sets = max(2, math.ceil(2 * L2_BYTES / sb) + 1)
+    sets += [_make_set(cfg, layouts, i, fk, workload, synth) for i in range(1, n_sets)]
+    T = layouts[0].n_tok
+    stream = torch.cuda.current_stream()
+
+    for i in range(args.warmup):
+        _step(fk, sets[i % n_sets])
+    fk.check_errors(sets[0].ws)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    fk.trace_begin(args.steps * 16 + 16)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        _step(fk, sets[i % n_sets])
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    trace = fk.trace_end()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    t = torch.tensor([ms], device="cuda", dtype=torch.float64)
+    if ws > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms = float(t.item())
+    for b in sets:
+        fk.check_errors(b.ws)
+
+    # per-kernel times from the trace (events on the launching stream)
+    per = {}
+    for name, kms in trace:
+        c, tot = per.get(name, (0, 0.0))
+        per[name] = (c + 1, tot + kms)
+    dom = max(per.items(), key=lambda kv: kv[1][1])[0] if per else None
+
+    # algorithmic work per launch
+    b0 = sets[0]
+    q = b0.reqs[0]
+    R = q.k + q.n_query
+    idx = b0.idx[:q.k].cpu().numpy().astype(np.int64)
+    S = np.concatenate([idx, np.arange(q.n_ctx, q.n_ctx + q.n_query)])
+    Hkv, Hq, d, D, N = cfg.n_kv_heads, cfg.n_q_heads, cfg.head_dim, cfg.hidden, q.n_ctx
+    work = {
+        "stitch_rerotate": ("hbm", 4.0 * N * Hkv * d * 2),
+        "deviation_gemm_tc": ("tensor", 2.0 * T * D * Hkv * d),
+        "deviation_gemm_simt": ("tensor", 2.0 * T * D * Hkv * d),
+        "qkv_gemm_tc": ("tensor", 2.0 * R * D * (Hq + 2 * Hkv) * d),
+        "qkv_gemm_simt": ("tensor", 2.0 * R * D * (Hq + 2 * Hkv) * d),
+        "attention_tc": ("tensor", 4.0 * d * Hq * float(np.sum(S + 1))),
+        "attention_simt": ("tensor", 4.0 * d * Hq * float(np.sum(S + 1))),
+    }
+    roof = None
+    kernels = {n: {"launches": c, "avg_us": 1e3 * tot / c} for n, (c, tot) in per.items()}
+    for n, (bound, amount) in work.items():
+        if n in per:
+            c, tot = per[n]
+            avg_s = tot / c / 1e3
+            if bound == "hbm":
+                kernels[n]["GB/s"] = amount / avg_s / 1e9
+                kernels[n]["frac_hbm"] = kernels[n]["GB/s"] / hbm_gbs
+            else:
+                kernels[n]["TFLOP/s"] = amount / avg_s / 1e12
+                kernels[n]["frac_bf16"] = kernels[n]["TFLOP/s"] / bf16_tf_sus
+    if dom in work:
+        bound, amount = work[dom]
+        c, tot = per[dom]
+        avg_s = tot / c / 1e3
+        if bound == "hbm":
+            ach, peak, unit = amount / avg_s / 1e9, hbm_gbs, "GB/s"
+        else:
+            ach, peak, unit = amount / avg_s / 1e12, bf16_tf_sus, "TFLOP/s"
+        roof = {"bound": bound, "kernel": dom, "achieved": ach, "peak": peak, "unit": unit,
+                "frac": ach / peak, "traffic": None,
+                "peak_source": f"{peak_src} ({'sustained bf16' if bound == 'tensor' else 'HBM copy'})"}
+
+    # end to end through the C ABI with host buffers
+    e2e = None
+    if args.e2e_steps > 0:
+        b = sets[0]
+        host_in = []
+        for tsr in [b.H] + [v for k, v in b.storage.items() if k in ("K", "V")]:
+            h = torch.empty(tsr.shape, dtype=tsr.dtype, pin_memory=True)
+            h.copy_(tsr)
+            host_in.append((h, tsr))
+        O_h = torch.empty(b.O.shape, dtype=b.O.dtype, pin_memory=True)
+        idx_h = torch.empty(b.idx.shape, dtype=b.idx.dtype, pin_memory=True)
+        h2d = sum(h.numel() * h.element_size() for h, _ in host_in)
+        d2h = O_h.numel() * O_h.element_size() + idx_h.numel() * idx_h.element_size()
+
+        def e2e_step():
+            for h, dv in host_in:
+                dv.copy_(h, non_blocking=True)
+            _step(fk, b)
+            O_h.copy_(b.O, non_blocking=True)
+            idx_h.copy_(b.idx, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1)
+        te = torch.tensor([ems], device="cuda", dtype=torch.float64)
+        if ws > 1:
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        ems = float(te.item())
+        e2e = {"value": ws * T * args.e2e_steps / (ems / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "steps": args.e2e_steps,
+               "what": "pinned-host chunk K/V caches and H copied in, fuse_layer_step, O and idx copied out"}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_run(cfg, 1, 0, budget_s=args.cpu_budget)
+        cpu.pop("ms_per_step", None)
+
+    launches = len(trace)
+    cfg_json = _config_json(cfg, layouts, n_sets, sb)
+    cfg_json["recomputed_rows"] = int(R)
+    cfg_json["parallelism"] = f"replicas x{ws}" if ws > 1 else "single GPU"
+    out = {
+        "metric": METRIC, "value": ws * T * args.steps / (ms / 1e3), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Gaussian draws; chunk caches from fuse_pic_precompute)",
+        "config": cfg_json, "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches, "clocks": clocks, "impl": "native",
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def reference_run(args, ws, rank):
+    if rank != 0:
+        return
+    from rag_kv_cache_rerotate_gb300 import synth
+    cfg = synth.CONFIGS[WORKLOAD]
+    layouts = synth.draw_layouts(cfg)
+    r = cpu_oracle_run(cfg, args.steps, args.warmup, budget_s=args.ref_budget)
+    ms = r.pop("ms_per_step")
+    out = {
+        "metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config_json(cfg, layouts, 1, 0), "impl": "reference", "cpu_baseline": r,
+        "e2e": {"value": r["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    out["config"].pop("l2")
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=30.0)
+    ap.add_argument("--ref-budget", type=float, default=150.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = _dist()
+    if args.impl == "reference":
+        reference_run(args, ws, rank)
+    else:
+        native_run(args, ws, rank, local)
+
+
+if __name__ == "__main__":
+    main()

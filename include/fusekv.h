@@ -1,0 +1,280 @@
+/*
+ * fusekv.h -- C ABI of the cache-fusion layer-step library (libfusekv.so).
+ *
+ * One layer-step of RAG KV-cache fusion with selective recomputation, as
+ * stated on two pages:
+ *   [QCFuse]  "QCFuse: Query-Aware Cache Fusion via Compressed View for
+ *             Efficient RAG Serving", section 2.1 (Eqs. 1-7), Eq. 11.
+ *   [KVBoost] "KVBoost: Chunk-Level KV Cache Reuse with Deviation-Guided
+ *             Recomputation", sections 3.1-3.2 (Eqs. 1-3), 4.5 (Eq. 7),
+ *             4.6.2 (Alg. 2, CacheBlendRecompute).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Ownership.  The caller allocates and owns every buffer, the workspace
+ *   included.  The library allocates no device memory and keeps no pointer
+ *   after a call returns.  All work is enqueued on the caller's stream; the
+ *   buffers must stay valid until the stream has passed that point.
+ * Pointers.  Every tensor pointer is a device pointer aligned to 16 bytes,
+ *   unless the field says "host".
+ * Errors.  Argument errors are detected on the host and returned before any
+ *   launch.  Launch failures return FUSE_ERR_CUDA.  Errors that only the GPU
+ *   can see (an out-of-range block id or selected index, an unsorted index
+ *   list, a wait that timed out) are recorded in the workspace's error word
+ *   and reported by fuse_check_errors().  Nothing aborts or exits.
+ * Layouts (row-major, innermost last).
+ *   H        [T_total, hidden]            current hidden states; request r owns
+ *                                         rows [row0, row0 + N_r + Qn_r): its N_r
+ *                                         context tokens, then its Qn_r query tokens.
+ *   Wq       [Hq * d, hidden]             projection weights (nn.Linear layout:
+ *   Wk, Wv   [Hkv * d, hidden]             out x in, both GEMM operands K-major).
+ *   Kf, Vf   [T_total, Hkv, d]            the fused cache, rows aligned with H.
+ *   score    [N_total]                    request r's scores at [score0, score0 + N_r).
+ *   idx      [K_total] int32              request r's k_r selected context
+ *                                         positions (request-local, ascending) at
+ *                                         [sel0, sel0 + k_r).
+ *   O        [R_total, Hq, d]             attention rows of S_r = idx_r U {N_r .. T_r-1}
+ *                                         in ascending position, at [out0, out0 + R_r),
+ *                                         R_r = k_r + Qn_r.
+ *   Query head h reads KV head h / (Hq / Hkv).  Positions are request-local:
+ *   context token t sits at position t, query token j at N_r + j.
+ * RoPE.  Rotate-half pairing (j, j + d/2) with theta_j = base^(-2j/d); the
+ *   rotation R^p turns pair j by the angle p * theta_j ([KVBoost] Eq. 3).
+ */
+#ifndef FUSEKV_H
+#define FUSEKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t); NULL is the legacy default stream. */
+typedef struct CUstream_st* fuse_stream_t;
+
+typedef enum {
+  FUSE_OK = 0,
+  FUSE_ERR_INVALID_ARG = 1,   /* null pointer, bad size, inconsistent tables      */
+  FUSE_ERR_MISALIGNED = 2,    /* a pointer or row stride not aligned to 16 bytes   */
+  FUSE_ERR_UNSUPPORTED = 3,   /* a valid request this build does not handle        */
+  FUSE_ERR_WORKSPACE = 4,     /* workspace null or smaller than fuse_workspace_size */
+  FUSE_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed              */
+  FUSE_ERR_TIMEOUT = 6,       /* (device) a bounded wait gave up                   */
+  FUSE_ERR_DEVICE_BOUNDS = 7  /* (device) an index read from device memory was out
+                                 of range or out of order; the access was skipped  */
+} fuse_status_t;
+
+typedef enum { FUSE_F32 = 0, FUSE_BF16 = 1, FUSE_U8_ASYM = 2 } fuse_dtype_t;
+typedef enum { FUSE_KV_CONTIGUOUS = 0, FUSE_KV_PAGED = 1 } fuse_kv_layout_t;
+typedef enum { FUSE_ROPE_ROTATE_HALF = 0 } fuse_pos_encoding_t;
+
+/* Shape of one attention layer.  head_dim must be 64 or 128 and n_q_heads a
+ * multiple of n_kv_heads.  dtype (FUSE_F32 or FUSE_BF16) is the storage type
+ * of H, the weights, the fused cache, Q and O; arithmetic accumulates in fp32.
+ * Only rotary position encoding is accepted ([KVBoost] section 5 limits reuse
+ * to RoPE models): any other pos_encoding returns FUSE_ERR_UNSUPPORTED. */
+typedef struct {
+  int32_t hidden;
+  int32_t n_q_heads;
+  int32_t n_kv_heads;
+  int32_t head_dim;
+  double rope_base;
+  int32_t pos_encoding;
+  int32_t dtype;
+} fuse_layer_desc_t;
+
+/* One cached chunk c_i of a request ([QCFuse] Eqs. 1, 3): its keys were
+ * computed alone at chunk-local positions 0 .. len-1.
+ *   dst_row  first row of the chunk in the packed fused cache / H.
+ *   pos      request-local position o_i of the chunk's first token (the
+ *            re-rotation angle offset, [QCFuse] Eq. 4).
+ *   len      number of tokens.
+ * Storage, selected by fuse_chunks_t.kv_layout / kv_storage:
+ *   CONTIGUOUS  k, v point at this chunk's own [len, Hkv, d] arrays.
+ *   PAGED       k, v point at the shared pool [n_blocks, block_size, Hkv, d];
+ *               block_table (device, [ceil(len / block_size)] int32) lists the
+ *               pool blocks holding tokens 0.., block_size per block.
+ *   U8_ASYM     KIVI asymmetric int8 ([KVBoost] Eq. 7), codes uint8 0..255,
+ *               x = zero + q * scale with fp16 scale and zero:
+ *               k_scale, k_zero  [Hkv, d]  per channel over the chunk's tokens;
+ *               v_scale, v_zero  [len, Hkv] per token (CONTIGUOUS) or
+ *                                [n_blocks, block_size, Hkv] (PAGED pool).
+ *   For fuse_pic_precompute, k and v are outputs (CONTIGUOUS F32/BF16 only). */
+typedef struct {
+  const void* k;
+  const void* v;
+  const int32_t* block_table;
+  const void* k_scale;
+  const void* k_zero;
+  const void* v_scale;
+  const void* v_zero;
+  int64_t dst_row;
+  int32_t pos;
+  int32_t len;
+} fuse_chunk_t;
+
+/* The chunk table of a call: the same n_chunks entries twice, once in host
+ * memory (validated and used to size the grid) and once in device memory
+ * (read by the kernels).  The two copies must be identical. */
+typedef struct {
+  int32_t n_chunks;
+  int32_t kv_layout;        /* fuse_kv_layout_t */
+  int32_t kv_storage;       /* fuse_dtype_t of the chunk caches */
+  int32_t block_size;       /* PAGED: tokens per pool block (> 0) */
+  int64_t n_pool_blocks;    /* PAGED: pool size in blocks, for bounds checks */
+  const fuse_chunk_t* h_chunks;   /* host   [n_chunks] */
+  const fuse_chunk_t* d_chunks;   /* device [n_chunks] */
+} fuse_chunks_t;
+
+/* One request of a batch.  fuse_plan_requests() fills these offsets for the
+ * packed layouts described at the top of this file. */
+typedef struct {
+  int64_t row0;     /* first row of the request in H, Kf, Vf            */
+  int64_t score0;   /* first entry of its N_r scores in score[]          */
+  int64_t sel0;     /* first entry of its k_r selected indices in idx[]  */
+  int64_t out0;     /* first row of its R_r = k_r + Qn_r rows in O       */
+  int32_t n_ctx;    /* N_r context tokens                                 */
+  int32_t n_query;  /* Qn_r query tokens (always recomputed, never scored) */
+  int32_t k;        /* k_r selected context tokens, 0 <= k_r <= N_r        */
+  int32_t reserved; /* must be 0 */
+} fuse_request_t;
+
+/* The request table of a call, host and device copies (identical). */
+typedef struct {
+  int32_t n_req;
+  const fuse_request_t* h_req;   /* host   [n_req] */
+  const fuse_request_t* d_req;   /* device [n_req] */
+} fuse_requests_t;
+
+/* Totals of a request table (filled by fuse_plan_requests). */
+typedef struct {
+  int64_t n_tok;    /* T_total = sum (N_r + Qn_r): rows of H, Kf, Vf */
+  int64_t n_ctx;    /* N_total: entries of score[] */
+  int64_t n_sel;    /* K_total = sum k_r: entries of idx[] */
+  int64_t n_out;    /* R_total = sum (k_r + Qn_r): rows of O */
+  int32_t max_ctx;  /* max N_r */
+  int32_t max_tok;  /* max N_r + Qn_r */
+} fuse_totals_t;
+
+/* ---------------------------------------------------------------------- */
+
+/* Number of recomputed context tokens for ratio rho = |P| / N ([QCFuse]
+ * Eq. 6): floor(rho * n_ctx + 1e-9), clamped to [0, n_ctx].  The epsilon
+ * keeps products such as 0.29 * 100 = 28.999999999999996 from losing a
+ * token.  Host function. */
+int64_t fuse_k_from_ratio(double ratio, int64_t n_ctx);
+
+/* Host helper: lay requests out back to back.  n_ctx, n_query: host arrays
+ * [n_req].  Writes out[n_req] (k_r = fuse_k_from_ratio(ratio, N_r)) and, if
+ * totals is not NULL, the totals.  Returns FUSE_ERR_INVALID_ARG on a
+ * negative size or a total beyond 2^31 - 1 rows. */
+fuse_status_t fuse_plan_requests(int32_t n_req, const int32_t* n_ctx, const int32_t* n_query,
+                                 double ratio, fuse_request_t* out, fuse_totals_t* totals);
+
+/* Workspace bytes needed by every call below for the given request table
+ * (host copy read) and layer shape.  The workspace is caller-owned device
+ * memory, 256-byte aligned, reusable across calls on one stream; it begins
+ * with the error word that fuse_check_errors() reads. */
+fuse_status_t fuse_workspace_size(const fuse_layer_desc_t* desc, const fuse_requests_t* reqs,
+                                  size_t* bytes);
+
+/* Zero the workspace's error word (enqueued on the stream). */
+fuse_status_t fuse_workspace_reset(void* ws, size_t ws_bytes, fuse_stream_t stream);
+
+/* Position remapping and stitching, [QCFuse] Eq. 4 with the RoPE correction
+ * of [KVBoost] section 3.2: for every chunk i and local row r < len_i,
+ *   Kf[dst_row_i + r] = R^{pos_i} K_i[r]     (keys re-rotated by the offset)
+ *   Vf[dst_row_i + r] = V_i[r]               (values copied in token order)
+ * after dequantisation when kv_storage is FUSE_U8_ASYM ([KVBoost] Eq. 7).
+ * A chunk with pos 0 whose storage type equals desc->dtype is copied bit for
+ * bit.  Kf, Vf: [fused_rows, Hkv, d] in desc->dtype; every chunk must satisfy
+ * dst_row + len <= fused_rows.  Query rows are not touched. */
+fuse_status_t fuse_stitch_rerotate(const fuse_layer_desc_t* desc, const fuse_chunks_t* chunks,
+                                   void* Kf, void* Vf, int64_t fused_rows,
+                                   void* ws, size_t ws_bytes, fuse_stream_t stream);
+
+/* Deviation score of every context token ([KVBoost] Alg. 2 step 2, taken on
+ * the values of one layer): with Vn = H_t W_V^T split into Hkv heads,
+ *   score_t = 1 - (1/Hkv) sum_h cos(Vn[t,h], Vf[t,h]),
+ * the cosine's denominator clamped at 1e-30.  Reads H and Vf at the context
+ * rows of each request (Vf holds the stitched cached values); writes
+ * score[score0 + t] in fp32.  Deterministic: no floating-point atomics. */
+fuse_status_t fuse_score_deviation(const fuse_layer_desc_t* desc, const fuse_requests_t* reqs,
+                                   const void* H, const void* Wv, const void* Vf, float* score,
+                                   void* ws, size_t ws_bytes, fuse_stream_t stream);
+
+/* TopK(score, k_r) per request ([QCFuse] Eq. 11; [KVBoost] Alg. 2 step 3):
+ * the k_r largest scores, ties broken toward the lower token index, -0 equal
+ * to +0, written as ascending request-local indices to idx[sel0 ..].  A NaN
+ * score is recorded as FUSE_ERR_DEVICE_BOUNDS (it ranks below every number). */
+fuse_status_t fuse_select_topk(const fuse_requests_t* reqs, const float* score, int32_t* idx,
+                               void* ws, size_t ws_bytes, fuse_stream_t stream);
+
+/* Selective recomputation, [QCFuse] Eqs. 6-7 with [KVBoost] Eqs. 1-3.  For
+ * every request and every row s of S_r = idx_r U {N_r .. T_r - 1}:
+ *   q = R^s W_Q x_s,  k = R^s W_K x_s,  v = W_V x_s     (x_s = H[row0 + s])
+ *   Kf[row0 + s] = k,  Vf[row0 + s] = v                 (scatter, Eq. 7)
+ * and, after all scatters, the causal attention row
+ *   O[s, h] = softmax_j(q_h . Kf[j, h/g] / sqrt(d)) Vf[j, h/g],  j <= s,
+ * over the fused cache (unselected j hold reused entries, selected j the
+ * refreshed ones).  idx must be ascending and < N_r (checked on the device). */
+fuse_status_t fuse_recompute_selected(const fuse_layer_desc_t* desc, const fuse_requests_t* reqs,
+                                      const void* H, const void* Wq, const void* Wk,
+                                      const void* Wv, const int32_t* idx, void* Kf, void* Vf,
+                                      void* O, void* ws, size_t ws_bytes, fuse_stream_t stream);
+
+/* One whole layer-step: fuse_stitch_rerotate, then (if score_this_layer)
+ * fuse_score_deviation and fuse_select_topk writing idx, then
+ * fuse_recompute_selected reading idx -- the order of [KVBoost] Alg. 2
+ * (probe, deviation, select, patch) on the cache of [QCFuse] Eq. 4.  With
+ * score_this_layer == 0, idx is an input (a selection made at another layer)
+ * and score is not touched (may be NULL).  Kf, Vf have reqs' T_total rows. */
+fuse_status_t fuse_layer_step(const fuse_layer_desc_t* desc, const fuse_chunks_t* chunks,
+                              const fuse_requests_t* reqs, const void* H, const void* Wq,
+                              const void* Wk, const void* Wv, int32_t score_this_layer,
+                              int32_t* idx, void* Kf, void* Vf, void* O, float* score,
+                              void* ws, size_t ws_bytes, fuse_stream_t stream);
+
+/* Position-independent chunk caches, [QCFuse] Eq. 3 with one projection layer
+ * standing in for the model: for every chunk i and local row r,
+ *   K_i[r] = R^r W_K x,  V_i[r] = W_V x,   x = H_clean[dst_row_i + r].
+ * This prepares inputs for the calls above (it is not part of a layer-step).
+ * Chunk storage must be CONTIGUOUS and equal to desc->dtype. */
+fuse_status_t fuse_pic_precompute(const fuse_layer_desc_t* desc, const fuse_chunks_t* chunks,
+                                  const void* H_clean, const void* Wk, const void* Wv,
+                                  void* ws, size_t ws_bytes, fuse_stream_t stream);
+
+/* Synchronise the stream, read the workspace's error word, clear it, and
+ * return it (FUSE_OK if no device-side error was recorded).  If detail is
+ * not NULL it receives a code locating the failed check. */
+fuse_status_t fuse_check_errors(void* ws, fuse_stream_t stream, uint32_t* detail);
+
+/* Kernel timing trace (no counterpart on the pages; a measurement aid).
+ * fuse_trace_begin(n) creates n pairs of CUDA events and, until
+ * fuse_trace_end, records one pair around each kernel the library launches,
+ * on that launch's stream; launches past n are not recorded.  fuse_trace_end
+ * waits for the recorded events and writes up to max_out entries
+ * {kernel name (static string), elapsed ms} in launch order, *n_out their
+ * count.  Host-side state: one trace at a time per process.  Do not open a
+ * trace while a stream is being captured into a CUDA graph. */
+typedef struct {
+  const char* kernel;
+  float ms;
+} fuse_trace_entry_t;
+
+fuse_status_t fuse_trace_begin(int32_t max_records);
+fuse_status_t fuse_trace_end(fuse_trace_entry_t* out, int32_t max_out, int32_t* n_out);
+
+/* A static, human-readable name of a status code. */
+const char* fuse_status_string(fuse_status_t status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t fuse_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FUSEKV_H */

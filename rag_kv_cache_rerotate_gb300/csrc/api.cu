@@ -1,0 +1,474 @@
+// The exported C ABI of libfusekv: argument validation, workspace carving,
+// and the order of launches of one layer-step (QCFuse section 2.1, Eqs.
+// 4-7; KVBoost Alg. 2: stitch, probe/deviation, select, patch).
+#include <cmath>
+#include <cstring>
+
+#include "common.cuh"
+#include "launch.h"
+#include "trace.h"
+
+namespace fusekv {
+
+// Tensor-core paths (bf16), defined in their own translation units.
+bool tc_gemm_supported(const fuse_layer_desc_t& desc);
+cudaError_t launch_deviation_partials_tc(const fuse_layer_desc_t& desc, int64_t n_rows,
+                                         const void* H, const void* Wv, const void* Vf,
+                                         const int32_t* map, float* partial, uint32_t* err,
+                                         cudaStream_t s);
+cudaError_t launch_project_recompute_tc(const fuse_layer_desc_t& desc, int64_t n_rows,
+                                        const WorkRow* rows, const float2* rope, const void* H,
+                                        const void* Wq, const void* Wk, const void* Wv, void* Q,
+                                        void* Kf, void* Vf, void* Hs, uint32_t* err, cudaStream_t s);
+bool tc_attention_supported(const fuse_layer_desc_t& desc);
+cudaError_t launch_attention_tc(const fuse_layer_desc_t& desc, int64_t n_rows, int n_req,
+                                const fuse_request_t* d_req, const WorkRow* rows, const void* Q,
+                                const void* Kf, const void* Vf, void* O, uint32_t* err,
+                                cudaStream_t s);
+
+namespace {
+
+constexpr int kMaxPosition = 1 << 24;   // positions stay exact in fp32
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t elem_size(int dtype) { return dtype == FUSE_F32 ? 4 : (dtype == FUSE_BF16 ? 2 : 1); }
+
+fuse_status_t check_desc(const fuse_layer_desc_t* d) {
+  if (!d) return FUSE_ERR_INVALID_ARG;
+  if (d->pos_encoding != FUSE_ROPE_ROTATE_HALF) return FUSE_ERR_UNSUPPORTED;
+  if (d->dtype != FUSE_F32 && d->dtype != FUSE_BF16) return FUSE_ERR_UNSUPPORTED;
+  if (d->hidden <= 0 || d->n_q_heads <= 0 || d->n_kv_heads <= 0 || d->head_dim <= 0)
+    return FUSE_ERR_INVALID_ARG;
+  if (d->n_q_heads % d->n_kv_heads != 0) return FUSE_ERR_INVALID_ARG;
+  if (d->head_dim != 64 && d->head_dim != 128) return FUSE_ERR_UNSUPPORTED;
+  const int g = d->n_q_heads / d->n_kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return FUSE_ERR_UNSUPPORTED;
+  if (d->hidden % 64 != 0) return FUSE_ERR_UNSUPPORTED;
+  if (!(d->rope_base > 1.0) || !std::isfinite(d->rope_base)) return FUSE_ERR_INVALID_ARG;
+  return FUSE_OK;
+}
+
+// theta_j / (2 pi) split into three floats (see rope_cos_sin).
+RopeFreqs make_freqs(const fuse_layer_desc_t& d) {
+  RopeFreqs f;
+  std::memset(&f, 0, sizeof(f));
+  const int h2 = d.head_dim / 2;
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int j = 0; j < h2; ++j) {
+    const double theta = std::pow(d.rope_base, -2.0 * j / (double)d.head_dim);
+    const double turns = theta / two_pi;
+    const float hi = (float)turns;
+    const float mid = (float)(turns - (double)hi);
+    const float lo = (float)(turns - (double)hi - (double)mid);
+    f.hi[j] = hi;
+    f.mid[j] = mid;
+    f.lo[j] = lo;
+  }
+  return f;
+}
+
+struct ReqInfo {
+  fuse_totals_t tot;   // extents implied by the offsets (max over requests)
+};
+
+fuse_status_t check_reqs(const fuse_requests_t* r, ReqInfo* info, bool need_device = true) {
+  if (!r || r->n_req < 0) return FUSE_ERR_INVALID_ARG;
+  std::memset(info, 0, sizeof(*info));
+  if (r->n_req == 0) return FUSE_OK;
+  if (!r->h_req || (need_device && !r->d_req)) return FUSE_ERR_INVALID_ARG;
+  fuse_totals_t& t = info->tot;
+  for (int i = 0; i < r->n_req; ++i) {
+    const fuse_request_t& q = r->h_req[i];
+    if (q.n_ctx < 0 || q.n_query < 0 || q.k < 0 || q.k > q.n_ctx || q.reserved != 0)
+      return FUSE_ERR_INVALID_ARG;
+    if (q.row0 < 0 || q.score0 < 0 || q.sel0 < 0 || q.out0 < 0) return FUSE_ERR_INVALID_ARG;
+    const int64_t T = (int64_t)q.n_ctx + q.n_query;
+    if (T > kMaxPosition) return FUSE_ERR_UNSUPPORTED;
+    t.n_tok = std::max<int64_t>(t.n_tok, q.row0 + T);
+    t.n_ctx = std::max<int64_t>(t.n_ctx, q.score0 + q.n_ctx);
+    t.n_sel = std::max<int64_t>(t.n_sel, q.sel0 + q.k);
+    t.n_out = std::max<int64_t>(t.n_out, q.out0 + q.k + q.n_query);
+    t.max_ctx = std::max<int32_t>(t.max_ctx, q.n_ctx);
+    t.max_tok = std::max<int32_t>(t.max_tok, (int32_t)T);
+  }
+  if (t.n_tok > INT32_MAX) return FUSE_ERR_UNSUPPORTED;
+  return FUSE_OK;
+}
+
+fuse_status_t check_chunks(const fuse_layer_desc_t& d, const fuse_chunks_t* c, int64_t fused_rows,
+                           int* max_len) {
+  if (!c || c->n_chunks < 0) return FUSE_ERR_INVALID_ARG;
+  *max_len = 0;
+  if (c->kv_layout != FUSE_KV_CONTIGUOUS && c->kv_layout != FUSE_KV_PAGED)
+    return FUSE_ERR_INVALID_ARG;
+  if (c->kv_storage != FUSE_F32 && c->kv_storage != FUSE_BF16 && c->kv_storage != FUSE_U8_ASYM)
+    return FUSE_ERR_INVALID_ARG;
+  const bool paged = c->kv_layout == FUSE_KV_PAGED;
+  const bool u8 = c->kv_storage == FUSE_U8_ASYM;
+  if (paged && (c->block_size <= 0 || c->n_pool_blocks <= 0)) return FUSE_ERR_INVALID_ARG;
+  if (c->n_chunks == 0) return FUSE_OK;
+  if (!c->h_chunks || !c->d_chunks) return FUSE_ERR_INVALID_ARG;
+  for (int i = 0; i < c->n_chunks; ++i) {
+    const fuse_chunk_t& q = c->h_chunks[i];
+    if (q.len < 0 || q.pos < 0 || q.dst_row < 0) return FUSE_ERR_INVALID_ARG;
+    if ((int64_t)q.pos + q.len > kMaxPosition) return FUSE_ERR_UNSUPPORTED;
+    if (q.dst_row + q.len > fused_rows) return FUSE_ERR_INVALID_ARG;
+    *max_len = std::max(*max_len, q.len);
+    if (q.len == 0) continue;
+    if (!q.k || !q.v) return FUSE_ERR_INVALID_ARG;
+    if (!aligned16(q.k) || !aligned16(q.v)) return FUSE_ERR_MISALIGNED;
+    if (paged && !q.block_table) return FUSE_ERR_INVALID_ARG;
+    if (u8) {
+      if (!q.k_scale || !q.k_zero || !q.v_scale || !q.v_zero) return FUSE_ERR_INVALID_ARG;
+      if (!aligned16(q.k_scale) || !aligned16(q.k_zero)) return FUSE_ERR_MISALIGNED;
+      if ((reinterpret_cast<uintptr_t>(q.v_scale) | reinterpret_cast<uintptr_t>(q.v_zero)) & 1u)
+        return FUSE_ERR_MISALIGNED;
+    }
+  }
+  (void)d;
+  return FUSE_OK;
+}
+
+// Workspace regions (each 256-byte aligned).
+struct WsLayout {
+  size_t partial, keys, map, rows, rope, q, hs, total;
+};
+
+WsLayout ws_layout(const fuse_layer_desc_t& d, const fuse_totals_t& t) {
+  WsLayout L;
+  size_t off = sizeof(WsHeader);
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  const size_t es = elem_size(d.dtype);
+  L.keys = take((size_t)t.n_ctx * sizeof(uint32_t));          // first: top-k needs only this
+  L.partial = take((size_t)t.n_ctx * d.n_kv_heads * sizeof(float));
+  L.map = take((size_t)t.n_tok * sizeof(int32_t));
+  L.rows = take((size_t)t.n_out * sizeof(WorkRow));
+  L.rope = take((size_t)t.n_out * (d.head_dim / 2) * sizeof(float2));
+  L.q = take((size_t)t.n_out * d.n_q_heads * d.head_dim * es);
+  L.hs = take((size_t)t.n_out * d.hidden * es);
+  L.total = off;
+  return L;
+}
+
+template <typename T> T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(reinterpret_cast<char*>(ws) + off);
+}
+
+fuse_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? FUSE_OK : FUSE_ERR_CUDA; }
+
+fuse_status_t check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (!ws) return FUSE_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return FUSE_ERR_MISALIGNED;
+  if (ws_bytes < need) return FUSE_ERR_WORKSPACE;
+  return FUSE_OK;
+}
+
+// ---- the steps (validated arguments) ------------------------------------
+
+fuse_status_t do_stitch(const fuse_layer_desc_t& d, const fuse_chunks_t& c, int max_len, void* Kf,
+                        void* Vf, void* ws, cudaStream_t s) {
+  if (c.n_chunks == 0 || max_len == 0) return FUSE_OK;
+  const RopeFreqs f = make_freqs(d);
+  return cuda_status(traced("stitch_rerotate", s, [&] {
+    return launch_stitch(d, c, f, max_len, Kf, Vf, at<uint32_t>(ws, 0), s);
+  }));
+}
+
+fuse_status_t do_score(const fuse_layer_desc_t& d, const fuse_requests_t& r, const ReqInfo& info,
+                       const void* H, const void* Wv, const void* Vf, float* score, void* ws,
+                       cudaStream_t s) {
+  const WsLayout L = ws_layout(d, info.tot);
+  if (info.tot.n_ctx == 0) return FUSE_OK;
+  int32_t* map = at<int32_t>(ws, L.map);
+  float* partial = at<float>(ws, L.partial);
+  cudaError_t e = cudaMemsetAsync(map, 0xFF, (size_t)info.tot.n_tok * sizeof(int32_t), s);
+  if (e == cudaSuccess)
+    e = traced("score_map", s, [&] { return launch_build_score_map(r, info.tot.max_tok, map, s); });
+  if (e == cudaSuccess) {
+    if (tc_gemm_supported(d))
+      e = traced("deviation_gemm_tc", s, [&] {
+        return launch_deviation_partials_tc(d, info.tot.n_tok, H, Wv, Vf, map, partial,
+                                            at<uint32_t>(ws, 0), s);
+      });
+    else
+      e = traced("deviation_gemm_simt", s, [&] {
+        return launch_deviation_partials_simt(d, info.tot.n_tok, H, Wv, Vf, map, partial,
+                                              at<uint32_t>(ws, 0), s);
+      });
+  }
+  if (e == cudaSuccess)
+    e = traced("deviation_reduce", s, [&] {
+      return launch_deviation_reduce(info.tot.n_ctx, d.n_kv_heads, partial, score, s);
+    });
+  return cuda_status(e);
+}
+
+fuse_status_t do_topk(const fuse_layer_desc_t& d, const fuse_requests_t& r, const ReqInfo& info,
+                      const float* score, int32_t* idx, void* ws, cudaStream_t s) {
+  const WsLayout L = ws_layout(d, info.tot);
+  if (info.tot.n_sel == 0) return FUSE_OK;
+  return cuda_status(traced("topk", s, [&] {
+    return launch_topk(r, info.tot.max_ctx, score, idx, at<uint32_t>(ws, L.keys),
+                       at<uint32_t>(ws, 0), s);
+  }));
+}
+
+fuse_status_t do_recompute(const fuse_layer_desc_t& d, const fuse_requests_t& r,
+                           const ReqInfo& info, const void* H, const void* Wq, const void* Wk,
+                           const void* Wv, const int32_t* idx, void* Kf, void* Vf, void* O,
+                           void* ws, cudaStream_t s) {
+  const WsLayout L = ws_layout(d, info.tot);
+  const int64_t R = info.tot.n_out;
+  if (R == 0) return FUSE_OK;
+  int max_rows = 0;
+  for (int i = 0; i < r.n_req; ++i)
+    max_rows = std::max(max_rows, r.h_req[i].k + r.h_req[i].n_query);
+  WorkRow* rows = at<WorkRow>(ws, L.rows);
+  float2* rope = at<float2>(ws, L.rope);
+  void* Q = at<void>(ws, L.q);
+  uint32_t* err = at<uint32_t>(ws, 0);
+  const RopeFreqs f = make_freqs(d);
+  cudaError_t e = traced("sel_rows", s, [&] {
+    return launch_build_sel_rows(r, max_rows, idx, f, d.head_dim, rows, rope, err, s);
+  });
+  if (e != cudaSuccess) return FUSE_ERR_CUDA;
+  if (tc_gemm_supported(d))
+    e = traced("qkv_gemm_tc", s, [&] {
+      return launch_project_recompute_tc(d, R, rows, rope, H, Wq, Wk, Wv, Q, Kf, Vf,
+                                         at<void>(ws, L.hs), err, s);
+    });
+  else
+    e = traced("qkv_gemm_simt", s, [&] {
+      return launch_project_recompute_simt(d, R, rows, rope, H, Wq, Wk, Wv, Q, Kf, Vf, err, s);
+    });
+  if (e != cudaSuccess) return FUSE_ERR_CUDA;
+  if (tc_attention_supported(d))
+    e = traced("attention_tc", s, [&] {
+      return launch_attention_tc(d, R, r.n_req, r.d_req, rows, Q, Kf, Vf, O, err, s);
+    });
+  else
+    e = traced("attention_simt", s, [&] { return launch_attention_simt(d, R, rows, Q, Kf, Vf, O, s); });
+  return cuda_status(e);
+}
+
+}  // namespace
+}  // namespace fusekv
+
+using namespace fusekv;
+
+extern "C" {
+
+int64_t fuse_k_from_ratio(double ratio, int64_t n_ctx) {
+  if (n_ctx <= 0 || !(ratio > 0.0)) return 0;
+  const double v = std::floor(ratio * (double)n_ctx + 1e-9);
+  if (v >= (double)n_ctx) return n_ctx;
+  return (int64_t)v;
+}
+
+fuse_status_t fuse_plan_requests(int32_t n_req, const int32_t* n_ctx, const int32_t* n_query,
+                                 double ratio, fuse_request_t* out, fuse_totals_t* totals) {
+  if (n_req < 0 || (n_req > 0 && (!n_ctx || !n_query || !out))) return FUSE_ERR_INVALID_ARG;
+  fuse_totals_t t;
+  std::memset(&t, 0, sizeof(t));
+  for (int i = 0; i < n_req; ++i) {
+    if (n_ctx[i] < 0 || n_query[i] < 0) return FUSE_ERR_INVALID_ARG;
+    fuse_request_t q;
+    std::memset(&q, 0, sizeof(q));
+    q.row0 = t.n_tok;
+    q.score0 = t.n_ctx;
+    q.sel0 = t.n_sel;
+    q.out0 = t.n_out;
+    q.n_ctx = n_ctx[i];
+    q.n_query = n_query[i];
+    q.k = (int32_t)fuse_k_from_ratio(ratio, n_ctx[i]);
+    out[i] = q;
+    t.n_tok += (int64_t)n_ctx[i] + n_query[i];
+    t.n_ctx += n_ctx[i];
+    t.n_sel += q.k;
+    t.n_out += (int64_t)q.k + n_query[i];
+    t.max_ctx = std::max(t.max_ctx, n_ctx[i]);
+    t.max_tok = std::max<int32_t>(t.max_tok, n_ctx[i] + n_query[i]);
+  }
+  if (t.n_tok > INT32_MAX) return FUSE_ERR_INVALID_ARG;
+  if (totals) *totals = t;
+  return FUSE_OK;
+}
+
+fuse_status_t fuse_workspace_size(const fuse_layer_desc_t* desc, const fuse_requests_t* reqs,
+                                  size_t* bytes) {
+  fuse_status_t st = check_desc(desc);
+  if (st != FUSE_OK) return st;
+  if (!bytes) return FUSE_ERR_INVALID_ARG;
+  ReqInfo info;
+  st = check_reqs(reqs, &info, /*need_device=*/false);
+  if (st != FUSE_OK) return st;
+  *bytes = ws_layout(*desc, info.tot).total;
+  return FUSE_OK;
+}
+
+fuse_status_t fuse_workspace_reset(void* ws, size_t ws_bytes, fuse_stream_t stream) {
+  if (!ws || ws_bytes < sizeof(WsHeader)) return FUSE_ERR_WORKSPACE;
+  return cuda_status(cudaMemsetAsync(ws, 0, 8, (cudaStream_t)stream));
+}
+
+fuse_status_t fuse_stitch_rerotate(const fuse_layer_desc_t* desc, const fuse_chunks_t* chunks,
+                                   void* Kf, void* Vf, int64_t fused_rows, void* ws,
+                                   size_t ws_bytes, fuse_stream_t stream) {
+  fuse_status_t st = check_desc(desc);
+  if (st != FUSE_OK) return st;
+  int max_len;
+  st = check_chunks(*desc, chunks, fused_rows, &max_len);
+  if (st != FUSE_OK) return st;
+  if (fused_rows < 0) return FUSE_ERR_INVALID_ARG;
+  if (fused_rows > 0 && (!Kf || !Vf)) return FUSE_ERR_INVALID_ARG;
+  if (!aligned16(Kf) || !aligned16(Vf)) return FUSE_ERR_MISALIGNED;
+  st = check_ws(ws, ws_bytes, sizeof(WsHeader));
+  if (st != FUSE_OK) return st;
+  return do_stitch(*desc, *chunks, max_len, Kf, Vf, ws, (cudaStream_t)stream);
+}
+
+fuse_status_t fuse_score_deviation(const fuse_layer_desc_t* desc, const fuse_requests_t* reqs,
+                                   const void* H, const void* Wv, const void* Vf, float* score,
+                                   void* ws, size_t ws_bytes, fuse_stream_t stream) {
+  fuse_status_t st = check_desc(desc);
+  if (st != FUSE_OK) return st;
+  ReqInfo info;
+  st = check_reqs(reqs, &info);
+  if (st != FUSE_OK) return st;
+  if (info.tot.n_ctx > 0 && (!H || !Wv || !Vf || !score)) return FUSE_ERR_INVALID_ARG;
+  if (!aligned16(H) || !aligned16(Wv) || !aligned16(Vf) || !aligned16(score))
+    return FUSE_ERR_MISALIGNED;
+  st = check_ws(ws, ws_bytes, ws_layout(*desc, info.tot).total);
+  if (st != FUSE_OK) return st;
+  return do_score(*desc, *reqs, info, H, Wv, Vf, score, ws, (cudaStream_t)stream);
+}
+
+fuse_status_t fuse_select_topk(const fuse_requests_t* reqs, const float* score, int32_t* idx,
+                               void* ws, size_t ws_bytes, fuse_stream_t stream) {
+  ReqInfo info;
+  fuse_status_t st = check_reqs(reqs, &info);
+  if (st != FUSE_OK) return st;
+  if (info.tot.n_sel > 0 && (!score || !idx)) return FUSE_ERR_INVALID_ARG;
+  // the top-k needs only the header and the key buffer (N_total words), the
+  // first region of every workspace layout
+  const size_t keys_at = sizeof(WsHeader);
+  st = check_ws(ws, ws_bytes, keys_at + (size_t)info.tot.n_ctx * sizeof(uint32_t));
+  if (st != FUSE_OK) return st;
+  if (info.tot.n_sel == 0) return FUSE_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  return cuda_status(traced("topk", s, [&] {
+    return launch_topk(*reqs, info.tot.max_ctx, score, idx, at<uint32_t>(ws, keys_at),
+                       at<uint32_t>(ws, 0), s);
+  }));
+}
+
+fuse_status_t fuse_recompute_selected(const fuse_layer_desc_t* desc, const fuse_requests_t* reqs,
+                                      const void* H, const void* Wq, const void* Wk,
+                                      const void* Wv, const int32_t* idx, void* Kf, void* Vf,
+                                      void* O, void* ws, size_t ws_bytes, fuse_stream_t stream) {
+  fuse_status_t st = check_desc(desc);
+  if (st != FUSE_OK) return st;
+  ReqInfo info;
+  st = check_reqs(reqs, &info);
+  if (st != FUSE_OK) return st;
+  if (info.tot.n_out > 0 && (!H || !Wq || !Wk || !Wv || !Kf || !Vf || !O))
+    return FUSE_ERR_INVALID_ARG;
+  if (info.tot.n_sel > 0 && !idx) return FUSE_ERR_INVALID_ARG;
+  if (!aligned16(H) || !aligned16(Wq) || !aligned16(Wk) || !aligned16(Wv) || !aligned16(Kf) ||
+      !aligned16(Vf) || !aligned16(O))
+    return FUSE_ERR_MISALIGNED;
+  st = check_ws(ws, ws_bytes, ws_layout(*desc, info.tot).total);
+  if (st != FUSE_OK) return st;
+  return do_recompute(*desc, *reqs, info, H, Wq, Wk, Wv, idx, Kf, Vf, O, ws, (cudaStream_t)stream);
+}
+
+fuse_status_t fuse_layer_step(const fuse_layer_desc_t* desc, const fuse_chunks_t* chunks,
+                              const fuse_requests_t* reqs, const void* H, const void* Wq,
+                              const void* Wk, const void* Wv, int32_t score_this_layer,
+                              int32_t* idx, void* Kf, void* Vf, void* O, float* score, void* ws,
+                              size_t ws_bytes, fuse_stream_t stream) {
+  fuse_status_t st = check_desc(desc);
+  if (st != FUSE_OK) return st;
+  ReqInfo info;
+  st = check_reqs(reqs, &info);
+  if (st != FUSE_OK) return st;
+  int max_len;
+  st = check_chunks(*desc, chunks, info.tot.n_tok, &max_len);
+  if (st != FUSE_OK) return st;
+  if (info.tot.n_out > 0 && (!H || !Wq || !Wk || !Wv || !Kf || !Vf || !O))
+    return FUSE_ERR_INVALID_ARG;
+  if (info.tot.n_sel > 0 && !idx) return FUSE_ERR_INVALID_ARG;
+  if (score_this_layer && info.tot.n_ctx > 0 && !score) return FUSE_ERR_INVALID_ARG;
+  if (!aligned16(H) || !aligned16(Wq) || !aligned16(Wk) || !aligned16(Wv) || !aligned16(Kf) ||
+      !aligned16(Vf) || !aligned16(O) || !aligned16(score))
+    return FUSE_ERR_MISALIGNED;
+  st = check_ws(ws, ws_bytes, ws_layout(*desc, info.tot).total);
+  if (st != FUSE_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  st = do_stitch(*desc, *chunks, max_len, Kf, Vf, ws, s);
+  if (st != FUSE_OK) return st;
+  if (score_this_layer) {
+    st = do_score(*desc, *reqs, info, H, Wv, Vf, score, ws, s);
+    if (st != FUSE_OK) return st;
+    st = do_topk(*desc, *reqs, info, score, idx, ws, s);
+    if (st != FUSE_OK) return st;
+  }
+  return do_recompute(*desc, *reqs, info, H, Wq, Wk, Wv, idx, Kf, Vf, O, ws, s);
+}
+
+fuse_status_t fuse_pic_precompute(const fuse_layer_desc_t* desc, const fuse_chunks_t* chunks,
+                                  const void* H_clean, const void* Wk, const void* Wv, void* ws,
+                                  size_t ws_bytes, fuse_stream_t stream) {
+  fuse_status_t st = check_desc(desc);
+  if (st != FUSE_OK) return st;
+  if (!chunks) return FUSE_ERR_INVALID_ARG;
+  if (chunks->kv_layout != FUSE_KV_CONTIGUOUS || chunks->kv_storage != desc->dtype)
+    return FUSE_ERR_UNSUPPORTED;
+  int max_len;
+  st = check_chunks(*desc, chunks, INT64_MAX / 2, &max_len);
+  if (st != FUSE_OK) return st;
+  if (chunks->n_chunks > 0 && (!H_clean || !Wk || !Wv)) return FUSE_ERR_INVALID_ARG;
+  if (!aligned16(H_clean) || !aligned16(Wk) || !aligned16(Wv)) return FUSE_ERR_MISALIGNED;
+  st = check_ws(ws, ws_bytes, sizeof(WsHeader));
+  if (st != FUSE_OK) return st;
+  if (chunks->n_chunks == 0 || max_len == 0) return FUSE_OK;
+  const RopeFreqs f = make_freqs(*desc);
+  cudaStream_t s = (cudaStream_t)stream;
+  return cuda_status(traced("pic_precompute", s, [&] {
+    return launch_project_pic(*desc, chunks->n_chunks, max_len, f, H_clean, Wk, Wv,
+                              chunks->d_chunks, at<uint32_t>(ws, 0), s);
+  }));
+}
+
+fuse_status_t fuse_check_errors(void* ws, fuse_stream_t stream, uint32_t* detail) {
+  if (!ws) return FUSE_ERR_WORKSPACE;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return FUSE_ERR_CUDA;
+  uint32_t h[2] = {0, 0};
+  if (cudaMemcpy(h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return FUSE_ERR_CUDA;
+  if (detail) *detail = h[1];
+  if (h[0] != 0 && cudaMemset(ws, 0, sizeof(h)) != cudaSuccess) return FUSE_ERR_CUDA;
+  return (fuse_status_t)h[0];
+}
+
+const char* fuse_status_string(fuse_status_t s) {
+  switch (s) {
+    case FUSE_OK: return "ok";
+    case FUSE_ERR_INVALID_ARG: return "invalid argument";
+    case FUSE_ERR_MISALIGNED: return "pointer or stride not aligned";
+    case FUSE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FUSE_ERR_WORKSPACE: return "workspace missing or too small";
+    case FUSE_ERR_CUDA: return "CUDA error";
+    case FUSE_ERR_TIMEOUT: return "device wait timed out";
+    case FUSE_ERR_DEVICE_BOUNDS: return "device-detected index out of range or order";
+  }
+  return "unknown status";
+}
+
+int32_t fuse_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,128 @@
+// Shared device helpers of libfusekv: error word, element loads/stores,
+// RoPE angles, the workspace header.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fusekv.h"
+
+namespace fusekv {
+
+// ----------------------------------------------------------------------------
+// Workspace header: the first 256 bytes of every workspace.
+// ----------------------------------------------------------------------------
+struct WsHeader {
+  uint32_t err_code;     // first device-detected fuse_status_t, 0 if none
+  uint32_t err_detail;   // where it was detected (see ErrSite)
+  uint32_t pad[62];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+// Sites that record a device error (err_detail = site << 24 | low bits of an index).
+enum ErrSite : uint32_t {
+  SITE_STITCH_BLOCK = 1,     // paged block id outside the pool
+  SITE_STITCH_ROWS = 2,      // chunk rows outside the fused cache
+  SITE_SEL_RANGE = 3,        // selected index >= N_r or < 0
+  SITE_SEL_ORDER = 4,        // selected indices not strictly ascending
+  SITE_TOPK_NAN = 5,         // NaN score
+  SITE_GEMM_TIMEOUT = 6,     // tensor-core pipeline wait gave up
+  SITE_ATTN_TIMEOUT = 7,     // attention pipeline wait gave up
+  SITE_STITCH_TIMEOUT = 8,   // stitch bulk-copy wait gave up
+};
+
+__device__ __forceinline__ void report_error(uint32_t* err, fuse_status_t code, uint32_t site,
+                                             uint32_t info) {
+  if (atomicCAS(err, 0u, (uint32_t)code) == 0u) {
+    err[1] = (site << 24) | (info & 0xFFFFFFu);
+  }
+}
+
+// ----------------------------------------------------------------------------
+// Element types
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 8 consecutive elements -> fp32.
+template <typename T> struct Vec8;
+
+template <> struct Vec8<float> {
+  static __device__ __forceinline__ void load(const float* p, float (&x)[8]) {
+    float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  }
+  static __device__ __forceinline__ void store(float* p, const float (&x)[8]) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
+  }
+};
+
+template <> struct Vec8<__nv_bfloat16> {
+  static __device__ __forceinline__ void load(const __nv_bfloat16* p, float (&x)[8]) {
+    uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+    x[0] = bf16_lo(a.x); x[1] = bf16_hi(a.x); x[2] = bf16_lo(a.y); x[3] = bf16_hi(a.y);
+    x[4] = bf16_lo(a.z); x[5] = bf16_hi(a.z); x[6] = bf16_lo(a.w); x[7] = bf16_hi(a.w);
+  }
+  static __device__ __forceinline__ void store(__nv_bfloat16* p, const float (&x)[8]) {
+    uint4 a;
+    a.x = pack_bf16x2(x[0], x[1]); a.y = pack_bf16x2(x[2], x[3]);
+    a.z = pack_bf16x2(x[4], x[5]); a.w = pack_bf16x2(x[6], x[7]);
+    *reinterpret_cast<uint4*>(p) = a;
+  }
+};
+
+// ----------------------------------------------------------------------------
+// RoPE angles in fp32 without losing the large-position accuracy.
+//
+// The rotation angle of pair j at position p is p * theta_j radians, i.e.
+// p * f_j turns with f_j = theta_j / (2 pi).  f_j is split on the host (in
+// fp64) into three floats hi + mid + lo.  The fractional part of p * f_j is
+// then formed with Cody and Waite's additive reduction against a multi-word
+// constant, using the FMA-exact product error (Dekker's two-product) for the
+// leading term:
+//   a = p * hi,  e = fma(p, hi, -a)   (a + e == p * hi exactly)
+//   t = (a - rint(a)) + (e + p * mid + p * lo),  t -= rint(t)
+// so |t| <= 1/2 turn with an absolute error near 2^-25 turn for p < 2^24.
+// sincospif(2 t) then gives cos and sin of the angle.
+// ----------------------------------------------------------------------------
+constexpr int kMaxHalfDim = 64;   // head_dim <= 128
+
+struct RopeFreqs {
+  float hi[kMaxHalfDim];
+  float mid[kMaxHalfDim];
+  float lo[kMaxHalfDim];
+};
+
+__device__ __forceinline__ void rope_cos_sin(int p, float hi, float mid, float lo, float& c,
+                                             float& s) {
+  const float fp = (float)p;
+  const float a = fp * hi;
+  const float e = fmaf(fp, hi, -a);
+  float t = (a - rintf(a)) + (e + fmaf(fp, mid, fp * lo));
+  t -= rintf(t);
+  sincospif(2.0f * t, &s, &c);
+}
+
+// ----------------------------------------------------------------------------
+// Per-row work item of the gathered GEMMs and the attention kernel.
+// ----------------------------------------------------------------------------
+struct WorkRow {
+  int64_t a_row;     // row of H (or H_clean) feeding the projection
+  int64_t dst_row;   // fused-cache row (recompute) or chunk-local row (PIC)
+  int32_t pos;       // RoPE position p
+  int32_t aux;       // request (recompute) or chunk (PIC) index
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace fusekv

@@ -1,0 +1,54 @@
+// Launchers of the kernels of libfusekv (host side, called by api.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace fusekv {
+
+// Stitch + re-rotate (+ dequantise, + paged gather) every chunk.
+cudaError_t launch_stitch(const fuse_layer_desc_t& desc, const fuse_chunks_t& chunks,
+                          const RopeFreqs& freqs, int max_len, void* Kf, void* Vf, uint32_t* err,
+                          cudaStream_t s);
+
+// Score slot of every packed row: score0 + t for context rows, -1 for query rows.
+cudaError_t launch_build_score_map(const fuse_requests_t& reqs, int max_tok, int32_t* map,
+                                   cudaStream_t s);
+
+// Work rows (and their RoPE table) of S_r = idx_r U query rows, per request.
+cudaError_t launch_build_sel_rows(const fuse_requests_t& reqs, int max_rows, const int32_t* idx,
+                                  const RopeFreqs& freqs, int head_dim, WorkRow* rows,
+                                  float2* rope, uint32_t* err, cudaStream_t s);
+
+// Deviation: partial[slot, h] = cos(H_t W_V^T [h], Vf[t, h]) over all packed rows.
+cudaError_t launch_deviation_partials_simt(const fuse_layer_desc_t& desc, int64_t n_rows, const void* H,
+                                      const void* Wv, const void* Vf, const int32_t* map,
+                                      float* partial, uint32_t* err, cudaStream_t s);
+
+// score[i] = 1 - mean_h partial[i, h].
+cudaError_t launch_deviation_reduce(int64_t n_ctx, int n_kv_heads, const float* partial,
+                                    float* score, cudaStream_t s);
+
+// Top-k per request, ascending indices.
+cudaError_t launch_topk(const fuse_requests_t& reqs, int max_ctx, const float* score, int32_t* idx,
+                        uint32_t* keys_ws, uint32_t* err, cudaStream_t s);
+
+// Gathered projection of work rows with RoPE and scatter (recompute: Q | K | V).
+cudaError_t launch_project_recompute_simt(const fuse_layer_desc_t& desc, int64_t n_rows,
+                                          const WorkRow* rows, const float2* rope, const void* H,
+                                          const void* Wq, const void* Wk, const void* Wv, void* Q,
+                                          void* Kf, void* Vf, uint32_t* err, cudaStream_t s);
+
+// Projection of chunk tokens into the chunk caches (PIC: K | V), RoPE at the
+// chunk-local position.
+cudaError_t launch_project_pic(const fuse_layer_desc_t& desc, int n_chunks, int max_len,
+                               const RopeFreqs& freqs, const void* H, const void* Wk, const void* Wv,
+                               const fuse_chunk_t* d_chunks, uint32_t* err, cudaStream_t s);
+
+// Causal GQA attention of the work rows over the fused cache.
+cudaError_t launch_attention_simt(const fuse_layer_desc_t& desc, int64_t n_rows, const WorkRow* rows,
+                                  const void* Q, const void* Kf, const void* Vf, void* O,
+                                  cudaStream_t s);
+
+}  // namespace fusekv

@@ -1,0 +1,166 @@
+// Top-k selection per request: TopK(score, k) of QCFuse (Eq. 11) and step 3
+// of KVBoost's CacheBlendRecompute (Alg. 2).
+//
+// Scores become order-preserving 32-bit keys (-0 folded onto +0, NaN below
+// every number and reported).  A block-wide radix select finds the k-th
+// largest key tau in four 8-bit rounds; then one pass in index order keeps
+// every key above tau and the lowest-indexed keys equal to tau, so ties go
+// to the lower index and the output is already ascending.  Exact integer
+// work: the result is unique given the score array.
+#include "common.cuh"
+#include "launch.h"
+
+namespace fusekv {
+
+namespace {
+
+constexpr int kTopkThreads = 1024;
+constexpr int kTopkSmemKeys = 40 * 1024;   // keys kept in shared memory (160 KB)
+
+__device__ __forceinline__ uint32_t float_key(float f, bool* is_nan) {
+  uint32_t b = __float_as_uint(f);
+  *is_nan = (b & 0x7FFFFFFFu) > 0x7F800000u;
+  if (*is_nan) return 0u;
+  if (b == 0x80000000u) b = 0u;                       // -0 -> +0
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// Exclusive block-wide scan of one value per thread; also returns the total.
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_buf,
+                                                         uint32_t* total) {
+  const int lane = threadIdx.x % 32;
+  const int warp = threadIdx.x / 32;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_buf[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t w = lane < (int)(blockDim.x / 32) ? warp_buf[lane] : 0u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_buf[lane] = w;   // inclusive prefix over warps
+  }
+  __syncthreads();
+  const uint32_t before = (warp > 0 ? warp_buf[warp - 1] : 0u) + x - v;
+  *total = warp_buf[blockDim.x / 32 - 1];
+  __syncthreads();
+  return before;
+}
+
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const fuse_request_t* reqs,
+                                                            const float* score, int32_t* idx,
+                                                            uint32_t* keys_ws, uint32_t* err,
+                                                            int keys_in_smem) {
+  extern __shared__ uint32_t dyn[];
+  __shared__ uint32_t hist[256];
+  __shared__ uint32_t warp_buf[32];
+  __shared__ uint32_t sel_digit, sel_remaining;
+  const int r = blockIdx.x;
+  const fuse_request_t R = reqs[r];
+  const int n = R.n_ctx;
+  const int k = R.k;
+  if (k <= 0 || n <= 0) return;
+  const int t = threadIdx.x;
+  uint32_t* keys = keys_in_smem ? dyn : keys_ws + R.score0;
+
+  bool nan_seen = false;
+  for (int i = t; i < n; i += kTopkThreads) {
+    bool nn;
+    keys[i] = float_key(score[R.score0 + i], &nn);
+    nan_seen |= nn;
+  }
+  if (nan_seen) report_error(err, FUSE_ERR_DEVICE_BOUNDS, SITE_TOPK_NAN, r);
+  __syncthreads();
+
+  uint32_t prefix = 0, mask = 0, remaining = (uint32_t)k;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int b = t; b < 256; b += kTopkThreads) hist[b] = 0u;
+    __syncthreads();
+    for (int i = t; i < n; i += kTopkThreads) {
+      const uint32_t key = keys[i];
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 0xFFu], 1u);
+    }
+    __syncthreads();
+    if (t < 32) {
+      // warp 0: scan the 256 bins from the top, 8 bins per lane
+      uint32_t c[8], lsum = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        c[q] = hist[255 - (t * 8 + q)];
+        lsum += c[q];
+      }
+      uint32_t incl = lsum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (t >= o) incl += y;
+      }
+      uint32_t cum = incl - lsum;   // count in bins above this lane's first bin
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (cum < remaining && cum + c[q] >= remaining) {
+          sel_digit = 255 - (t * 8 + q);
+          sel_remaining = remaining - cum;
+        }
+        cum += c[q];
+      }
+    }
+    __syncthreads();
+    prefix |= sel_digit << shift;
+    mask |= 0xFFu << shift;
+    remaining = sel_remaining;
+    __syncthreads();
+  }
+  const uint32_t tau = prefix;
+  const uint32_t need_eq = remaining;
+
+  // compaction in index order: thread t owns indices [i0, i1)
+  const int per = (n + kTopkThreads - 1) / kTopkThreads;
+  const int i0 = min(n, t * per);
+  const int i1 = min(n, i0 + per);
+  uint32_t n_gt = 0, n_eq = 0;
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t key = keys[i];
+    n_gt += key > tau;
+    n_eq += key == tau;
+  }
+  uint32_t tot;
+  const uint32_t eq_before = block_exclusive_scan(n_eq, warp_buf, &tot);
+  const uint32_t take_eq = eq_before >= need_eq ? 0u : min(n_eq, need_eq - eq_before);
+  const uint32_t out_before = block_exclusive_scan(n_gt + take_eq, warp_buf, &tot);
+  int32_t* out = idx + R.sel0;
+  uint32_t o = out_before, eq_taken = 0;
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t key = keys[i];
+    if (key > tau || (key == tau && eq_taken < take_eq)) {
+      eq_taken += key == tau;
+      if (o < (uint32_t)k) out[o] = i;
+      ++o;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_topk(const fuse_requests_t& reqs, int max_ctx, const float* score, int32_t* idx,
+                        uint32_t* keys_ws, uint32_t* err, cudaStream_t s) {
+  if (reqs.n_req == 0) return cudaSuccess;
+  const int in_smem = max_ctx <= kTopkSmemKeys;
+  const size_t smem = in_smem ? (size_t)max_ctx * sizeof(uint32_t) : 0;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kTopkSmemKeys * (int)sizeof(uint32_t));
+    if (e != cudaSuccess) return e;
+  }
+  topk_kernel<<<reqs.n_req, kTopkThreads, smem, s>>>(reqs.d_req, score, idx, keys_ws, err, in_smem);
+  return cudaGetLastError();
+}
+
+}  // namespace fusekv

@@ -1,0 +1,137 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+header declares, and its host-side logic (k from ratio, request planning,
+workspace sizing, argument validation) behaves as documented.  No call here
+reaches a kernel launch."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def fk():
+    from rag_kv_cache_rerotate_gb300 import _build, fusekv
+    _build.build()
+    fusekv.load()
+    return fusekv
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "fusekv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fuse_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(fk):
+    names = _declared()
+    assert "fuse_layer_step" in names and len(names) >= 13
+    lib = fk.load()
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_k_from_ratio_host(fk):
+    assert fk.k_from_ratio(0.30, 256) == 76
+    assert fk.k_from_ratio(0.15, 4096) == 614
+    assert fk.k_from_ratio(0.29, 100) == 29
+    assert fk.k_from_ratio(0.0, 10) == 0 and fk.k_from_ratio(1.0, 10) == 10
+    assert fk.k_from_ratio(2.0, 10) == 10 and fk.k_from_ratio(-1.0, 10) == 0
+    assert fk.k_from_ratio(float("nan"), 10) == 0
+
+
+def test_plan_requests_offsets(fk):
+    t = fk.plan_requests([100, 0, 37], [5, 3, 0], 0.2, device=None)
+    r = [t[i] for i in range(3)]
+    assert [x.row0 for x in r] == [0, 105, 108]
+    assert [x.score0 for x in r] == [0, 100, 100]
+    assert [x.k for x in r] == [20, 0, 7]
+    assert [x.sel0 for x in r] == [0, 20, 20]
+    assert [x.out0 for x in r] == [0, 25, 28]
+    tot = t.totals()
+    assert (tot.n_tok, tot.n_ctx, tot.n_sel, tot.n_out) == (145, 137, 27, 35)
+
+
+def _desc(fk, **kw):
+    a = dict(hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=64, rope_base=1e4, dtype=fk.FUSE_F32)
+    a.update(kw)
+    return fk.layer_desc(**a)
+
+
+def test_workspace_size_and_validation(fk):
+    t = fk.plan_requests([256], [16], 0.3, device=None)
+    n = fk.workspace_size(_desc(fk), t)
+    assert n > 256 and n % 256 == 0
+    for bad, code in [(dict(head_dim=96), fk.FUSE_ERR_UNSUPPORTED),
+                      (dict(n_q_heads=6, n_kv_heads=4), fk.FUSE_ERR_INVALID_ARG),
+                      (dict(n_q_heads=12, n_kv_heads=1), fk.FUSE_ERR_UNSUPPORTED),
+                      (dict(hidden=200), fk.FUSE_ERR_UNSUPPORTED),
+                      (dict(rope_base=1.0), fk.FUSE_ERR_INVALID_ARG),
+                      (dict(pos_encoding=7), fk.FUSE_ERR_UNSUPPORTED),
+                      (dict(dtype=fk.FUSE_U8_ASYM), fk.FUSE_ERR_UNSUPPORTED)]:
+        with pytest.raises(fk.FuseError) as e:
+            fk.workspace_size(_desc(fk, **bad), t)
+        assert e.value.status == code, bad
+
+
+def test_invalid_requests_rejected_before_launch(fk):
+    bad = fk.Request()
+    bad.n_ctx, bad.n_query, bad.k = 10, 2, 11          # k > N
+    t = fk.RequestTable([bad], device=None)
+    t.c.d_req = 16                                      # a non-null stand-in, never dereferenced
+    with pytest.raises(fk.FuseError) as e:
+        fk.workspace_size(_desc(fk), t)
+    assert e.value.status == fk.FUSE_ERR_INVALID_ARG
+
+
+def test_stitch_argument_errors(fk):
+    lib = fk.load()
+    desc = _desc(fk)
+    e = fk.Chunk()
+    e.k, e.v, e.dst_row, e.pos, e.len = 4096, 4096, 10, 10, 8
+    tab = fk.ChunkTable([e], fk.FUSE_KV_CONTIGUOUS, fk.FUSE_F32, device=None)
+    tab.c.d_chunks = 4096
+    ws = ctypes.c_void_p(1 << 20)
+    # rows past the fused cache
+    st = lib.fuse_stitch_rerotate(ctypes.byref(desc), ctypes.byref(tab.c), 4096, 4096, 12, ws, 1 << 20, None)
+    assert st == fk.FUSE_ERR_INVALID_ARG
+    # misaligned chunk pointer
+    e2 = fk.Chunk()
+    e2.k, e2.v, e2.dst_row, e2.pos, e2.len = 4100, 4096, 0, 0, 8
+    tab2 = fk.ChunkTable([e2], fk.FUSE_KV_CONTIGUOUS, fk.FUSE_F32, device=None)
+    tab2.c.d_chunks = 4096
+    st = lib.fuse_stitch_rerotate(ctypes.byref(desc), ctypes.byref(tab2.c), 4096, 4096, 64, ws, 1 << 20, None)
+    assert st == fk.FUSE_ERR_MISALIGNED
+    # missing workspace
+    st = lib.fuse_stitch_rerotate(ctypes.byref(desc), ctypes.byref(tab.c), 4096, 4096, 64, None, 0, None)
+    assert st == fk.FUSE_ERR_WORKSPACE
+    # paged without a block table / pool size
+    tab3 = fk.ChunkTable([e], fk.FUSE_KV_PAGED, fk.FUSE_F32, block_size=16, n_pool_blocks=0, device=None)
+    tab3.c.d_chunks = 4096
+    st = lib.fuse_stitch_rerotate(ctypes.byref(desc), ctypes.byref(tab3.c), 4096, 4096, 64, ws, 1 << 20, None)
+    assert st == fk.FUSE_ERR_INVALID_ARG
+    # int8 storage without its scales
+    tab4 = fk.ChunkTable([e], fk.FUSE_KV_CONTIGUOUS, fk.FUSE_U8_ASYM, device=None)
+    tab4.c.d_chunks = 4096
+    e.dst_row = 0
+    st = lib.fuse_stitch_rerotate(ctypes.byref(desc), ctypes.byref(tab4.c), 4096, 4096, 64, ws, 1 << 20, None)
+    assert st == fk.FUSE_ERR_INVALID_ARG
+
+
+def test_status_strings(fk):
+    for s in range(8):
+        assert fk.status_string(s)
+    assert fk.load().fuse_version() >= 100
+
+
+def test_struct_layouts_match_header(fk):
+    # sizes implied by the header's field order under the platform C ABI
+    assert ctypes.sizeof(fk.LayerDesc) == 32
+    assert ctypes.sizeof(fk.Chunk) == 72
+    assert ctypes.sizeof(fk.Chunks) == 40
+    assert ctypes.sizeof(fk.Request) == 48
+    assert ctypes.sizeof(fk.Requests) == 24
+    assert ctypes.sizeof(fk.Totals) == 40
