@@ -38,6 +38,10 @@ Readings taken where the pages leave a step open:
   a NaN score is an error.
 * KIVI codes are unsigned ``0 .. 2^b - 1`` with ``zero = min``; a channel
   (or token) whose max equals its min gets scale 0 and code 0.
+* A bf16 layer stores its fused cache and its Q in bf16: with ``store=``
+  ``round_bf16`` the stitched keys and values and the fresh q, k, v are
+  rounded to bf16 where they are materialised, and attention reads the
+  stored values.  Every other step stays in fp64.
 
 Every function is pinned by tests that do not re-run its own formula:
 closed forms, special cases, a textbook library routine, brute force.
@@ -53,11 +57,25 @@ import numpy as np
 F64 = np.float64
 
 __all__ = [
-    "rope_inv_freq", "rope_rotate", "pic_precompute", "kivi_quantize_key",
+    "round_bf16", "rope_inv_freq", "rope_rotate", "pic_precompute", "kivi_quantize_key",
     "kivi_quantize_value", "kivi_dequantize", "stitch_rerotate",
     "deviation_scores", "k_from_ratio", "select_topk", "selected_rows",
     "project_rows", "recompute_selected", "layer_step",
 ]
+
+
+# --------------------------------------------------------------------------
+# Storage rounding of a bf16 layer
+# --------------------------------------------------------------------------
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest bfloat16 value (8 significant bits, ties to even),
+    returned as fp64.  A bf16 layer stores its fused cache and its Q in this
+    format; the oracle applies it where the layer materialises those tensors.
+    Normal range only (|x| >= 2^-126), which covers every value here."""
+    x = np.asarray(x, dtype=F64)
+    m, e = np.frexp(x)                      # x = m * 2^e, 0.5 <= |m| < 1
+    return np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)
 
 
 # --------------------------------------------------------------------------
@@ -154,14 +172,15 @@ def kivi_dequantize(q: np.ndarray, scale: np.ndarray, zero: np.ndarray) -> np.nd
 # --------------------------------------------------------------------------
 
 def stitch_rerotate(K_chunks: Sequence[np.ndarray], V_chunks: Sequence[np.ndarray],
-                    base: float):
+                    base: float, store=None):
     """``KV^PIC(C) = [Pi_1(KV_1); ...; Pi_m(KV_m)]``.
 
     Chunk ``i`` starts at request position ``o_i = sum_{j<i} len_j``.  Its
     keys, cached at local positions ``r``, are rotated by ``R^{o_i}`` so that
     they carry ``R^{o_i + r}`` (KVBoost section 3.2: a key cached at 50 and
     reused at 1050 needs ``R^{1000}``); its values are copied unchanged.
-    Returns the context rows ``[N, Hkv, d]`` of the fused K and V.
+    Returns the context rows ``[N, Hkv, d]`` of the fused K and V, passed
+    through ``store`` (the storage rounding of the fused cache) if given.
     """
     Ks, Vs = [], []
     o = 0
@@ -169,7 +188,10 @@ def stitch_rerotate(K_chunks: Sequence[np.ndarray], V_chunks: Sequence[np.ndarra
         Ks.append(rope_rotate(K, o, base))
         Vs.append(np.asarray(V, F64))
         o += K.shape[0]
-    return np.concatenate(Ks, axis=0), np.concatenate(Vs, axis=0)
+    K, V = np.concatenate(Ks, axis=0), np.concatenate(Vs, axis=0)
+    if store is not None:
+        K, V = store(K), store(V)
+    return K, V
 
 
 # --------------------------------------------------------------------------
@@ -245,7 +267,7 @@ def project_rows(H_rows: np.ndarray, Wq, Wk, Wv, pos: np.ndarray,
 def recompute_selected(H: np.ndarray, Wq, Wk, Wv, idx: np.ndarray, n_ctx: int,
                        K_fused: np.ndarray, V_fused: np.ndarray,
                        n_q_heads: int, n_kv_heads: int, head_dim: int, base: float,
-                       out_rows: Optional[np.ndarray] = None):
+                       out_rows: Optional[np.ndarray] = None, store=None):
     """Selective recomputation of one request at one layer.
 
     ``H`` is ``[T, D]`` (context then query), ``K_fused``/``V_fused`` are
@@ -257,6 +279,8 @@ def recompute_selected(H: np.ndarray, Wq, Wk, Wv, idx: np.ndarray, n_ctx: int,
     ``h // (Hq/Hkv)``), two-pass softmax with the maximum subtracted.
 
     ``out_rows`` (indices into S) limits which attention rows are evaluated.
+    ``store`` (the storage rounding of the layer, if any) is applied to the
+    fresh q, k, v as they are materialised.
     Returns ``(K_fused', V_fused', O [len(out_rows), Hq, d], S)``.
     """
     T = H.shape[0]
@@ -265,6 +289,8 @@ def recompute_selected(H: np.ndarray, Wq, Wk, Wv, idx: np.ndarray, n_ctx: int,
     S = selected_rows(idx, n_ctx, T)
     q, k, v = project_rows(np.asarray(H, F64)[S], Wq, Wk, Wv, S,
                            n_q_heads, n_kv_heads, d, base)
+    if store is not None:
+        q, k, v = store(q), store(k), store(v)
     Kf = np.array(K_fused, dtype=F64, copy=True)
     Vf = np.array(V_fused, dtype=F64, copy=True)
     Kf[S] = k
@@ -288,7 +314,7 @@ def recompute_selected(H: np.ndarray, Wq, Wk, Wv, idx: np.ndarray, n_ctx: int,
 def layer_step(H: np.ndarray, Wq, Wk, Wv, K_chunks, V_chunks, ratio: float,
                n_q_heads: int, n_kv_heads: int, head_dim: int, base: float,
                score: bool = True, idx: Optional[np.ndarray] = None,
-               out_rows: Optional[np.ndarray] = None):
+               out_rows: Optional[np.ndarray] = None, store=None):
     """One layer-step for one request: stitch -> deviation -> top-k ->
     recompute, in the order of KVBoost Alg. 2 (probe, deviation, select,
     patch) on the cache stitched by QCFuse Eq. 4.
@@ -297,7 +323,7 @@ def layer_step(H: np.ndarray, Wq, Wk, Wv, K_chunks, V_chunks, ratio: float,
     another layer).  Returns a dict with the fused cache, scores, idx, S, O.
     """
     T = H.shape[0]
-    Kc, Vc = stitch_rerotate(K_chunks, V_chunks, base)
+    Kc, Vc = stitch_rerotate(K_chunks, V_chunks, base, store)
     n_ctx = Kc.shape[0]
     Kf = np.zeros((T, n_kv_heads, head_dim), F64)
     Vf = np.zeros((T, n_kv_heads, head_dim), F64)
@@ -308,6 +334,7 @@ def layer_step(H: np.ndarray, Wq, Wk, Wv, K_chunks, V_chunks, ratio: float,
         sc = deviation_scores(np.asarray(H, F64)[:n_ctx], Wv, Vc, n_kv_heads, head_dim)
         idx = select_topk(sc, k_from_ratio(ratio, n_ctx))
     Kf2, Vf2, O, S = recompute_selected(H, Wq, Wk, Wv, idx, n_ctx, Kf, Vf,
-                                        n_q_heads, n_kv_heads, head_dim, base, out_rows)
+                                        n_q_heads, n_kv_heads, head_dim, base, out_rows,
+                                        store)
     return {"K_stitched": Kc, "V_stitched": Vc, "score": sc, "idx": idx, "S": S,
             "K_fused": Kf2, "V_fused": Vf2, "O": O}

@@ -68,12 +68,17 @@ def _lib():
     fk.load()
 
 
-def _oracle_stitched(case):
+def _store(cfg):
+    """Storage rounding of the layer's fused cache and Q (bf16 layers)."""
+    return orc.round_bf16 if cfg.dtype == "bf16" else None
+
+
+def _oracle_stitched(case, store=None):
     """Per request: oracle stitched K, V of its context rows."""
     out = []
     for (r, row0, n, T, cis) in request_slices(case):
         K, V = orc.stitch_rerotate([case.K_cached[i] for i in cis], [case.V_cached[i] for i in cis],
-                                   case.cfg.rope_base)
+                                   case.cfg.rope_base, store)
         out.append((K, V))
     return out
 
@@ -143,7 +148,7 @@ def test_score_and_topk(name):
     score = b.score.cpu().numpy()
     idx = b.idx.cpu().numpy()
     cfg = case.cfg
-    for (r, row0, n, T, cis), (K, V) in zip(request_slices(case), _oracle_stitched(case)):
+    for (r, row0, n, T, cis), (K, V) in zip(request_slices(case), _oracle_stitched(case, _store(cfg))):
         q = b.reqs[r]
         s_gpu = score[q.score0:q.score0 + n]
         if n > 0:
@@ -181,7 +186,8 @@ def _recompute_and_compare(case, b, idx_np):
     H = f64(b.H)
     Wq, Wk, Wv = f64(b.Wq), f64(b.Wk), f64(b.Wv)
     Kf, Vf, O = f64(b.Kf), f64(b.Vf), f64(b.O)
-    for (r, row0, n, T, cis), (Ks, Vs) in zip(request_slices(case), _oracle_stitched(case)):
+    store = _store(cfg)
+    for (r, row0, n, T, cis), (Ks, Vs) in zip(request_slices(case), _oracle_stitched(case, store)):
         q = b.reqs[r]
         idx = idx_np[q.sel0:q.sel0 + q.k].astype(np.int64)
         Kf0 = np.zeros((T, cfg.n_kv_heads, cfg.head_dim))
@@ -191,7 +197,7 @@ def _recompute_and_compare(case, b, idx_np):
         rows = _rows_for_attention(S)
         Ko, Vo, Oo, S = orc.recompute_selected(H[row0:row0 + T], Wq, Wk, Wv, idx, n, Kf0, Vf0,
                                                cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim,
-                                               cfg.rope_base, out_rows=rows)
+                                               cfg.rope_base, out_rows=rows, store=store)
         if len(S) == 0:
             continue
         tol = 2e-2 if cfg.dtype == "bf16" else 1e-4
@@ -226,7 +232,7 @@ def test_layer_step(name):
     score = b.score.cpu().numpy()
     H, Wv = f64(b.H), f64(b.Wv)
     cfg = case.cfg
-    for (r, row0, n, T, cis), (K, V) in zip(request_slices(case), _oracle_stitched(case)):
+    for (r, row0, n, T, cis), (K, V) in zip(request_slices(case), _oracle_stitched(case, _store(cfg))):
         q = b.reqs[r]
         sel = idx[q.sel0:q.sel0 + q.k]
         assert np.all(np.diff(sel) > 0) and (q.k == 0 or (sel[0] >= 0 and sel[-1] < n))

@@ -20,6 +20,29 @@ def _rng(seed):
     return np.random.default_rng(seed)
 
 
+# --------------------------------------------------------- bf16 storage ----
+
+def test_round_bf16_matches_torch_on_fp32_values():
+    rng = _rng(40)
+    x = (rng.standard_normal(20000) * np.exp(rng.uniform(-20, 20, 20000))).astype(np.float32)
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(orc.round_bf16(x.astype(np.float64)), want)
+
+
+def test_round_bf16_nearest_by_brute_force():
+    # the result is the nearest of the two bf16 neighbours, ties to the even one
+    rng = _rng(41)
+    for x in np.concatenate([rng.standard_normal(300) * 37.0, [1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -3.0]]):
+        e = math.floor(math.log2(abs(x)))
+        ulp = 2.0 ** (e - 7)
+        lo = math.floor(x / ulp) * ulp
+        hi = lo + ulp
+        dl, dh = x - lo, hi - x
+        want = lo if dl < dh else hi if dh < dl else (lo if (lo / ulp) % 2 == 0 else hi)
+        assert orc.round_bf16(np.array([x]))[0] == want, x
+    assert orc.round_bf16(np.array([0.0]))[0] == 0.0
+
+
 # ---------------------------------------------------------------- RoPE ----
 
 def test_rope_inv_freq_closed_form():
