@@ -21,10 +21,11 @@ cudaError_t launch_project_recompute_tc(const fuse_layer_desc_t& desc, int64_t n
                                         const void* Wq, const void* Wk, const void* Wv, void* Q,
                                         void* Kf, void* Vf, void* Hs, uint32_t* err, cudaStream_t s);
 bool tc_attention_supported(const fuse_layer_desc_t& desc);
-cudaError_t launch_attention_tc(const fuse_layer_desc_t& desc, int64_t n_rows, int n_req,
-                                const fuse_request_t* d_req, const WorkRow* rows, const void* Q,
-                                const void* Kf, const void* Vf, void* O, uint32_t* err,
-                                cudaStream_t s);
+size_t attention_tiles_bytes(int64_t n_out, int n_req);
+cudaError_t launch_attention_tc(const fuse_layer_desc_t& d, const fuse_requests_t& reqs,
+                                int64_t n_out, int64_t n_tok, const WorkRow* rows, const void* Q,
+                                const void* Kf, const void* Vf, void* O, void* tiles_ws,
+                                uint32_t* err, cudaStream_t s);
 
 namespace {
 
@@ -70,11 +71,13 @@ RopeFreqs make_freqs(const fuse_layer_desc_t& d) {
 
 struct ReqInfo {
   fuse_totals_t tot;   // extents implied by the offsets (max over requests)
+  int n_req;
 };
 
 fuse_status_t check_reqs(const fuse_requests_t* r, ReqInfo* info, bool need_device = true) {
   if (!r || r->n_req < 0) return FUSE_ERR_INVALID_ARG;
   std::memset(info, 0, sizeof(*info));
+  info->n_req = r->n_req;
   if (r->n_req == 0) return FUSE_OK;
   if (!r->h_req || (need_device && !r->d_req)) return FUSE_ERR_INVALID_ARG;
   fuse_totals_t& t = info->tot;
@@ -132,10 +135,10 @@ fuse_status_t check_chunks(const fuse_layer_desc_t& d, const fuse_chunks_t* c, i
 
 // Workspace regions (each 256-byte aligned).
 struct WsLayout {
-  size_t partial, keys, map, rows, rope, q, hs, total;
+  size_t partial, keys, map, rows, rope, q, hs, tiles, total;
 };
 
-WsLayout ws_layout(const fuse_layer_desc_t& d, const fuse_totals_t& t) {
+WsLayout ws_layout(const fuse_layer_desc_t& d, const fuse_totals_t& t, int n_req) {
   WsLayout L;
   size_t off = sizeof(WsHeader);
   auto take = [&](size_t bytes) {
@@ -151,6 +154,7 @@ WsLayout ws_layout(const fuse_layer_desc_t& d, const fuse_totals_t& t) {
   L.rope = take((size_t)t.n_out * (d.head_dim / 2) * sizeof(float2));
   L.q = take((size_t)t.n_out * d.n_q_heads * d.head_dim * es);
   L.hs = take((size_t)t.n_out * d.hidden * es);
+  L.tiles = take(attention_tiles_bytes(t.n_out, n_req));
   L.total = off;
   return L;
 }
@@ -182,7 +186,7 @@ fuse_status_t do_stitch(const fuse_layer_desc_t& d, const fuse_chunks_t& c, int 
 fuse_status_t do_score(const fuse_layer_desc_t& d, const fuse_requests_t& r, const ReqInfo& info,
                        const void* H, const void* Wv, const void* Vf, float* score, void* ws,
                        cudaStream_t s) {
-  const WsLayout L = ws_layout(d, info.tot);
+  const WsLayout L = ws_layout(d, info.tot, info.n_req);
   if (info.tot.n_ctx == 0) return FUSE_OK;
   int32_t* map = at<int32_t>(ws, L.map);
   float* partial = at<float>(ws, L.partial);
@@ -210,7 +214,7 @@ fuse_status_t do_score(const fuse_layer_desc_t& d, const fuse_requests_t& r, con
 
 fuse_status_t do_topk(const fuse_layer_desc_t& d, const fuse_requests_t& r, const ReqInfo& info,
                       const float* score, int32_t* idx, void* ws, cudaStream_t s) {
-  const WsLayout L = ws_layout(d, info.tot);
+  const WsLayout L = ws_layout(d, info.tot, info.n_req);
   if (info.tot.n_sel == 0) return FUSE_OK;
   return cuda_status(traced("topk", s, [&] {
     return launch_topk(r, info.tot.max_ctx, score, idx, at<uint32_t>(ws, L.keys),
@@ -222,7 +226,7 @@ fuse_status_t do_recompute(const fuse_layer_desc_t& d, const fuse_requests_t& r,
                            const ReqInfo& info, const void* H, const void* Wq, const void* Wk,
                            const void* Wv, const int32_t* idx, void* Kf, void* Vf, void* O,
                            void* ws, cudaStream_t s) {
-  const WsLayout L = ws_layout(d, info.tot);
+  const WsLayout L = ws_layout(d, info.tot, info.n_req);
   const int64_t R = info.tot.n_out;
   if (R == 0) return FUSE_OK;
   int max_rows = 0;
@@ -249,7 +253,8 @@ fuse_status_t do_recompute(const fuse_layer_desc_t& d, const fuse_requests_t& r,
   if (e != cudaSuccess) return FUSE_ERR_CUDA;
   if (tc_attention_supported(d))
     e = traced("attention_tc", s, [&] {
-      return launch_attention_tc(d, R, r.n_req, r.d_req, rows, Q, Kf, Vf, O, err, s);
+      return launch_attention_tc(d, r, R, info.tot.n_tok, rows, Q, Kf, Vf, O, at<void>(ws, L.tiles),
+                                 err, s);
     });
   else
     e = traced("attention_simt", s, [&] { return launch_attention_simt(d, R, rows, Q, Kf, Vf, O, s); });
@@ -307,7 +312,7 @@ fuse_status_t fuse_workspace_size(const fuse_layer_desc_t* desc, const fuse_requ
   ReqInfo info;
   st = check_reqs(reqs, &info, /*need_device=*/false);
   if (st != FUSE_OK) return st;
-  *bytes = ws_layout(*desc, info.tot).total;
+  *bytes = ws_layout(*desc, info.tot, info.n_req).total;
   return FUSE_OK;
 }
 
@@ -343,7 +348,7 @@ fuse_status_t fuse_score_deviation(const fuse_layer_desc_t* desc, const fuse_req
   if (info.tot.n_ctx > 0 && (!H || !Wv || !Vf || !score)) return FUSE_ERR_INVALID_ARG;
   if (!aligned16(H) || !aligned16(Wv) || !aligned16(Vf) || !aligned16(score))
     return FUSE_ERR_MISALIGNED;
-  st = check_ws(ws, ws_bytes, ws_layout(*desc, info.tot).total);
+  st = check_ws(ws, ws_bytes, ws_layout(*desc, info.tot, info.n_req).total);
   if (st != FUSE_OK) return st;
   return do_score(*desc, *reqs, info, H, Wv, Vf, score, ws, (cudaStream_t)stream);
 }
@@ -382,7 +387,7 @@ fuse_status_t fuse_recompute_selected(const fuse_layer_desc_t* desc, const fuse_
   if (!aligned16(H) || !aligned16(Wq) || !aligned16(Wk) || !aligned16(Wv) || !aligned16(Kf) ||
       !aligned16(Vf) || !aligned16(O))
     return FUSE_ERR_MISALIGNED;
-  st = check_ws(ws, ws_bytes, ws_layout(*desc, info.tot).total);
+  st = check_ws(ws, ws_bytes, ws_layout(*desc, info.tot, info.n_req).total);
   if (st != FUSE_OK) return st;
   return do_recompute(*desc, *reqs, info, H, Wq, Wk, Wv, idx, Kf, Vf, O, ws, (cudaStream_t)stream);
 }
@@ -407,7 +412,7 @@ fuse_status_t fuse_layer_step(const fuse_layer_desc_t* desc, const fuse_chunks_t
   if (!aligned16(H) || !aligned16(Wq) || !aligned16(Wk) || !aligned16(Wv) || !aligned16(Kf) ||
       !aligned16(Vf) || !aligned16(O) || !aligned16(score))
     return FUSE_ERR_MISALIGNED;
-  st = check_ws(ws, ws_bytes, ws_layout(*desc, info.tot).total);
+  st = check_ws(ws, ws_bytes, ws_layout(*desc, info.tot, info.n_req).total);
   if (st != FUSE_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
   st = do_stitch(*desc, *chunks, max_len, Kf, Vf, ws, s);

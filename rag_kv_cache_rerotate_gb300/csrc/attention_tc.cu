@@ -1,0 +1,505 @@
+// Sparse-query causal GQA attention on tcgen05 tensor cores (bf16 layers,
+// head_dim 128).
+//
+// QCFuse (section 2.1.3, Eq. 6): every recomputed row at position p reads the
+// fused cache at positions j <= p.  KVBoost (section 3.1, Eq. 2):
+// softmax(q K^T / sqrt(d)) V.
+//
+// Work unit: one KV head and a tile of 128 / g consecutive recomputed rows of
+// one request, whose g query heads share that KV head, packed as the M = 128
+// rows of the MMA (row r, head hh -> M row r * g + hh).  Keys stream in
+// blocks of 128 up to the tile's last position:
+//   S_b = Q K_b^T            tcgen05.mma into one of two TMEM S buffers
+//   P_b = exp2(S_b - m)      four softmax warps, one thread per M row, causal
+//                            mask by position; P written to shared memory in
+//                            the 128B-swizzled K-major operand layout
+//   O  += P_b V_b            tcgen05.mma, V read as an MN-major operand
+// The running maximum m is raised only when a block exceeds it by more than
+// 2^8 (then O in TMEM and the running sum are rescaled), so most blocks skip
+// the rescale.  Warp 0 issues TMA loads (Q once per unit, K and V blocks into
+// a 2-stage ring), warp 1 issues the MMAs, warps 2-5 run the softmax and the
+// epilogue.  The kernel is persistent; units are taken heaviest first.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tc_ptx.cuh"
+
+namespace fusekv {
+
+bool tma_encode_available();
+bool make_map_3d(CUtensorMap* m, const void* base, const uint64_t dims[3], const uint64_t strides[2],
+                 const uint32_t box[3]);
+
+namespace {
+
+constexpr int kD = 128;
+constexpr int kKB = 128;                      // keys per block
+constexpr int kHalf = 128 * 64 * 2;           // one 64-column half of a 128-row tile (16 KB)
+constexpr int kTile = 2 * kHalf;              // 32 KB
+constexpr int kStages = 2;
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;                // S0 | S1 | O | unused
+constexpr int kSmemBytes = (2 + 2 * kStages) * kTile + 1024 + 256;
+constexpr float kRescaleThreshold = 8.0f;     // log2 units
+
+struct AttnTile {
+  int32_t req;
+  int32_t r0;     // first row of the tile within the request's recomputed rows
+  int32_t n;      // rows in the tile
+  int32_t pad;
+};
+
+struct AttnArgs {
+  const AttnTile* tiles;
+  int n_tiles;
+  int n_units;
+  const fuse_request_t* reqs;
+  const WorkRow* rows;
+  __nv_bfloat16* O;
+  int Hq, Hkv, g, rtile;
+  float scale_log2;       // log2(e) / sqrt(d)
+  uint32_t* err;
+};
+
+struct Ctl {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+  uint64_t s_full[2];
+  uint64_t p_full, pv_done, o_empty;
+  uint32_t tmem_base;
+  volatile int abort_flag;
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ctl* ctl) {
+  return tc::mbar_wait(bar, parity, &ctl->abort_flag);
+}
+
+// The softmax warps issue warp-collective TMEM loads after their waits.
+__device__ __forceinline__ bool warp_wait_or_abort(uint64_t* bar, uint32_t parity, Ctl* ctl) {
+  return tc::mbar_wait_warp(bar, parity, &ctl->abort_flag);
+}
+
+// Which wait gave up: info = wait id (4 bits) << 20 | CTA (8 bits) << 12 | key block (12 bits).
+enum AttnWait : uint32_t {
+  W_Q_EMPTY = 1, W_KV_EMPTY, W_Q_FULL, W_K_FULL0, W_K_FULL, W_P_FULL, W_O_EMPTY, W_V_FULL,
+  W_S_FULL, W_PV_DONE, W_PV_LAST
+};
+
+__device__ __forceinline__ void abort_kernel(Ctl* ctl, uint32_t* err, uint32_t which = 0,
+                                             int j = 0) {
+  const bool first = ctl->abort_flag == 0;
+  ctl->abort_flag = 1;
+  if (first)
+    report_error(err, FUSE_ERR_TIMEOUT, SITE_ATTN_TIMEOUT,
+                 (which << 20) | ((blockIdx.x & 0xFFu) << 12) | ((uint32_t)j & 0xFFFu));
+}
+
+struct Unit {
+  int kvh, out0, row0, r0, n, pmax, nkb;
+};
+
+__device__ __forceinline__ Unit unit_of(const AttnArgs& a, int u) {
+  Unit x;
+  const AttnTile t = a.tiles[a.n_tiles - 1 - u / a.Hkv];   // heaviest tiles first
+  x.kvh = u % a.Hkv;
+  const fuse_request_t& R = a.reqs[t.req];
+  x.out0 = (int)R.out0;
+  x.row0 = (int)R.row0;
+  x.r0 = t.r0;
+  x.n = t.n;
+  x.pmax = a.rows[R.out0 + t.r0 + t.n - 1].pos;
+  x.nkb = x.pmax / kKB + 1;
+  return x;
+}
+
+// descriptor of K-step kk (16 columns) of a 128-row K-major tile stored as two
+// 64-column halves
+__device__ __forceinline__ uint64_t kmajor_step(uint32_t tile, int kk) {
+  return tc::smem_desc_k128(tile + (kk >> 2) * kHalf + (kk & 3) * 32);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
+                   const __grid_constant__ CUtensorMap mapV, const AttnArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sP = smem + kTile;
+  uint8_t* sK = smem + 2 * kTile;                   // stage s: K at sK + 2s*kTile, V after it
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + (2 + 2 * kStages) * kTile);
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&ctl->q_full, 1);
+    tc::mbar_init(&ctl->q_empty, 1);
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&ctl->k_full[s], 1);
+      tc::mbar_init(&ctl->v_full[s], 1);
+      tc::mbar_init(&ctl->kv_empty[s], 1);
+    }
+    tc::mbar_init(&ctl->s_full[0], 1);
+    tc::mbar_init(&ctl->s_full[1], 1);
+    tc::mbar_init(&ctl->p_full, 128);
+    tc::mbar_init(&ctl->pv_done, 1);
+    tc::mbar_init(&ctl->o_empty, 128);
+    ctl->abort_flag = 0;
+    tc::fence_barrier_init();
+    tc::tma_prefetch_desc(&mapQ);
+    tc::tma_prefetch_desc(&mapK);
+    tc::tma_prefetch_desc(&mapV);
+  }
+  if (warp == 1) tc::tmem_alloc(&ctl->tmem_base, kTmemCols);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    if (lane == 0) {
+      uint32_t uc = 0, kvc = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x, ++uc) {
+        const Unit x = unit_of(a, u);
+        if (!wait_or_abort(&ctl->q_empty, (uc & 1) ^ 1, ctl)) {
+          abort_kernel(ctl, a.err, W_Q_EMPTY, 0);
+          break;
+        }
+        tc::mbar_arrive_expect_tx(&ctl->q_full, kTile);
+        tc::tma_load_3d(sQ, &mapQ, &ctl->q_full, 0, x.kvh * a.g, x.out0 + x.r0);
+        tc::tma_load_3d(sQ + kHalf, &mapQ, &ctl->q_full, 64, x.kvh * a.g, x.out0 + x.r0);
+        for (int j = 0; j < x.nkb; ++j, ++kvc) {
+          const int st = kvc & 1;
+          if (!wait_or_abort(&ctl->kv_empty[st], ((kvc >> 1) & 1) ^ 1, ctl)) {
+            abort_kernel(ctl, a.err, W_KV_EMPTY, j);
+            ok = false;
+            break;
+          }
+          uint8_t* k = sK + 2 * st * kTile;
+          uint8_t* v = k + kTile;
+          const int z = x.row0 + j * kKB;
+          tc::mbar_arrive_expect_tx(&ctl->k_full[st], kTile);
+          tc::tma_load_3d(k, &mapK, &ctl->k_full[st], 0, x.kvh, z);
+          tc::tma_load_3d(k + kHalf, &mapK, &ctl->k_full[st], 64, x.kvh, z);
+          tc::mbar_arrive_expect_tx(&ctl->v_full[st], kTile);
+          tc::tma_load_3d(v, &mapV, &ctl->v_full[st], 0, x.kvh, z);
+          tc::tma_load_3d(v + kHalf, &mapV, &ctl->v_full[st], 64, x.kvh, z);
+        }
+      }
+      // let copies in flight land before the CTA may exit
+      tc::mbar_wait(&ctl->q_full, (uc & 1) ^ 1);
+      for (int s = 0; s < kStages; ++s) {
+        if (kvc > (uint32_t)s) {
+          const uint32_t last = kvc - 1 - ((kvc - 1 - s) & 1);   // last use of stage s
+          tc::mbar_wait(&ctl->k_full[s], (last >> 1) & 1);
+          tc::mbar_wait(&ctl->v_full[s], (last >> 1) & 1);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ------------------------------
+    if (lane == 0) {
+      const uint32_t idesc_s = tc::idesc_bf16_f32(128, kKB);
+      const uint32_t idesc_o = tc::idesc_bf16_f32(128, kD, /*b_mn_major=*/true);
+      const uint32_t q_addr = tc::smem_u32(sQ);
+      const uint32_t p_addr = tc::smem_u32(sP);
+      uint32_t uc = 0, kvc = 0, bc = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x, ++uc) {
+        const Unit x = unit_of(a, u);
+        if (!wait_or_abort(&ctl->q_full, uc & 1, ctl)) {
+          abort_kernel(ctl, a.err, W_Q_FULL, 0);
+          break;
+        }
+        tc::tc_fence_after();
+        // S of block 0
+        {
+          const int st = kvc & 1;
+          if (!wait_or_abort(&ctl->k_full[st], (kvc >> 1) & 1, ctl)) {
+            abort_kernel(ctl, a.err, W_K_FULL0, 0);
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t kaddr = tc::smem_u32(sK + 2 * st * kTile);
+          const uint32_t d = tmem + (bc & 1) * kKB;
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            tc::mma_bf16(d, kmajor_step(q_addr, kk), kmajor_step(kaddr, kk), idesc_s, kk != 0);
+          tc::mma_commit(&ctl->s_full[bc & 1]);
+        }
+        for (int j = 0; j < x.nkb; ++j) {
+          const uint32_t b = bc + j;
+          const uint32_t kv = kvc + j;
+          if (j + 1 < x.nkb) {
+            const int st1 = (kv + 1) & 1;
+            if (!wait_or_abort(&ctl->k_full[st1], ((kv + 1) >> 1) & 1, ctl)) {
+              abort_kernel(ctl, a.err, W_K_FULL, j);
+              ok = false;
+              break;
+            }
+            tc::tc_fence_after();
+            const uint32_t kaddr = tc::smem_u32(sK + 2 * st1 * kTile);
+            const uint32_t d = tmem + ((b + 1) & 1) * kKB;
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk)
+              tc::mma_bf16(d, kmajor_step(q_addr, kk), kmajor_step(kaddr, kk), idesc_s, kk != 0);
+            tc::mma_commit(&ctl->s_full[(b + 1) & 1]);
+          }
+          if (!wait_or_abort(&ctl->p_full, b & 1, ctl)) {
+            abort_kernel(ctl, a.err, W_P_FULL, j);
+            ok = false;
+            break;
+          }
+          if (j == 0 && !wait_or_abort(&ctl->o_empty, (uc & 1) ^ 1, ctl)) {
+            abort_kernel(ctl, a.err, W_O_EMPTY, j);
+            ok = false;
+            break;
+          }
+          const int st = kv & 1;
+          if (!wait_or_abort(&ctl->v_full[st], (kv >> 1) & 1, ctl)) {
+            abort_kernel(ctl, a.err, W_V_FULL, j);
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t vaddr = tc::smem_u32(sK + (2 * st + 1) * kTile);
+          const uint32_t o = tmem + 2 * kKB;
+#pragma unroll
+          for (int kk = 0; kk < kKB / 16; ++kk)
+            tc::mma_bf16(o, kmajor_step(p_addr, kk),
+                         tc::smem_desc_mn128(vaddr + kk * 16 * 128, kHalf), idesc_o,
+                         (j | kk) != 0);
+          tc::mma_commit(&ctl->pv_done);
+          tc::mma_commit(&ctl->kv_empty[st]);
+        }
+        if (!ok) break;
+        tc::mma_commit(&ctl->q_empty);
+        bc += x.nkb;
+        kvc += x.nkb;
+      }
+    }
+  } else {
+    // --------------------------- softmax + epilogue ---------------------------
+    const int quarter = warp % 4;
+    const int m = quarter * 32 + lane;                 // M row = TMEM lane
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    uint32_t uc = 0, bc = 0;
+    for (int u = blockIdx.x; u < a.n_units; u += gridDim.x, ++uc) {
+      const Unit x = unit_of(a, u);
+      const int rl = m / a.g;
+      const int hh = m % a.g;
+      const bool valid = rl < x.n;
+      const int p = a.rows[x.out0 + x.r0 + (valid ? rl : x.n - 1)].pos;
+      float mu = -1e30f, l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < x.nkb; ++j) {
+        const uint32_t b = bc + j;
+        if (!warp_wait_or_abort(&ctl->s_full[b & 1], (b >> 1) & 1, ctl)) {
+          abort_kernel(ctl, a.err, W_S_FULL, j);
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+        float s[kKB];
+        {
+          const uint32_t ts = tmem + lane_off + (b & 1) * kKB;
+#pragma unroll
+          for (int c0 = 0; c0 < kKB; c0 += 32) {
+            uint32_t r[32];
+            tc::tmem_ld_32x32b_x32(ts + c0, r);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) s[c0 + i] = __uint_as_float(r[i]);
+          }
+        }
+        const int key0 = j * kKB;
+        float mx = -1e30f;
+#pragma unroll
+        for (int c = 0; c < kKB; ++c) {
+          s[c] = (key0 + c <= p) ? s[c] * a.scale_log2 : -1e30f;
+          mx = fmaxf(mx, s[c]);
+        }
+        float mnew = mu;
+        bool rescale = false;
+        if (j == 0) {
+          mnew = mx;
+        } else if (mx > mu + kRescaleThreshold) {
+          mnew = mx;
+          rescale = true;
+        }
+        float sum = 0.f;
+        uint32_t pk[kKB / 2];
+#pragma unroll
+        for (int c = 0; c < kKB; c += 2) {
+          const float p0 = exp2f(s[c] - mnew);
+          const float p1 = exp2f(s[c + 1] - mnew);
+          sum += p0 + p1;
+          pk[c / 2] = pack_bf16x2(p0, p1);
+        }
+        const float alpha = rescale ? exp2f(mu - mnew) : 1.f;
+        l = l * alpha + sum;
+        if (j > 0) {
+          if (!warp_wait_or_abort(&ctl->pv_done, (b - 1) & 1, ctl)) {
+            abort_kernel(ctl, a.err, W_PV_DONE, j);
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+        }
+        // tcgen05.ld/st are warp-collective (.sync.aligned): the whole warp
+        // rescales when any of its rows needs it (alpha is 1 for the others)
+        if (__any_sync(0xffffffffu, rescale)) {
+          const uint32_t to = tmem + lane_off + 2 * kKB;
+#pragma unroll
+          for (int c0 = 0; c0 < kD; c0 += 32) {
+            uint32_t r[32];
+            tc::tmem_ld_32x32b_x32(to + c0, r);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tc::tmem_st_32x32b_x32(to + c0, r);
+          }
+          tc::tmem_st_wait();
+        }
+        // P row m into the swizzled K-major layout: 16-byte chunk c of the
+        // 64-column half h lands at chunk (c ^ (m & 7)) of row m
+#pragma unroll
+        for (int c = 0; c < kKB / 8; ++c) {
+          const int h = c >> 3;
+          const int cc = c & 7;
+          uint4 w = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          *reinterpret_cast<uint4*>(sP + h * kHalf + m * 128 + ((cc ^ (m & 7)) << 4)) = w;
+        }
+        tc::fence_proxy_async_smem();
+        tc::tc_fence_before();
+        tc::mbar_arrive(&ctl->p_full);
+        mu = mnew;
+      }
+      if (!ok) break;
+      if (!warp_wait_or_abort(&ctl->pv_done, (bc + x.nkb - 1) & 1, ctl)) {
+        abort_kernel(ctl, a.err, W_PV_LAST, x.nkb);
+        break;
+      }
+      tc::tc_fence_after();
+      {
+        const float inv = 1.f / l;
+        const uint32_t to = tmem + lane_off + 2 * kKB;
+        __nv_bfloat16* dst =
+            a.O + ((int64_t)(x.out0 + x.r0 + rl) * a.Hq + x.kvh * a.g + hh) * kD;
+#pragma unroll
+        for (int c0 = 0; c0 < kD; c0 += 32) {
+          uint32_t r[32];
+          tc::tmem_ld_32x32b_x32(to + c0, r);
+          tc::tmem_ld_wait();
+          if (valid) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(r[8 * q + 0]) * inv, __uint_as_float(r[8 * q + 1]) * inv);
+              w.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]) * inv, __uint_as_float(r[8 * q + 3]) * inv);
+              w.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]) * inv, __uint_as_float(r[8 * q + 5]) * inv);
+              w.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]) * inv, __uint_as_float(r[8 * q + 7]) * inv);
+              reinterpret_cast<uint4*>(dst + c0)[q] = w;
+            }
+          }
+        }
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(&ctl->o_empty);
+      bc += x.nkb;
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+// One block: the tiles of every request, in request order.
+__global__ void attn_tiles_kernel(const fuse_request_t* reqs, int n_req, int rtile, AttnTile* tiles) {
+  if (threadIdx.x != 0) return;
+  int t = 0;
+  for (int r = 0; r < n_req; ++r) {
+    const int R = reqs[r].k + reqs[r].n_query;
+    for (int r0 = 0; r0 < R; r0 += rtile) {
+      AttnTile x;
+      x.req = r;
+      x.r0 = r0;
+      x.n = min(rtile, R - r0);
+      x.pad = 0;
+      tiles[t++] = x;
+    }
+  }
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+}  // namespace
+
+size_t attention_tiles_bytes(int64_t n_out, int n_req) {
+  return (size_t)(n_out / 16 + n_req + 1) * sizeof(AttnTile);
+}
+
+bool tc_attention_supported(const fuse_layer_desc_t& d) {
+  const int g = d.n_q_heads / d.n_kv_heads;
+  return d.dtype == FUSE_BF16 && d.head_dim == kD && (g == 1 || g == 2 || g == 4 || g == 8) &&
+         tma_encode_available();
+}
+
+cudaError_t launch_attention_tc(const fuse_layer_desc_t& d, const fuse_requests_t& reqs,
+                                int64_t n_out, int64_t n_tok, const WorkRow* rows, const void* Q,
+                                const void* Kf, const void* Vf, void* O, void* tiles_ws,
+                                uint32_t* err, cudaStream_t s) {
+  const int g = d.n_q_heads / d.n_kv_heads;
+  const int rtile = 128 / g;
+  int n_tiles = 0;
+  for (int r = 0; r < reqs.n_req; ++r) {
+    const int R = reqs.h_req[r].k + reqs.h_req[r].n_query;
+    n_tiles += (R + rtile - 1) / rtile;
+  }
+  if (n_tiles == 0) return cudaSuccess;
+  AttnTile* tiles = reinterpret_cast<AttnTile*>(tiles_ws);
+  attn_tiles_kernel<<<1, 32, 0, s>>>(reqs.d_req, reqs.n_req, rtile, tiles);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  CUtensorMap mQ, mK, mV;
+  const uint64_t dq[3] = {(uint64_t)kD, (uint64_t)d.n_q_heads, (uint64_t)n_out};
+  const uint64_t sq[2] = {(uint64_t)kD * 2, (uint64_t)d.n_q_heads * kD * 2};
+  const uint32_t bq[3] = {64, (uint32_t)g, (uint32_t)rtile};
+  const uint64_t dk[3] = {(uint64_t)kD, (uint64_t)d.n_kv_heads, (uint64_t)n_tok};
+  const uint64_t sk[2] = {(uint64_t)kD * 2, (uint64_t)d.n_kv_heads * kD * 2};
+  const uint32_t bk[3] = {64, 1, (uint32_t)kKB};
+  if (!make_map_3d(&mQ, Q, dq, sq, bq) || !make_map_3d(&mK, Kf, dk, sk, bk) ||
+      !make_map_3d(&mV, Vf, dk, sk, bk))
+    return cudaErrorInvalidValue;
+
+  AttnArgs a;
+  a.tiles = tiles;
+  a.n_tiles = n_tiles;
+  a.n_units = n_tiles * d.n_kv_heads;
+  a.reqs = reqs.d_req;
+  a.rows = rows;
+  a.O = reinterpret_cast<__nv_bfloat16*>(O);
+  a.Hq = d.n_q_heads;
+  a.Hkv = d.n_kv_heads;
+  a.g = g;
+  a.rtile = rtile;
+  a.scale_log2 = 1.4426950408889634f / sqrtf((float)kD);
+  a.err = err;
+  e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int grid = a.n_units < sm_count() ? a.n_units : sm_count();
+  attn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(mQ, mK, mV, a);
+  return cudaGetLastError();
+}
+
+}  // namespace fusekv

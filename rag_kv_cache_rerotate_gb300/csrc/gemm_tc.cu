@@ -72,12 +72,7 @@ struct SharedCtl {
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, SharedCtl* ctl) {
-  for (uint32_t i = 0; i < tc::kSpinLimit; ++i) {
-    if (tc::mbar_try_wait(bar, parity)) return true;
-    if ((i & 1023u) == 1023u && ctl->abort_flag) return false;
-    if (i > 64) __nanosleep(32);
-  }
-  return false;
+  return tc::mbar_wait(bar, parity, &ctl->abort_flag);
 }
 
 __device__ __forceinline__ void abort_kernel(SharedCtl* ctl, uint32_t* err) {
@@ -308,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const int mt = tile % a.m_tiles;
       const int nt = tile / a.m_tiles;
-      if (!wait_or_abort(&ctl->tfull[acc], acc_ph, ctl)) {
+      if (!tc::mbar_wait_warp(&ctl->tfull[acc], acc_ph, &ctl->abort_flag)) {
         abort_kernel(ctl, a.err);
         break;
       }
@@ -395,6 +390,23 @@ __global__ void gather_rows_kernel(const __nv_bfloat16* H, const WorkRow* rows, 
 
 }  // namespace
 
+bool tma_encode_available() { return encode_fn() != nullptr; }
+
+// Row-major bf16 tensor of rank 3 (dims innermost first, byte strides of
+// dims 1 and 2) read in boxes of `box` elements, 128-byte swizzled.
+bool make_map_3d(CUtensorMap* m, const void* base, const uint64_t dims[3], const uint64_t strides[2],
+                 const uint32_t box[3]) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t gd[3] = {dims[0], dims[1], dims[2]};
+  cuuint64_t gs[2] = {strides[0], strides[1]};
+  cuuint32_t bx[3] = {box[0], box[1], box[2]};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gd, gs, bx, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool tc_gemm_supported(const fuse_layer_desc_t& d) {
   return d.dtype == FUSE_BF16 && d.head_dim == 128 && d.hidden % BK == 0 && encode_fn() != nullptr;
 }
@@ -461,14 +473,6 @@ cudaError_t launch_project_recompute_tc(const fuse_layer_desc_t& d, int64_t n_ro
   a.Vout = reinterpret_cast<__nv_bfloat16*>(Vf);
   a.err = err;
   return launch(mA, mQ, mK, mV, a, s);
-}
-
-bool tc_attention_supported(const fuse_layer_desc_t&) { return false; }
-
-cudaError_t launch_attention_tc(const fuse_layer_desc_t&, int64_t, int, const fuse_request_t*,
-                                const WorkRow*, const void*, const void*, const void*, void*,
-                                uint32_t*, cudaStream_t) {
-  return cudaErrorNotSupported;
 }
 
 }  // namespace fusekv

@@ -1,7 +1,7 @@
 // Inline-PTX wrappers for sm_103a: mbarriers, TMA tensor copies, tcgen05
 // (tensor memory allocation, MMA, commit, loads) and the shared-memory and
-// instruction descriptors of tcgen05.mma.  Every wait is bounded: after
-// kSpinLimit failed polls it reports failure instead of spinning forever.
+// instruction descriptors of tcgen05.mma.  Every wait is bounded in time:
+// after kWaitLimitNs it reports failure instead of spinning forever.
 #pragma once
 
 #include <cuda.h>
@@ -10,7 +10,14 @@
 namespace fusekv {
 namespace tc {
 
-constexpr uint32_t kSpinLimit = 1u << 26;   // polls (with back-off) before a wait gives up
+constexpr uint64_t kWaitLimitNs = 1000000000ull;   // a wait gives up after one second
+constexpr uint32_t kWaitPollLimit = 1u << 24;      // ... or after this many polls
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -49,13 +56,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait until the phase with the given parity has completed; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+// Wait until the phase with the given parity has completed; false once
+// kWaitLimitNs have passed.  If abort_flag is given, also false soon after
+// it becomes non-zero.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          const volatile int* abort_flag = nullptr) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1; i < kWaitPollLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (i > 64) __nanosleep(32);
+    if ((i & 63u) == 0) {
+      if (abort_flag && *abort_flag) return false;
+      if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+    if (i > 32) __nanosleep(64);
   }
   return false;
+}
+
+// mbar_wait by every lane of a warp, with one warp-wide answer: a warp that
+// goes on to warp-collective (.sync.aligned) instructions must not split
+// because one lane gave up.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
+                                               const volatile int* abort_flag) {
+  const bool ok = mbar_wait(bar, parity, abort_flag);
+  return __all_sync(0xffffffffu, ok);
 }
 
 // ---- TMA ---------------------------------------------------------------------
@@ -71,6 +96,22 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
+}
+
+// 3-D tiled load; x innermost (elements), then y, then z.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the
+// async proxy (TMA, tcgen05.mma operand reads).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ---- tcgen05 ----------------------------------------------------------------
@@ -138,6 +179,25 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Store 32 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0],"
+      " {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16,"
+      " %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+      "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]),
+      "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]),
+      "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor of a K-major operand tile written by TMA
 // with 128-byte swizzling: rows of 128 bytes (64 bf16), 8-row groups 1024
 // bytes apart (stride byte offset), leading byte offset unused for this
@@ -153,12 +213,28 @@ __device__ __forceinline__ uint64_t smem_desc_k128(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor of kind::f16 with bf16 A and B, fp32 D, both
-// operands K-major, shape M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+// Shared-memory matrix descriptor of an MN-major operand with 128-byte
+// swizzling: each 128-byte row holds 64 consecutive MN elements of one K
+// index, 8 K rows form a 1024-byte swizzle atom (stride byte offset between
+// 8-row K groups), and the next 64 MN elements start mn_atom_bytes later
+// (leading byte offset).
+__device__ __forceinline__ uint64_t smem_desc_mn128(uint32_t saddr, uint32_t mn_atom_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((mn_atom_bytes >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::f16 with bf16 A and B, fp32 D, shape
+// M x N; A K-major, B K-major unless b_mn_major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major = false) {
   return (1u << 4)                    // D format: f32
          | (1u << 7)                  // A format: bf16
          | (1u << 10)                 // B format: bf16
+         | ((b_mn_major ? 1u : 0u) << 16)
          | ((uint32_t)(N >> 3) << 17) // N / 8
          | ((uint32_t)(M >> 4) << 24);// M / 16
 }
