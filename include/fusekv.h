@@ -251,6 +251,27 @@ fuse_status_t fuse_pic_precompute(const fuse_layer_desc_t* desc, const fuse_chun
  * not NULL it receives a code locating the failed check. */
 fuse_status_t fuse_check_errors(void* ws, fuse_stream_t stream, uint32_t* detail);
 
+/* Top-k without a workspace (no counterpart on the pages).  Same selection
+ * as fuse_select_topk, for callers that cannot allocate device memory when
+ * they select: a serving loop that has given all free HBM to its KV-cache
+ * pool, or code running where the allocator must not be touched.  The key
+ * scratch is a fixed device array inside the library (4 *
+ * FUSE_TOPK_NOALLOC_MAX_KEYS + 256 bytes, 2 MiB), held on every GPU that
+ * loads the library until the process exits; this call allocates nothing.
+ *   - N_total (the largest score0 + N_r) above FUSE_TOPK_NOALLOC_MAX_KEYS is
+ *     rejected with FUSE_ERR_WORKSPACE before any launch.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before
+ *     any stream capture.
+ *   - All calls share the one array: calls whose work overlaps on the GPU
+ *     (different streams, no ordering between them) race and give wrong
+ *     indices.  Order them on one stream or with events.
+ *   - NaN scores still rank below every number, but this variant does not
+ *     report them (fuse_select_topk with a workspace does). */
+#define FUSE_TOPK_NOALLOC_MAX_KEYS (1 << 19)
+fuse_status_t fuse_select_topk_noalloc(const fuse_requests_t* reqs, const float* score,
+                                       int32_t* idx, fuse_stream_t stream);
+
 /* Kernel timing trace (no counterpart on the pages; a measurement aid).
  * fuse_trace_begin(n) creates n pairs of CUDA events and, until
  * fuse_trace_end, records one pair around each kernel the library launches,

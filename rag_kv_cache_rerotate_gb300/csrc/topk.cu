@@ -164,3 +164,82 @@ cudaError_t launch_topk(const fuse_requests_t& reqs, int max_ctx, const float* s
 }
 
 }  // namespace fusekv
+
+// ----------------------------------------------------------------------------
+// Top-k without a caller workspace.
+//
+// Some callers cannot allocate device memory at the point where they select
+// tokens: a serving loop that has handed every byte of HBM to its KV-cache
+// pool, or code running inside a framework callback that must not touch the
+// allocator.  For them the key scratch of the top-k lives in this file-scope
+// device array instead of a workspace.  It is created when the library is
+// loaded and held on every GPU that loads the library until the process
+// exits.
+// ----------------------------------------------------------------------------
+#include <mutex>
+
+namespace fusekv {
+namespace {
+
+constexpr int kNoallocHeaderWords = 64;          // word 0: device error code (cleared per call)
+constexpr int kNoallocMaxDevices = 64;
+
+static __device__ __align__(256) uint32_t g_topk_scratch[kNoallocHeaderWords + FUSE_TOPK_NOALLOC_MAX_KEYS];
+
+std::mutex g_noalloc_mu;
+uint32_t* g_noalloc_addr[kNoallocMaxDevices] = {};
+
+// Device address of g_topk_scratch on the current device; looked up once
+// per device (host code cannot use the symbol itself as an address).
+cudaError_t noalloc_scratch(uint32_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kNoallocMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_topk_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_addr[dev] = static_cast<uint32_t*>(p);
+  }
+  *out = g_noalloc_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace fusekv
+
+extern "C" fuse_status_t fuse_select_topk_noalloc(const fuse_requests_t* reqs, const float* score,
+                                                  int32_t* idx, fuse_stream_t stream) {
+  using namespace fusekv;
+  if (!reqs || reqs->n_req < 0) return FUSE_ERR_INVALID_ARG;
+  if (reqs->n_req == 0) return FUSE_OK;
+  if (!reqs->h_req || !reqs->d_req) return FUSE_ERR_INVALID_ARG;
+  int64_t n_ctx = 0, n_sel = 0;
+  int max_ctx = 0;
+  for (int i = 0; i < reqs->n_req; ++i) {
+    const fuse_request_t& q = reqs->h_req[i];
+    if (q.n_ctx < 0 || q.n_query < 0 || q.k < 0 || q.k > q.n_ctx || q.reserved != 0 ||
+        q.score0 < 0 || q.sel0 < 0)
+      return FUSE_ERR_INVALID_ARG;
+    n_ctx = std::max<int64_t>(n_ctx, q.score0 + q.n_ctx);
+    n_sel = std::max<int64_t>(n_sel, q.sel0 + q.k);
+    max_ctx = std::max(max_ctx, q.n_ctx);
+  }
+  if (n_ctx > FUSE_TOPK_NOALLOC_MAX_KEYS) return FUSE_ERR_WORKSPACE;
+  if (n_sel == 0) return FUSE_OK;
+  if (!score || !idx) return FUSE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(score) | reinterpret_cast<uintptr_t>(idx)) & 15u)
+    return FUSE_ERR_MISALIGNED;
+  uint32_t* scratch = nullptr;
+  if (noalloc_scratch(&scratch) != cudaSuccess) return FUSE_ERR_CUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  // the error word must start at zero for the kernel's first-error report
+  if (cudaMemsetAsync(scratch, 0, sizeof(uint32_t) * 2, s) != cudaSuccess) return FUSE_ERR_CUDA;
+  topk_kernel<<<reqs->n_req, kTopkThreads, 0, s>>>(reqs->d_req, score, idx,
+                                                   scratch + kNoallocHeaderWords, scratch,
+                                                   /*keys_in_smem=*/0);
+  (void)max_ctx;
+  return cudaGetLastError() == cudaSuccess ? FUSE_OK : FUSE_ERR_CUDA;
+}
