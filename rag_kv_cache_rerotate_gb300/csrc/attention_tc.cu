@@ -10,14 +10,17 @@
 // rows of the MMA (row r, head hh -> M row r * g + hh).  Keys stream in
 // blocks of 128 up to the tile's last position:
 //   S_b = Q K_b^T            tcgen05.mma into one of two TMEM S buffers
-//   P_b = exp2(S_b - m)      four softmax warps, one thread per M row, causal
-//                            mask by position; P written to shared memory in
-//                            the 128B-swizzled K-major operand layout
+//   P_b = exp2(S_b - m)      two softmax warpgroups, each thread one M row and
+//                            one 64-key half of the block (the two halves of a
+//                            row exchange their maxima and sums through shared
+//                            memory); causal mask by position on the blocks
+//                            that need it; P written to shared memory in the
+//                            128B-swizzled K-major operand layout
 //   O  += P_b V_b            tcgen05.mma, V read as an MN-major operand
 // The running maximum m is raised only when a block exceeds it by more than
 // 2^8 (then O in TMEM and the running sum are rescaled), so most blocks skip
 // the rescale.  Warp 0 issues TMA loads (Q once per unit, K and V blocks into
-// a 2-stage ring), warp 1 issues the MMAs, warps 2-5 run the softmax and the
+// a 2-stage ring), warp 1 issues the MMAs, warps 2-9 run the softmax and the
 // epilogue.  The kernel is persistent; units are taken heaviest first.
 #include <cudaTypedefs.h>
 
@@ -38,9 +41,10 @@ constexpr int kKB = 128;                      // keys per block
 constexpr int kHalf = 128 * 64 * 2;           // one 64-column half of a 128-row tile (16 KB)
 constexpr int kTile = 2 * kHalf;              // 32 KB
 constexpr int kStages = 2;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;                 // producer, MMA, 2 softmax warpgroups
+constexpr int kSoftThreads = 256;
 constexpr int kTmemCols = 512;                // S0 | S1 | O | unused
-constexpr int kSmemBytes = (2 + 2 * kStages) * kTile + 1024 + 256;
+constexpr int kSmemBytes = (2 + 2 * kStages) * kTile + 1024 + 8192;
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
 
 struct AttnTile {
@@ -69,6 +73,10 @@ struct Ctl {
   uint64_t p_full, pv_done, o_empty;
   uint32_t tmem_base;
   volatile int abort_flag;
+  uint64_t xmax_bar[2][4];  // [block parity][lane quarter]: both half-row maxima written
+  uint64_t xsum_bar[2][4];  // [unit parity][lane quarter]: both half-row sums written
+  float xmax[2][2][128];     // [block parity][warpgroup][row]: half-row maxima
+  float xsum[2][2][128];     // [unit parity][warpgroup][row]: half-row sums
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ctl* ctl) {
@@ -83,7 +91,7 @@ __device__ __forceinline__ bool warp_wait_or_abort(uint64_t* bar, uint32_t parit
 // Which wait gave up: info = wait id (4 bits) << 20 | CTA (8 bits) << 12 | key block (12 bits).
 enum AttnWait : uint32_t {
   W_Q_EMPTY = 1, W_KV_EMPTY, W_Q_FULL, W_K_FULL0, W_K_FULL, W_P_FULL, W_O_EMPTY, W_V_FULL,
-  W_S_FULL, W_PV_DONE, W_PV_LAST
+  W_S_FULL, W_PV_DONE, W_PV_LAST, W_XCHG
 };
 
 __device__ __forceinline__ void abort_kernel(Ctl* ctl, uint32_t* err, uint32_t which = 0,
@@ -113,6 +121,19 @@ __device__ __forceinline__ Unit unit_of(const AttnArgs& a, int u) {
   return x;
 }
 
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+
 // descriptor of K-step kk (16 columns) of a 128-row K-major tile stored as two
 // 64-column halves
 __device__ __forceinline__ uint64_t kmajor_step(uint32_t tile, int kk) {
@@ -141,9 +162,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::mbar_init(&ctl->s_full[0], 1);
     tc::mbar_init(&ctl->s_full[1], 1);
-    tc::mbar_init(&ctl->p_full, 128);
+    tc::mbar_init(&ctl->p_full, kSoftThreads);
     tc::mbar_init(&ctl->pv_done, 1);
-    tc::mbar_init(&ctl->o_empty, 128);
+    tc::mbar_init(&ctl->o_empty, kSoftThreads);
+    // the two warps (one per softmax warpgroup) owning a TMEM lane quarter
+    // exchange half-row values through these
+    for (int par = 0; par < 2; ++par)
+      for (int q = 0; q < 4; ++q) {
+        tc::mbar_init(&ctl->xmax_bar[par][q], 64);
+        tc::mbar_init(&ctl->xsum_bar[par][q], 64);
+      }
     ctl->abort_flag = 0;
     tc::fence_barrier_init();
     tc::tma_prefetch_desc(&mapQ);
@@ -282,9 +310,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // --------------------------- softmax + epilogue ---------------------------
+    const int wg = (warp - 2) >> 2;                    // key half of this warpgroup
     const int quarter = warp % 4;
     const int m = quarter * 32 + lane;                 // M row = TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int c_half = wg * 64;                        // first S / O column of this half
     uint32_t uc = 0, bc = 0;
     for (int u = blockIdx.x; u < a.n_units; u += gridDim.x, ++uc) {
       const Unit x = unit_of(a, u);
@@ -292,7 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int hh = m % a.g;
       const bool valid = rl < x.n;
       const int p = a.rows[x.out0 + x.r0 + (valid ? rl : x.n - 1)].pos;
-      float mu = -1e30f, l = 0.f;
+      const int p_first = a.rows[x.out0 + x.r0].pos;   // rows ascend: the tile's smallest
+      float mu = -1e30f, l = 0.f;                      // running max (log2 units), half sum
       bool ok = true;
       for (int j = 0; j < x.nkb; ++j) {
         const uint32_t b = bc + j;
@@ -302,25 +333,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc::tc_fence_after();
-        float s[kKB];
+        float s[64];
         {
-          const uint32_t ts = tmem + lane_off + (b & 1) * kKB;
+          const uint32_t ts = tmem + lane_off + (b & 1) * kKB + c_half;
+          uint32_t r0[32], r1[32];
+          tc::tmem_ld_32x32b_x32(ts, r0);
+          tc::tmem_ld_32x32b_x32(ts + 32, r1);
+          tc::tmem_ld_wait();
 #pragma unroll
-          for (int c0 = 0; c0 < kKB; c0 += 32) {
-            uint32_t r[32];
-            tc::tmem_ld_32x32b_x32(ts + c0, r);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) s[c0 + i] = __uint_as_float(r[i]);
+          for (int i = 0; i < 32; ++i) {
+            s[i] = __uint_as_float(r0[i]);
+            s[32 + i] = __uint_as_float(r1[i]);
           }
         }
-        const int key0 = j * kKB;
+        const int key0 = j * kKB + c_half;
+        if (key0 + 63 > p_first) {                     // warp-uniform: some key may be masked
+#pragma unroll
+          for (int c = 0; c < 64; ++c) s[c] = (key0 + c <= p) ? s[c] : -1e30f;
+        }
         float mx = -1e30f;
 #pragma unroll
-        for (int c = 0; c < kKB; ++c) {
-          s[c] = (key0 + c <= p) ? s[c] * a.scale_log2 : -1e30f;
-          mx = fmaxf(mx, s[c]);
+        for (int c = 0; c < 64; c += 2) mx = max3(mx, s[c], s[c + 1]);
+        ctl->xmax[b & 1][wg][m] = mx;
+        tc::mbar_arrive(&ctl->xmax_bar[b & 1][quarter]);
+        if (!warp_wait_or_abort(&ctl->xmax_bar[b & 1][quarter], (b >> 1) & 1, ctl)) {
+          abort_kernel(ctl, a.err, W_XCHG, j);
+          ok = false;
+          break;
         }
+        mx = fmaxf(mx, ctl->xmax[b & 1][wg ^ 1][m]) * a.scale_log2;
         float mnew = mu;
         bool rescale = false;
         if (j == 0) {
@@ -329,17 +370,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           mnew = mx;
           rescale = true;
         }
-        float sum = 0.f;
-        uint32_t pk[kKB / 2];
+        const float neg = -mnew;
+        float sum0 = 0.f, sum1 = 0.f;
+        uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < kKB; c += 2) {
-          const float p0 = exp2f(s[c] - mnew);
-          const float p1 = exp2f(s[c + 1] - mnew);
-          sum += p0 + p1;
+        for (int c = 0; c < 64; c += 2) {
+          const float p0 = ex2(fmaf(s[c], a.scale_log2, neg));
+          const float p1 = ex2(fmaf(s[c + 1], a.scale_log2, neg));
+          sum0 += p0;
+          sum1 += p1;
           pk[c / 2] = pack_bf16x2(p0, p1);
         }
-        const float alpha = rescale ? exp2f(mu - mnew) : 1.f;
-        l = l * alpha + sum;
+        const float alpha = rescale ? ex2(mu - mnew) : 1.f;
+        l = l * alpha + (sum0 + sum1);
         if (j > 0) {
           if (!warp_wait_or_abort(&ctl->pv_done, (b - 1) & 1, ctl)) {
             abort_kernel(ctl, a.err, W_PV_DONE, j);
@@ -349,11 +392,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tc_fence_after();
         }
         // tcgen05.ld/st are warp-collective (.sync.aligned): the whole warp
-        // rescales when any of its rows needs it (alpha is 1 for the others)
+        // rescales its half of O when any of its rows needs it (alpha is 1
+        // for the others); both warps of a lane quarter decide alike
         if (__any_sync(0xffffffffu, rescale)) {
-          const uint32_t to = tmem + lane_off + 2 * kKB;
+          const uint32_t to = tmem + lane_off + 2 * kKB + c_half;
 #pragma unroll
-          for (int c0 = 0; c0 < kD; c0 += 32) {
+          for (int c0 = 0; c0 < 64; c0 += 32) {
             uint32_t r[32];
             tc::tmem_ld_32x32b_x32(to + c0, r);
             tc::tmem_ld_wait();
@@ -363,14 +407,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc::tmem_st_wait();
         }
-        // P row m into the swizzled K-major layout: 16-byte chunk c of the
-        // 64-column half h lands at chunk (c ^ (m & 7)) of row m
+        // this half of P row m into the swizzled K-major layout: 16-byte
+        // chunk c of the 64-key half lands at chunk (c ^ (m & 7)) of row m
+        uint8_t* prow = sP + wg * kHalf + m * 128;
 #pragma unroll
-        for (int c = 0; c < kKB / 8; ++c) {
-          const int h = c >> 3;
-          const int cc = c & 7;
-          uint4 w = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-          *reinterpret_cast<uint4*>(sP + h * kHalf + m * 128 + ((cc ^ (m & 7)) << 4)) = w;
+        for (int c = 0; c < 8; ++c) {
+          const uint4 w = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          *reinterpret_cast<uint4*>(prow + ((c ^ (m & 7)) << 4)) = w;
         }
         tc::fence_proxy_async_smem();
         tc::tc_fence_before();
@@ -378,18 +421,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         mu = mnew;
       }
       if (!ok) break;
+      ctl->xsum[uc & 1][wg][m] = l;
       if (!warp_wait_or_abort(&ctl->pv_done, (bc + x.nkb - 1) & 1, ctl)) {
         abort_kernel(ctl, a.err, W_PV_LAST, x.nkb);
         break;
       }
       tc::tc_fence_after();
+      tc::mbar_arrive(&ctl->xsum_bar[uc & 1][quarter]);
+      if (!warp_wait_or_abort(&ctl->xsum_bar[uc & 1][quarter], (uc >> 1) & 1, ctl)) {
+        abort_kernel(ctl, a.err, W_XCHG, x.nkb);
+        break;
+      }
       {
-        const float inv = 1.f / l;
-        const uint32_t to = tmem + lane_off + 2 * kKB;
+        const float inv = 1.f / (l + ctl->xsum[uc & 1][wg ^ 1][m]);
+        const uint32_t to = tmem + lane_off + 2 * kKB + c_half;
         __nv_bfloat16* dst =
-            a.O + ((int64_t)(x.out0 + x.r0 + rl) * a.Hq + x.kvh * a.g + hh) * kD;
+            a.O + ((int64_t)(x.out0 + x.r0 + rl) * a.Hq + x.kvh * a.g + hh) * kD + c_half;
 #pragma unroll
-        for (int c0 = 0; c0 < kD; c0 += 32) {
+        for (int c0 = 0; c0 < 64; c0 += 32) {
           uint32_t r[32];
           tc::tmem_ld_32x32b_x32(to + c0, r);
           tc::tmem_ld_wait();
