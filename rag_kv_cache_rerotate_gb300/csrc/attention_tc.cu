@@ -14,9 +14,10 @@
 //                            one 64-key half of the block (the two halves of a
 //                            row exchange their maxima and sums through shared
 //                            memory); causal mask by position on the blocks
-//                            that need it; P written to shared memory in the
-//                            128B-swizzled K-major operand layout
-//   O  += P_b V_b            tcgen05.mma, V read as an MN-major operand
+//                            that need it; P (bf16) stored to one of two TMEM
+//                            P buffers
+//   O  += P_b V_b            tcgen05.mma with A = P in TMEM, V read from
+//                            shared memory as an MN-major operand
 // The running maximum m is raised only when a block exceeds it by more than
 // 2^8 (then O in TMEM and the running sum are rescaled), so most blocks skip
 // the rescale.  Warp 0 issues TMA loads (Q once per unit, K and V blocks into
@@ -43,8 +44,11 @@ constexpr int kTile = 2 * kHalf;              // 32 KB
 constexpr int kStages = 2;
 constexpr int kThreads = 320;                 // producer, MMA, 2 softmax warpgroups
 constexpr int kSoftThreads = 256;
-constexpr int kTmemCols = 512;                // S0 | S1 | O | unused
-constexpr int kSmemBytes = (2 + 2 * kStages) * kTile + 1024 + 8192;
+constexpr int kTmemCols = 512;                // S0 | S1 | O | P0 | P1
+constexpr int kColS = 0;                      // + 128 * (b & 1)
+constexpr int kColO = 256;
+constexpr int kColP = 384;                    // + 64 * (b & 1); bf16 pairs
+constexpr int kSmemBytes = (1 + 2 * kStages) * kTile + 1024 + 8192;
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
 
 struct AttnTile {
@@ -70,7 +74,7 @@ struct Ctl {
   uint64_t q_full, q_empty;
   uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
   uint64_t s_full[2];
-  uint64_t p_full, pv_done, o_empty;
+  uint64_t p_full[2], pv_done[2], o_empty;   // [block parity]
   uint32_t tmem_base;
   volatile int abort_flag;
   uint64_t xmax_bar[2][4];  // [block parity][lane quarter]: both half-row maxima written
@@ -146,9 +150,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
-  uint8_t* sP = smem + kTile;
-  uint8_t* sK = smem + 2 * kTile;                   // stage s: K at sK + 2s*kTile, V after it
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + (2 + 2 * kStages) * kTile);
+  uint8_t* sK = smem + kTile;                       // stage s: K at sK + 2s*kTile, V after it
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + (1 + 2 * kStages) * kTile);
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
@@ -162,8 +165,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::mbar_init(&ctl->s_full[0], 1);
     tc::mbar_init(&ctl->s_full[1], 1);
-    tc::mbar_init(&ctl->p_full, kSoftThreads);
-    tc::mbar_init(&ctl->pv_done, 1);
+    for (int par = 0; par < 2; ++par) {
+      tc::mbar_init(&ctl->p_full[par], kSoftThreads);
+      tc::mbar_init(&ctl->pv_done[par], 1);
+    }
     tc::mbar_init(&ctl->o_empty, kSoftThreads);
     // the two warps (one per softmax warpgroup) owning a TMEM lane quarter
     // exchange half-row values through these
@@ -232,7 +237,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_s = tc::idesc_bf16_f32(128, kKB);
       const uint32_t idesc_o = tc::idesc_bf16_f32(128, kD, /*b_mn_major=*/true);
       const uint32_t q_addr = tc::smem_u32(sQ);
-      const uint32_t p_addr = tc::smem_u32(sP);
       uint32_t uc = 0, kvc = 0, bc = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x, ++uc) {
@@ -251,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc::tc_fence_after();
           const uint32_t kaddr = tc::smem_u32(sK + 2 * st * kTile);
-          const uint32_t d = tmem + (bc & 1) * kKB;
+          const uint32_t d = tmem + kColS + (bc & 1) * kKB;
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk)
             tc::mma_bf16(d, kmajor_step(q_addr, kk), kmajor_step(kaddr, kk), idesc_s, kk != 0);
@@ -269,13 +273,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc::tc_fence_after();
             const uint32_t kaddr = tc::smem_u32(sK + 2 * st1 * kTile);
-            const uint32_t d = tmem + ((b + 1) & 1) * kKB;
+            const uint32_t d = tmem + kColS + ((b + 1) & 1) * kKB;
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk)
               tc::mma_bf16(d, kmajor_step(q_addr, kk), kmajor_step(kaddr, kk), idesc_s, kk != 0);
             tc::mma_commit(&ctl->s_full[(b + 1) & 1]);
           }
-          if (!wait_or_abort(&ctl->p_full, b & 1, ctl)) {
+          if (!wait_or_abort(&ctl->p_full[b & 1], (b >> 1) & 1, ctl)) {
             abort_kernel(ctl, a.err, W_P_FULL, j);
             ok = false;
             break;
@@ -293,13 +297,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc::tc_fence_after();
           const uint32_t vaddr = tc::smem_u32(sK + (2 * st + 1) * kTile);
-          const uint32_t o = tmem + 2 * kKB;
+          const uint32_t o = tmem + kColO;
+          const uint32_t pa = tmem + kColP + (b & 1) * (kKB / 2);
 #pragma unroll
           for (int kk = 0; kk < kKB / 16; ++kk)
-            tc::mma_bf16(o, kmajor_step(p_addr, kk),
-                         tc::smem_desc_mn128(vaddr + kk * 16 * 128, kHalf), idesc_o,
-                         (j | kk) != 0);
-          tc::mma_commit(&ctl->pv_done);
+            tc::mma_bf16_ts(o, pa + kk * 8, tc::smem_desc_mn128(vaddr + kk * 16 * 128, kHalf),
+                            idesc_o, (j | kk) != 0);
+          tc::mma_commit(&ctl->pv_done[b & 1]);
           tc::mma_commit(&ctl->kv_empty[st]);
         }
         if (!ok) break;
@@ -335,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tc_fence_after();
         float s[64];
         {
-          const uint32_t ts = tmem + lane_off + (b & 1) * kKB + c_half;
+          const uint32_t ts = tmem + lane_off + kColS + (b & 1) * kKB + c_half;
           uint32_t r0[32], r1[32];
           tc::tmem_ld_32x32b_x32(ts, r0);
           tc::tmem_ld_32x32b_x32(ts + 32, r1);
@@ -383,8 +387,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float alpha = rescale ? ex2(mu - mnew) : 1.f;
         l = l * alpha + (sum0 + sum1);
-        if (j > 0) {
-          if (!warp_wait_or_abort(&ctl->pv_done, (b - 1) & 1, ctl)) {
+        // P buffer b & 1 was last read by the P.V of block b - 2; a rescale of
+        // O also needs the P.V of block b - 1 done (commits complete in order)
+        const bool any_rescale = __any_sync(0xffffffffu, rescale);
+        if (j >= 1 && (any_rescale || j >= 2)) {
+          const uint32_t wb = any_rescale ? b - 1 : b - 2;
+          if (!warp_wait_or_abort(&ctl->pv_done[wb & 1], (wb >> 1) & 1, ctl)) {
             abort_kernel(ctl, a.err, W_PV_DONE, j);
             ok = false;
             break;
@@ -394,8 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // tcgen05.ld/st are warp-collective (.sync.aligned): the whole warp
         // rescales its half of O when any of its rows needs it (alpha is 1
         // for the others); both warps of a lane quarter decide alike
-        if (__any_sync(0xffffffffu, rescale)) {
-          const uint32_t to = tmem + lane_off + 2 * kKB + c_half;
+        if (any_rescale) {
+          const uint32_t to = tmem + lane_off + kColO + c_half;
 #pragma unroll
           for (int c0 = 0; c0 < 64; c0 += 32) {
             uint32_t r[32];
@@ -405,24 +413,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
             tc::tmem_st_32x32b_x32(to + c0, r);
           }
-          tc::tmem_st_wait();
         }
-        // this half of P row m into the swizzled K-major layout: 16-byte
-        // chunk c of the 64-key half lands at chunk (c ^ (m & 7)) of row m
-        uint8_t* prow = sP + wg * kHalf + m * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 w = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-          *reinterpret_cast<uint4*>(prow + ((c ^ (m & 7)) << 4)) = w;
-        }
-        tc::fence_proxy_async_smem();
+        // this half of P row m: 64 bf16 in 32 TMEM columns
+        tc::tmem_st_32x32b_x32(tmem + lane_off + kColP + (b & 1) * (kKB / 2) + wg * 32, pk);
+        tc::tmem_st_wait();
         tc::tc_fence_before();
-        tc::mbar_arrive(&ctl->p_full);
+        tc::mbar_arrive(&ctl->p_full[b & 1]);
         mu = mnew;
       }
       if (!ok) break;
       ctl->xsum[uc & 1][wg][m] = l;
-      if (!warp_wait_or_abort(&ctl->pv_done, (bc + x.nkb - 1) & 1, ctl)) {
+      const uint32_t last = bc + x.nkb - 1;
+      if (!warp_wait_or_abort(&ctl->pv_done[last & 1], (last >> 1) & 1, ctl)) {
         abort_kernel(ctl, a.err, W_PV_LAST, x.nkb);
         break;
       }
@@ -434,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       {
         const float inv = 1.f / (l + ctl->xsum[uc & 1][wg ^ 1][m]);
-        const uint32_t to = tmem + lane_off + 2 * kKB + c_half;
+        const uint32_t to = tmem + lane_off + kColO + c_half;
         __nv_bfloat16* dst =
             a.O + ((int64_t)(x.out0 + x.r0 + rl) * a.Hq + x.kvh * a.g + hh) * kD + c_half;
 #pragma unroll
