@@ -10,19 +10,23 @@
 // rows of the MMA (row r, head hh -> M row r * g + hh).  Keys stream in
 // blocks of 128 up to the tile's last position:
 //   S_b = Q K_b^T            tcgen05.mma into one of two TMEM S buffers
-//   P_b = exp2(S_b - m)      two softmax warpgroups, each thread one M row and
-//                            one 64-key half of the block (the two halves of a
-//                            row exchange their maxima and sums through shared
-//                            memory); causal mask by position on the blocks
-//                            that need it; P (bf16) stored to one of two TMEM
-//                            P buffers
+//   P_b = exp2(S_b - m)      four softmax warpgroups, each thread one M row and
+//                            one 32-key quarter of the block (the quarters of
+//                            a row exchange their maxima and sums through
+//                            shared memory); causal mask by position on the
+//                            blocks that need it; P (bf16) stored to one of
+//                            two TMEM P buffers
 //   O  += P_b V_b            tcgen05.mma with A = P in TMEM, V read from
 //                            shared memory as an MN-major operand
 // The running maximum m is raised only when a block exceeds it by more than
 // 2^8 (then O in TMEM and the running sum are rescaled), so most blocks skip
-// the rescale.  Warp 0 issues TMA loads (Q once per unit, K and V blocks into
-// a 2-stage ring), warp 1 issues the MMAs, warps 2-9 run the softmax and the
-// epilogue.  The kernel is persistent; units are taken heaviest first.
+// the rescale.  Six roles run decoupled, each behind its own mbarriers:
+// warp 0 loads Q and K blocks (3-stage ring), warp 18 loads V blocks (2-stage
+// ring), warp 1 issues the S MMAs, warp 19 the P.V MMAs, warps 2-17 run the
+// softmax and the epilogue.  A K stage is released as soon as its S MMA has
+// completed and an S buffer as soon as the softmax has read it, so loads and
+// S MMAs run ahead of the softmax.  The kernel is persistent; units are taken
+// heaviest first.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -41,14 +45,19 @@ constexpr int kD = 128;
 constexpr int kKB = 128;                      // keys per block
 constexpr int kHalf = 128 * 64 * 2;           // one 64-column half of a 128-row tile (16 KB)
 constexpr int kTile = 2 * kHalf;              // 32 KB
-constexpr int kStages = 2;
-constexpr int kThreads = 320;                 // producer, MMA, 2 softmax warpgroups
-constexpr int kSoftThreads = 256;
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
+constexpr int kWG = 4;                        // softmax warpgroups
+constexpr int kCols = kKB / kWG;              // keys of a block per softmax thread
+constexpr int kSoftThreads = 128 * kWG;
+constexpr int kThreads = 128 + kSoftThreads;  // K/Q loads, S MMAs, softmax, V loads, P.V MMAs
+constexpr int kWarpVLoad = 2 + kSoftThreads / 32;
+constexpr int kWarpPV = kWarpVLoad + 1;
 constexpr int kTmemCols = 512;                // S0 | S1 | O | P0 | P1
 constexpr int kColS = 0;                      // + 128 * (b & 1)
 constexpr int kColO = 256;
 constexpr int kColP = 384;                    // + 64 * (b & 1); bf16 pairs
-constexpr int kSmemBytes = (1 + 2 * kStages) * kTile + 1024 + 8192;
+constexpr int kSmemBytes = (1 + kKStages + kVStages) * kTile + 1024 + 12288;
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
 
 struct AttnTile {
@@ -72,15 +81,16 @@ struct AttnArgs {
 
 struct Ctl {
   uint64_t q_full, q_empty;
-  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
-  uint64_t s_full[2];
+  uint64_t k_full[kKStages], k_empty[kKStages];
+  uint64_t v_full[kVStages], v_empty[kVStages];
+  uint64_t s_full[2], s_empty[2];
   uint64_t p_full[2], pv_done[2], o_empty;   // [block parity]
   uint32_t tmem_base;
   volatile int abort_flag;
-  uint64_t xmax_bar[2][4];  // [block parity][lane quarter]: both half-row maxima written
-  uint64_t xsum_bar[2][4];  // [unit parity][lane quarter]: both half-row sums written
-  float xmax[2][2][128];     // [block parity][warpgroup][row]: half-row maxima
-  float xsum[2][2][128];     // [unit parity][warpgroup][row]: half-row sums
+  uint64_t xmax_bar[2][4];  // [block parity][lane quarter]: all partial row maxima written
+  uint64_t xsum_bar[2][4];  // [unit parity][lane quarter]: all partial row sums written
+  float xmax[2][kWG][128];   // [block parity][warpgroup][row]: partial row maxima
+  float xsum[2][kWG][128];   // [unit parity][warpgroup][row]: partial row sums
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ctl* ctl) {
@@ -94,8 +104,8 @@ __device__ __forceinline__ bool warp_wait_or_abort(uint64_t* bar, uint32_t parit
 
 // Which wait gave up: info = wait id (4 bits) << 20 | CTA (8 bits) << 12 | key block (12 bits).
 enum AttnWait : uint32_t {
-  W_Q_EMPTY = 1, W_KV_EMPTY, W_Q_FULL, W_K_FULL0, W_K_FULL, W_P_FULL, W_O_EMPTY, W_V_FULL,
-  W_S_FULL, W_PV_DONE, W_PV_LAST, W_XCHG
+  W_Q_EMPTY = 1, W_K_EMPTY, W_V_EMPTY, W_Q_FULL, W_K_FULL, W_S_EMPTY, W_P_FULL, W_O_EMPTY,
+  W_V_FULL, W_S_FULL, W_PV_DONE, W_PV_LAST, W_XCHG
 };
 
 __device__ __forceinline__ void abort_kernel(Ctl* ctl, uint32_t* err, uint32_t which = 0,
@@ -150,32 +160,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
-  uint8_t* sK = smem + kTile;                       // stage s: K at sK + 2s*kTile, V after it
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + (1 + 2 * kStages) * kTile);
+  uint8_t* sK = smem + kTile;                       // K stage s at sK + s * kTile
+  uint8_t* sV = sK + kKStages * kTile;              // V stage s at sV + s * kTile
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + (1 + kKStages + kVStages) * kTile);
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
     tc::mbar_init(&ctl->q_full, 1);
     tc::mbar_init(&ctl->q_empty, 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       tc::mbar_init(&ctl->k_full[s], 1);
-      tc::mbar_init(&ctl->v_full[s], 1);
-      tc::mbar_init(&ctl->kv_empty[s], 1);
+      tc::mbar_init(&ctl->k_empty[s], 1);
     }
-    tc::mbar_init(&ctl->s_full[0], 1);
-    tc::mbar_init(&ctl->s_full[1], 1);
+    for (int s = 0; s < kVStages; ++s) {
+      tc::mbar_init(&ctl->v_full[s], 1);
+      tc::mbar_init(&ctl->v_empty[s], 1);
+    }
+    for (int par = 0; par < 2; ++par) {
+      tc::mbar_init(&ctl->s_full[par], 1);
+      tc::mbar_init(&ctl->s_empty[par], kSoftThreads);
+    }
     for (int par = 0; par < 2; ++par) {
       tc::mbar_init(&ctl->p_full[par], kSoftThreads);
       tc::mbar_init(&ctl->pv_done[par], 1);
     }
     tc::mbar_init(&ctl->o_empty, kSoftThreads);
-    // the two warps (one per softmax warpgroup) owning a TMEM lane quarter
-    // exchange half-row values through these
+    // the warps (one per softmax warpgroup) owning a TMEM lane quarter
+    // exchange partial row values through these
     for (int par = 0; par < 2; ++par)
       for (int q = 0; q < 4; ++q) {
-        tc::mbar_init(&ctl->xmax_bar[par][q], 64);
-        tc::mbar_init(&ctl->xsum_bar[par][q], 64);
+        tc::mbar_init(&ctl->xmax_bar[par][q], 32 * kWG);
+        tc::mbar_init(&ctl->xsum_bar[par][q], 32 * kWG);
       }
     ctl->abort_flag = 0;
     tc::fence_barrier_init();
@@ -190,9 +206,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = ctl->tmem_base;
 
   if (warp == 0) {
-    // ------------------------------ TMA producer ------------------------------
+    // --------------------------- Q and K loads ---------------------------
     if (lane == 0) {
-      uint32_t uc = 0, kvc = 0;
+      uint32_t uc = 0, kc = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x, ++uc) {
         const Unit x = unit_of(a, u);
@@ -203,41 +219,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_arrive_expect_tx(&ctl->q_full, kTile);
         tc::tma_load_3d(sQ, &mapQ, &ctl->q_full, 0, x.kvh * a.g, x.out0 + x.r0);
         tc::tma_load_3d(sQ + kHalf, &mapQ, &ctl->q_full, 64, x.kvh * a.g, x.out0 + x.r0);
-        for (int j = 0; j < x.nkb; ++j, ++kvc) {
-          const int st = kvc & 1;
-          if (!wait_or_abort(&ctl->kv_empty[st], ((kvc >> 1) & 1) ^ 1, ctl)) {
-            abort_kernel(ctl, a.err, W_KV_EMPTY, j);
+        for (int j = 0; j < x.nkb; ++j, ++kc) {
+          const int st = kc % kKStages;
+          if (!wait_or_abort(&ctl->k_empty[st], ((kc / kKStages) & 1) ^ 1, ctl)) {
+            abort_kernel(ctl, a.err, W_K_EMPTY, j);
             ok = false;
             break;
           }
-          uint8_t* k = sK + 2 * st * kTile;
-          uint8_t* v = k + kTile;
+          uint8_t* k = sK + st * kTile;
           const int z = x.row0 + j * kKB;
           tc::mbar_arrive_expect_tx(&ctl->k_full[st], kTile);
           tc::tma_load_3d(k, &mapK, &ctl->k_full[st], 0, x.kvh, z);
           tc::tma_load_3d(k + kHalf, &mapK, &ctl->k_full[st], 64, x.kvh, z);
+        }
+      }
+      // let copies in flight land before the CTA may exit
+      tc::mbar_wait(&ctl->q_full, (uc & 1) ^ 1);
+      for (uint32_t i = (kc > (uint32_t)kKStages ? kc - kKStages : 0); i < kc; ++i)
+        tc::mbar_wait(&ctl->k_full[i % kKStages], (i / kKStages) & 1);
+    }
+  } else if (warp == kWarpVLoad) {
+    // ------------------------------ V loads ------------------------------
+    if (lane == 0) {
+      uint32_t vc = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
+        const Unit x = unit_of(a, u);
+        for (int j = 0; j < x.nkb; ++j, ++vc) {
+          const int st = vc % kVStages;
+          if (!wait_or_abort(&ctl->v_empty[st], ((vc / kVStages) & 1) ^ 1, ctl)) {
+            abort_kernel(ctl, a.err, W_V_EMPTY, j);
+            ok = false;
+            break;
+          }
+          uint8_t* v = sV + st * kTile;
+          const int z = x.row0 + j * kKB;
           tc::mbar_arrive_expect_tx(&ctl->v_full[st], kTile);
           tc::tma_load_3d(v, &mapV, &ctl->v_full[st], 0, x.kvh, z);
           tc::tma_load_3d(v + kHalf, &mapV, &ctl->v_full[st], 64, x.kvh, z);
         }
       }
-      // let copies in flight land before the CTA may exit
-      tc::mbar_wait(&ctl->q_full, (uc & 1) ^ 1);
-      for (int s = 0; s < kStages; ++s) {
-        if (kvc > (uint32_t)s) {
-          const uint32_t last = kvc - 1 - ((kvc - 1 - s) & 1);   // last use of stage s
-          tc::mbar_wait(&ctl->k_full[s], (last >> 1) & 1);
-          tc::mbar_wait(&ctl->v_full[s], (last >> 1) & 1);
-        }
-      }
+      for (uint32_t i = (vc > (uint32_t)kVStages ? vc - kVStages : 0); i < vc; ++i)
+        tc::mbar_wait(&ctl->v_full[i % kVStages], (i / kVStages) & 1);
     }
   } else if (warp == 1) {
-    // ------------------------------ MMA issuer ------------------------------
+    // ------------------------------ S = Q K^T ------------------------------
     if (lane == 0) {
       const uint32_t idesc_s = tc::idesc_bf16_f32(128, kKB);
-      const uint32_t idesc_o = tc::idesc_bf16_f32(128, kD, /*b_mn_major=*/true);
       const uint32_t q_addr = tc::smem_u32(sQ);
-      uint32_t uc = 0, kvc = 0, bc = 0;
+      uint32_t uc = 0, kc = 0, bc = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x, ++uc) {
         const Unit x = unit_of(a, u);
@@ -245,40 +275,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           abort_kernel(ctl, a.err, W_Q_FULL, 0);
           break;
         }
-        tc::tc_fence_after();
-        // S of block 0
-        {
-          const int st = kvc & 1;
-          if (!wait_or_abort(&ctl->k_full[st], (kvc >> 1) & 1, ctl)) {
-            abort_kernel(ctl, a.err, W_K_FULL0, 0);
+        for (int j = 0; j < x.nkb; ++j, ++kc) {
+          const uint32_t b = bc + j;
+          const int st = kc % kKStages;
+          if (!wait_or_abort(&ctl->k_full[st], (kc / kKStages) & 1, ctl)) {
+            abort_kernel(ctl, a.err, W_K_FULL, j);
+            ok = false;
+            break;
+          }
+          // S buffer b & 1 is free once the softmax has read S of block b - 2
+          if (b >= 2 && !wait_or_abort(&ctl->s_empty[b & 1], ((b - 2) >> 1) & 1, ctl)) {
+            abort_kernel(ctl, a.err, W_S_EMPTY, j);
+            ok = false;
             break;
           }
           tc::tc_fence_after();
-          const uint32_t kaddr = tc::smem_u32(sK + 2 * st * kTile);
-          const uint32_t d = tmem + kColS + (bc & 1) * kKB;
+          const uint32_t kaddr = tc::smem_u32(sK + st * kTile);
+          const uint32_t d = tmem + kColS + (b & 1) * kKB;
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk)
             tc::mma_bf16(d, kmajor_step(q_addr, kk), kmajor_step(kaddr, kk), idesc_s, kk != 0);
-          tc::mma_commit(&ctl->s_full[bc & 1]);
+          tc::mma_commit(&ctl->s_full[b & 1]);
+          tc::mma_commit(&ctl->k_empty[st]);
         }
-        for (int j = 0; j < x.nkb; ++j) {
+        if (!ok) break;
+        tc::mma_commit(&ctl->q_empty);
+        bc += x.nkb;
+      }
+    }
+  } else if (warp == kWarpPV) {
+    // ------------------------------ O += P V ------------------------------
+    if (lane == 0) {
+      const uint32_t idesc_o = tc::idesc_bf16_f32(128, kD, /*b_mn_major=*/true);
+      uint32_t uc = 0, vc = 0, bc = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x, ++uc) {
+        const Unit x = unit_of(a, u);
+        for (int j = 0; j < x.nkb; ++j, ++vc) {
           const uint32_t b = bc + j;
-          const uint32_t kv = kvc + j;
-          if (j + 1 < x.nkb) {
-            const int st1 = (kv + 1) & 1;
-            if (!wait_or_abort(&ctl->k_full[st1], ((kv + 1) >> 1) & 1, ctl)) {
-              abort_kernel(ctl, a.err, W_K_FULL, j);
-              ok = false;
-              break;
-            }
-            tc::tc_fence_after();
-            const uint32_t kaddr = tc::smem_u32(sK + 2 * st1 * kTile);
-            const uint32_t d = tmem + kColS + ((b + 1) & 1) * kKB;
-#pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk)
-              tc::mma_bf16(d, kmajor_step(q_addr, kk), kmajor_step(kaddr, kk), idesc_s, kk != 0);
-            tc::mma_commit(&ctl->s_full[(b + 1) & 1]);
-          }
           if (!wait_or_abort(&ctl->p_full[b & 1], (b >> 1) & 1, ctl)) {
             abort_kernel(ctl, a.err, W_P_FULL, j);
             ok = false;
@@ -289,14 +323,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          const int st = kv & 1;
-          if (!wait_or_abort(&ctl->v_full[st], (kv >> 1) & 1, ctl)) {
+          const int st = vc % kVStages;
+          if (!wait_or_abort(&ctl->v_full[st], (vc / kVStages) & 1, ctl)) {
             abort_kernel(ctl, a.err, W_V_FULL, j);
             ok = false;
             break;
           }
           tc::tc_fence_after();
-          const uint32_t vaddr = tc::smem_u32(sK + (2 * st + 1) * kTile);
+          const uint32_t vaddr = tc::smem_u32(sV + st * kTile);
           const uint32_t o = tmem + kColO;
           const uint32_t pa = tmem + kColP + (b & 1) * (kKB / 2);
 #pragma unroll
@@ -304,21 +338,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mma_bf16_ts(o, pa + kk * 8, tc::smem_desc_mn128(vaddr + kk * 16 * 128, kHalf),
                             idesc_o, (j | kk) != 0);
           tc::mma_commit(&ctl->pv_done[b & 1]);
-          tc::mma_commit(&ctl->kv_empty[st]);
+          tc::mma_commit(&ctl->v_empty[st]);
         }
-        if (!ok) break;
-        tc::mma_commit(&ctl->q_empty);
         bc += x.nkb;
-        kvc += x.nkb;
       }
     }
   } else {
     // --------------------------- softmax + epilogue ---------------------------
-    const int wg = (warp - 2) >> 2;                    // key half of this warpgroup
-    const int quarter = warp % 4;
+    const int wg = (warp - 2) >> 2;                    // key quarter of this warpgroup
+    const int quarter = warp % 4;                      // TMEM lane quarter
     const int m = quarter * 32 + lane;                 // M row = TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const int c_half = wg * 64;                        // first S / O column of this half
+    const int c_off = wg * kCols;                      // first S / O column of this thread
     uint32_t uc = 0, bc = 0;
     for (int u = blockIdx.x; u < a.n_units; u += gridDim.x, ++uc) {
       const Unit x = unit_of(a, u);
@@ -327,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = rl < x.n;
       const int p = a.rows[x.out0 + x.r0 + (valid ? rl : x.n - 1)].pos;
       const int p_first = a.rows[x.out0 + x.r0].pos;   // rows ascend: the tile's smallest
-      float mu = -1e30f, l = 0.f;                      // running max (log2 units), half sum
+      float mu = -1e30f, l = 0.f;                      // running max (log2 units), partial sum
       bool ok = true;
       for (int j = 0; j < x.nkb; ++j) {
         const uint32_t b = bc + j;
@@ -337,27 +368,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc::tc_fence_after();
-        float s[64];
+        float s[kCols];
         {
-          const uint32_t ts = tmem + lane_off + kColS + (b & 1) * kKB + c_half;
-          uint32_t r0[32], r1[32];
-          tc::tmem_ld_32x32b_x32(ts, r0);
-          tc::tmem_ld_32x32b_x32(ts + 32, r1);
+          uint32_t r[32];
+          tc::tmem_ld_32x32b_x32(tmem + lane_off + kColS + (b & 1) * kKB + c_off, r);
           tc::tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            s[i] = __uint_as_float(r0[i]);
-            s[32 + i] = __uint_as_float(r1[i]);
-          }
+          for (int i = 0; i < kCols; ++i) s[i] = __uint_as_float(r[i]);
         }
-        const int key0 = j * kKB + c_half;
-        if (key0 + 63 > p_first) {                     // warp-uniform: some key may be masked
+        tc::tc_fence_before();
+        tc::mbar_arrive(&ctl->s_empty[b & 1]);
+        const int key0 = j * kKB + c_off;
+        if (key0 + kCols - 1 > p_first) {              // warp-uniform: some key may be masked
 #pragma unroll
-          for (int c = 0; c < 64; ++c) s[c] = (key0 + c <= p) ? s[c] : -1e30f;
+          for (int c = 0; c < kCols; ++c) s[c] = (key0 + c <= p) ? s[c] : -1e30f;
         }
-        float mx = -1e30f;
+        float mx;
+        {                                              // tree maximum of the 32 scores
+          float t[11];
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) mx = max3(mx, s[c], s[c + 1]);
+          for (int i = 0; i < 10; ++i) t[i] = max3(s[3 * i], s[3 * i + 1], s[3 * i + 2]);
+          t[10] = fmaxf(s[30], s[31]);
+          const float u0 = max3(t[0], t[1], t[2]), u1 = max3(t[3], t[4], t[5]);
+          const float u2 = max3(t[6], t[7], t[8]), u3 = fmaxf(t[9], t[10]);
+          mx = fmaxf(max3(u0, u1, u2), u3);
+        }
         ctl->xmax[b & 1][wg][m] = mx;
         tc::mbar_arrive(&ctl->xmax_bar[b & 1][quarter]);
         if (!warp_wait_or_abort(&ctl->xmax_bar[b & 1][quarter], (b >> 1) & 1, ctl)) {
@@ -365,7 +400,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        mx = fmaxf(mx, ctl->xmax[b & 1][wg ^ 1][m]) * a.scale_log2;
+        {
+          const float* xm = &ctl->xmax[b & 1][0][m];
+          mx = fmaxf(max3(xm[0], xm[128], xm[256]), xm[384]) * a.scale_log2;
+        }
         float mnew = mu;
         bool rescale = false;
         if (j == 0) {
@@ -375,18 +413,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           rescale = true;
         }
         const float neg = -mnew;
-        float sum0 = 0.f, sum1 = 0.f;
-        uint32_t pk[32];
+        float e[kCols];
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const float p0 = ex2(fmaf(s[c], a.scale_log2, neg));
-          const float p1 = ex2(fmaf(s[c + 1], a.scale_log2, neg));
-          sum0 += p0;
-          sum1 += p1;
-          pk[c / 2] = pack_bf16x2(p0, p1);
+        for (int c = 0; c < kCols; ++c) e[c] = ex2(fmaf(s[c], a.scale_log2, neg));
+        uint32_t pk[kCols / 2];
+#pragma unroll
+        for (int c = 0; c < kCols; c += 2) pk[c / 2] = pack_bf16x2(e[c], e[c + 1]);
+        float sum;
+        {                                              // tree sum of the 32 probabilities
+#pragma unroll
+          for (int w = kCols / 2; w >= 1; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i) e[i] += e[i + w];
+          sum = e[0];
         }
         const float alpha = rescale ? ex2(mu - mnew) : 1.f;
-        l = l * alpha + (sum0 + sum1);
+        l = l * alpha + sum;
         // P buffer b & 1 was last read by the P.V of block b - 2; a rescale of
         // O also needs the P.V of block b - 1 done (commits complete in order)
         const bool any_rescale = __any_sync(0xffffffffu, rescale);
@@ -400,22 +442,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tc_fence_after();
         }
         // tcgen05.ld/st are warp-collective (.sync.aligned): the whole warp
-        // rescales its half of O when any of its rows needs it (alpha is 1
-        // for the others); both warps of a lane quarter decide alike
+        // rescales its columns of O when any of its rows needs it (alpha is 1
+        // for the others); all warps of a lane quarter decide alike
         if (any_rescale) {
-          const uint32_t to = tmem + lane_off + kColO + c_half;
+          uint32_t r[32];
+          const uint32_t to = tmem + lane_off + kColO + c_off;
+          tc::tmem_ld_32x32b_x32(to, r);
+          tc::tmem_ld_wait();
 #pragma unroll
-          for (int c0 = 0; c0 < 64; c0 += 32) {
-            uint32_t r[32];
-            tc::tmem_ld_32x32b_x32(to + c0, r);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tc::tmem_st_32x32b_x32(to + c0, r);
-          }
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          tc::tmem_st_32x32b_x32(to, r);
         }
-        // this half of P row m: 64 bf16 in 32 TMEM columns
-        tc::tmem_st_32x32b_x32(tmem + lane_off + kColP + (b & 1) * (kKB / 2) + wg * 32, pk);
+        // this thread's 32 keys of P row m: 32 bf16 in 16 TMEM columns
+        tc::tmem_st_32x32b_x16(tmem + lane_off + kColP + (b & 1) * (kKB / 2) + wg * (kCols / 2), pk);
         tc::tmem_st_wait();
         tc::tc_fence_before();
         tc::mbar_arrive(&ctl->p_full[b & 1]);
@@ -435,25 +474,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       {
-        const float inv = 1.f / (l + ctl->xsum[uc & 1][wg ^ 1][m]);
-        const uint32_t to = tmem + lane_off + kColO + c_half;
+        const float* xs = &ctl->xsum[uc & 1][0][m];
+        const float inv = 1.f / ((xs[0] + xs[128]) + (xs[256] + xs[384]));
         __nv_bfloat16* dst =
-            a.O + ((int64_t)(x.out0 + x.r0 + rl) * a.Hq + x.kvh * a.g + hh) * kD + c_half;
+            a.O + ((int64_t)(x.out0 + x.r0 + rl) * a.Hq + x.kvh * a.g + hh) * kD + c_off;
+        uint32_t r[32];
+        tc::tmem_ld_32x32b_x32(tmem + lane_off + kColO + c_off, r);
+        tc::tmem_ld_wait();
+        if (valid) {
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 32) {
-          uint32_t r[32];
-          tc::tmem_ld_32x32b_x32(to + c0, r);
-          tc::tmem_ld_wait();
-          if (valid) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(r[8 * q + 0]) * inv, __uint_as_float(r[8 * q + 1]) * inv);
-              w.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]) * inv, __uint_as_float(r[8 * q + 3]) * inv);
-              w.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]) * inv, __uint_as_float(r[8 * q + 5]) * inv);
-              w.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]) * inv, __uint_as_float(r[8 * q + 7]) * inv);
-              reinterpret_cast<uint4*>(dst + c0)[q] = w;
-            }
+          for (int q = 0; q < 4; ++q) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(r[8 * q + 0]) * inv, __uint_as_float(r[8 * q + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]) * inv, __uint_as_float(r[8 * q + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]) * inv, __uint_as_float(r[8 * q + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]) * inv, __uint_as_float(r[8 * q + 7]) * inv);
+            reinterpret_cast<uint4*>(dst)[q] = w;
           }
         }
       }
