@@ -9,12 +9,15 @@
 //     over the gathered rows S, RoPE at each row's request position on Q and
 //     K heads, Q to a compact buffer, K and V scattered into the fused cache.
 //
-// One 128 x 128 output tile is one head of 128 rows, so every epilogue sees
-// whole heads.  The kernel is persistent (one CTA per SM) and warp
-// specialised: warp 0 issues TMA loads into a 6-stage shared-memory ring,
-// warp 1 issues tcgen05.mma into one of two TMEM accumulators, warps 2-5
-// drain the other accumulator through tcgen05.ld and run the epilogue, so
-// the epilogue of tile i overlaps the main loop of tile i + 1.
+// One 128 x 256 output tile is two heads of 128 rows, so every epilogue sees
+// whole heads; its 256 B rows are loaded as two 128-row halves, each from the
+// weight matrix of its own head.  The wide tile halves the operand bytes each
+// SM must take in per flop compared with 128 x 128.  The kernel is persistent
+// (one CTA per SM) and warp specialised: warp 0 issues TMA loads into a
+// 4-stage shared-memory ring, warp 1 issues tcgen05.mma into one of two TMEM
+// accumulators, warps 2-9 (one warpgroup per head of the tile) drain the other
+// accumulator through tcgen05.ld and run the epilogue, so the epilogue of tile
+// i overlaps the main loop of tile i + 1.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -28,14 +31,16 @@ namespace fusekv {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = 128;
+constexpr int BN = 128;                             // one head
+constexpr int BN2 = 2 * BN;                         // one tile: two heads
 constexpr int BK = 64;
-constexpr int STAGES = 6;
-constexpr int kTileBytes = BM * BK * 2;             // 16 KB per operand tile
-constexpr int kStageBytes = 2 * kTileBytes;
-constexpr int kAccCols = 128;
-constexpr int kTmemCols = 2 * kAccCols;
-constexpr int kThreads = 192;                       // 6 warps
+constexpr int STAGES = 4;
+constexpr int kTileBytes = BM * BK * 2;             // 16 KB: A, or one head's B half
+constexpr int kStageBytes = 3 * kTileBytes;         // A + two B halves
+constexpr int kAccCols = BN2;
+constexpr int kTmemCols = 2 * kAccCols;             // two accumulators: all 512 columns
+constexpr int kEpiThreads = 256;                    // two warpgroups, one per head
+constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kSmemBytes = STAGES * kStageBytes + 1024 + 256;
 
 enum Mode : int { MODE_DEVIATION = 0, MODE_RECOMPUTE = 1 };
@@ -45,7 +50,7 @@ struct TcArgs {
   int K;                 // hidden
   int m_tiles;
   int n_tiles;
-  int nt0, nt1;          // n-tiles taken by B map 0 and 1 (map 2 takes the rest)
+  int h0, h1;            // heads taken by B map 0 and 1 (map 2 takes the rest)
   int mode;
   int n_q_heads;
   int n_kv_heads;
@@ -192,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&ctl->tfull[b], 1);
-      tc::mbar_init(&ctl->tempty[b], 4 * 32);
+      tc::mbar_init(&ctl->tempty[b], kEpiThreads);
     }
     ctl->abort_flag = 0;
     tc::fence_barrier_init();
@@ -219,17 +224,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         const int mt = tile % a.m_tiles;
         const int nt = tile / a.m_tiles;
-        const CUtensorMap* mb;
-        int nrow;
-        if (nt < a.nt0) {
-          mb = &mapB0;
-          nrow = nt * BN;
-        } else if (nt < a.nt0 + a.nt1) {
-          mb = &mapB1;
-          nrow = (nt - a.nt0) * BN;
-        } else {
-          mb = &mapB2;
-          nrow = (nt - a.nt0 - a.nt1) * BN;
+        const CUtensorMap* mb[2];
+        int nrow[2];
+        for (int hb = 0; hb < 2; ++hb) {
+          const int head = 2 * nt + hb;
+          if (head < a.h0) {
+            mb[hb] = &mapB0;
+            nrow[hb] = head * BN;
+          } else if (head < a.h0 + a.h1) {
+            mb[hb] = &mapB1;
+            nrow[hb] = (head - a.h0) * BN;
+          } else {
+            mb[hb] = &mapB2;
+            nrow[hb] = (head - a.h0 - a.h1) * BN;
+          }
         }
         for (int kb = 0; kb < k_blocks; ++kb) {
           if (!wait_or_abort(&ctl->empty[s], ph ^ 1, ctl)) {
@@ -240,7 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sa = smem + s * kStageBytes;
           tc::mbar_arrive_expect_tx(&ctl->full[s], kStageBytes);
           tc::tma_load_2d(sa, &mapA, &ctl->full[s], kb * BK, mt * BM);
-          tc::tma_load_2d(sa + kTileBytes, mb, &ctl->full[s], kb * BK, nrow);
+          tc::tma_load_2d(sa + kTileBytes, mb[0], &ctl->full[s], kb * BK, nrow[0]);
+          tc::tma_load_2d(sa + 2 * kTileBytes, mb[1], &ctl->full[s], kb * BK, nrow[1]);
           armed[s] = true;
           armed_ph[s] = ph;
           if (++s == STAGES) {
@@ -256,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      const uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
+      const uint32_t idesc = tc::idesc_bf16_f32(BM, BN2);
       int s = 0;
       uint32_t ph = 0;
       int acc = 0;
@@ -295,7 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ---------------- epilogue warps 2..5 ----------------
+    // ---------------- epilogue warps 2..9 ----------------
+    const int hb = (warp - 2) >> 2;          // head of the tile this warpgroup drains
     const int quarter = warp % 4;            // TMEM lanes this warp may access
     const int row = quarter * 32 + lane;
     int acc = 0;
@@ -308,12 +318,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc::tc_fence_after();
-      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * kAccCols;
+      const uint32_t taddr =
+          tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * kAccCols + hb * BN;
       const int m = mt * BM + row;
       if (a.mode == MODE_DEVIATION)
-        epi_deviation(a, taddr, m, nt);
+        epi_deviation(a, taddr, m, 2 * nt + hb);
       else
-        epi_recompute(a, taddr, m, nt);
+        epi_recompute(a, taddr, m, 2 * nt + hb);
       tc::tc_fence_before();
       tc::mbar_arrive(&ctl->tempty[acc]);
       acc ^= 1;
@@ -408,7 +419,10 @@ bool make_map_3d(CUtensorMap* m, const void* base, const uint64_t dims[3], const
 }
 
 bool tc_gemm_supported(const fuse_layer_desc_t& d) {
-  return d.dtype == FUSE_BF16 && d.head_dim == 128 && d.hidden % BK == 0 && encode_fn() != nullptr;
+  // tiles pair heads: even head counts keep a pair inside Q, inside K/V or
+  // across the K/V boundary (handled by per-half weight maps)
+  return d.dtype == FUSE_BF16 && d.head_dim == 128 && d.hidden % BK == 0 &&
+         d.n_q_heads % 2 == 0 && d.n_kv_heads % 2 == 0 && encode_fn() != nullptr;
 }
 
 cudaError_t launch_deviation_partials_tc(const fuse_layer_desc_t& d, int64_t n_rows, const void* H,
@@ -423,9 +437,9 @@ cudaError_t launch_deviation_partials_tc(const fuse_layer_desc_t& d, int64_t n_r
   a.M = (int)n_rows;
   a.K = d.hidden;
   a.m_tiles = (int)((n_rows + BM - 1) / BM);
-  a.n_tiles = d.n_kv_heads;
-  a.nt0 = d.n_kv_heads;
-  a.nt1 = 0;
+  a.n_tiles = d.n_kv_heads / 2;
+  a.h0 = d.n_kv_heads;
+  a.h1 = 0;
   a.mode = MODE_DEVIATION;
   a.n_q_heads = d.n_q_heads;
   a.n_kv_heads = d.n_kv_heads;
@@ -460,9 +474,9 @@ cudaError_t launch_project_recompute_tc(const fuse_layer_desc_t& d, int64_t n_ro
   a.M = (int)n_rows;
   a.K = d.hidden;
   a.m_tiles = (int)((n_rows + BM - 1) / BM);
-  a.n_tiles = d.n_q_heads + 2 * d.n_kv_heads;
-  a.nt0 = d.n_q_heads;
-  a.nt1 = d.n_kv_heads;
+  a.n_tiles = (d.n_q_heads + 2 * d.n_kv_heads) / 2;
+  a.h0 = d.n_q_heads;
+  a.h1 = d.n_kv_heads;
   a.mode = MODE_RECOMPUTE;
   a.n_q_heads = d.n_q_heads;
   a.n_kv_heads = d.n_kv_heads;
