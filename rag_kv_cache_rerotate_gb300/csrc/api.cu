@@ -14,18 +14,19 @@ namespace fusekv {
 bool tc_gemm_supported(const fuse_layer_desc_t& desc);
 cudaError_t launch_deviation_partials_tc(const fuse_layer_desc_t& desc, int64_t n_rows,
                                          const void* H, const void* Wv, const void* Vf,
-                                         const int32_t* map, float* partial, uint32_t* err,
-                                         cudaStream_t s);
+                                         const int32_t* map, const fuse_request_t* d_req,
+                                         int n_req, float* partial, uint32_t* err, cudaStream_t s);
 cudaError_t launch_project_recompute_tc(const fuse_layer_desc_t& desc, int64_t n_rows,
                                         const WorkRow* rows, const float2* rope, const void* H,
                                         const void* Wq, const void* Wk, const void* Wv, void* Q,
                                         void* Kf, void* Vf, void* Hs, uint32_t* err, cudaStream_t s);
 bool tc_attention_supported(const fuse_layer_desc_t& desc);
+int attention_rtile(const fuse_layer_desc_t& d);
 size_t attention_tiles_bytes(int64_t n_out, int n_req);
 cudaError_t launch_attention_tc(const fuse_layer_desc_t& d, const fuse_requests_t& reqs,
                                 int64_t n_out, int64_t n_tok, const WorkRow* rows, const void* Q,
                                 const void* Kf, const void* Vf, void* O, void* tiles_ws,
-                                uint32_t* err, cudaStream_t s);
+                                bool tiles_ready, uint32_t* err, cudaStream_t s);
 
 namespace {
 
@@ -72,6 +73,7 @@ RopeFreqs make_freqs(const fuse_layer_desc_t& d) {
 struct ReqInfo {
   fuse_totals_t tot;   // extents implied by the offsets (max over requests)
   int n_req;
+  bool sorted;         // row0 ascending, request row ranges disjoint
 };
 
 fuse_status_t check_reqs(const fuse_requests_t* r, ReqInfo* info, bool need_device = true) {
@@ -81,8 +83,11 @@ fuse_status_t check_reqs(const fuse_requests_t* r, ReqInfo* info, bool need_devi
   if (r->n_req == 0) return FUSE_OK;
   if (!r->h_req || (need_device && !r->d_req)) return FUSE_ERR_INVALID_ARG;
   fuse_totals_t& t = info->tot;
+  info->sorted = true;
   for (int i = 0; i < r->n_req; ++i) {
     const fuse_request_t& q = r->h_req[i];
+    if (i > 0 && q.row0 < r->h_req[i - 1].row0 + r->h_req[i - 1].n_ctx + r->h_req[i - 1].n_query)
+      info->sorted = false;
     if (q.n_ctx < 0 || q.n_query < 0 || q.k < 0 || q.k > q.n_ctx || q.reserved != 0)
       return FUSE_ERR_INVALID_ARG;
     if (q.row0 < 0 || q.score0 < 0 || q.sel0 < 0 || q.out0 < 0) return FUSE_ERR_INVALID_ARG;
@@ -185,19 +190,24 @@ fuse_status_t do_stitch(const fuse_layer_desc_t& d, const fuse_chunks_t& c, int 
 
 fuse_status_t do_score(const fuse_layer_desc_t& d, const fuse_requests_t& r, const ReqInfo& info,
                        const void* H, const void* Wv, const void* Vf, float* score, void* ws,
-                       cudaStream_t s) {
+                       cudaStream_t s, bool reduce = true) {
   const WsLayout L = ws_layout(d, info.tot, info.n_req);
   if (info.tot.n_ctx == 0) return FUSE_OK;
   int32_t* map = at<int32_t>(ws, L.map);
   float* partial = at<float>(ws, L.partial);
-  cudaError_t e = cudaMemsetAsync(map, 0xFF, (size_t)info.tot.n_tok * sizeof(int32_t), s);
-  if (e == cudaSuccess)
-    e = traced("score_map", s, [&] { return launch_build_score_map(r, info.tot.max_tok, map, s); });
+  const bool tc = tc_gemm_supported(d);
+  const bool need_map = !tc || !info.sorted;    // the tensor-core epilogue searches sorted tables
+  cudaError_t e = cudaSuccess;
+  if (need_map) {
+    e = cudaMemsetAsync(map, 0xFF, (size_t)info.tot.n_tok * sizeof(int32_t), s);
+    if (e == cudaSuccess)
+      e = traced("score_map", s, [&] { return launch_build_score_map(r, info.tot.max_tok, map, s); });
+  }
   if (e == cudaSuccess) {
-    if (tc_gemm_supported(d))
+    if (tc)
       e = traced("deviation_gemm_tc", s, [&] {
-        return launch_deviation_partials_tc(d, info.tot.n_tok, H, Wv, Vf, map, partial,
-                                            at<uint32_t>(ws, 0), s);
+        return launch_deviation_partials_tc(d, info.tot.n_tok, H, Wv, Vf, need_map ? map : nullptr,
+                                            r.d_req, r.n_req, partial, at<uint32_t>(ws, 0), s);
       });
     else
       e = traced("deviation_gemm_simt", s, [&] {
@@ -205,20 +215,22 @@ fuse_status_t do_score(const fuse_layer_desc_t& d, const fuse_requests_t& r, con
                                               at<uint32_t>(ws, 0), s);
       });
   }
-  if (e == cudaSuccess)
+  if (e == cudaSuccess && reduce)
     e = traced("deviation_reduce", s, [&] {
       return launch_deviation_reduce(info.tot.n_ctx, d.n_kv_heads, partial, score, s);
     });
   return cuda_status(e);
 }
 
-fuse_status_t do_topk(const fuse_layer_desc_t& d, const fuse_requests_t& r, const ReqInfo& info,
-                      const float* score, int32_t* idx, void* ws, cudaStream_t s) {
+// score from the partials of do_score(..., reduce = false), then top-k, one launch
+fuse_status_t do_reduce_topk(const fuse_layer_desc_t& d, const fuse_requests_t& r,
+                             const ReqInfo& info, float* score, int32_t* idx, void* ws,
+                             cudaStream_t s) {
   const WsLayout L = ws_layout(d, info.tot, info.n_req);
-  if (info.tot.n_sel == 0) return FUSE_OK;
-  return cuda_status(traced("topk", s, [&] {
-    return launch_topk(r, info.tot.max_ctx, score, idx, at<uint32_t>(ws, L.keys),
-                       at<uint32_t>(ws, 0), s);
+  if (info.tot.n_ctx == 0) return FUSE_OK;
+  return cuda_status(traced("reduce_topk", s, [&] {
+    return launch_reduce_topk(r, info.tot.max_ctx, at<float>(ws, L.partial), d.n_kv_heads, score,
+                              idx, at<uint32_t>(ws, L.keys), at<uint32_t>(ws, 0), s);
   }));
 }
 
@@ -237,24 +249,34 @@ fuse_status_t do_recompute(const fuse_layer_desc_t& d, const fuse_requests_t& r,
   void* Q = at<void>(ws, L.q);
   uint32_t* err = at<uint32_t>(ws, 0);
   const RopeFreqs f = make_freqs(d);
-  cudaError_t e = traced("sel_rows", s, [&] {
-    return launch_build_sel_rows(r, max_rows, idx, f, d.head_dim, rows, rope, err, s);
-  });
-  if (e != cudaSuccess) return FUSE_ERR_CUDA;
-  if (tc_gemm_supported(d))
+  const bool tc_gemm = tc_gemm_supported(d);
+  const bool tc_attn = tc_attention_supported(d);
+  cudaError_t e;
+  if (tc_gemm) {
+    e = traced("prepare_rows", s, [&] {
+      return launch_prepare_rows(r, max_rows, idx, f, d.head_dim, H, d.hidden, rows, rope,
+                                 at<void>(ws, L.hs), tc_attn ? attention_rtile(d) : 128,
+                                 tc_attn ? at<void>(ws, L.tiles) : nullptr, err, s);
+    });
+    if (e != cudaSuccess) return FUSE_ERR_CUDA;
     e = traced("qkv_gemm_tc", s, [&] {
       return launch_project_recompute_tc(d, R, rows, rope, H, Wq, Wk, Wv, Q, Kf, Vf,
                                          at<void>(ws, L.hs), err, s);
     });
-  else
+  } else {
+    e = traced("sel_rows", s, [&] {
+      return launch_build_sel_rows(r, max_rows, idx, f, d.head_dim, rows, rope, err, s);
+    });
+    if (e != cudaSuccess) return FUSE_ERR_CUDA;
     e = traced("qkv_gemm_simt", s, [&] {
       return launch_project_recompute_simt(d, R, rows, rope, H, Wq, Wk, Wv, Q, Kf, Vf, err, s);
     });
+  }
   if (e != cudaSuccess) return FUSE_ERR_CUDA;
-  if (tc_attention_supported(d))
+  if (tc_attn)
     e = traced("attention_tc", s, [&] {
       return launch_attention_tc(d, r, R, info.tot.n_tok, rows, Q, Kf, Vf, O, at<void>(ws, L.tiles),
-                                 err, s);
+                                 /*tiles_ready=*/tc_gemm, err, s);
     });
   else
     e = traced("attention_simt", s, [&] { return launch_attention_simt(d, R, rows, Q, Kf, Vf, O, s); });
@@ -418,9 +440,9 @@ fuse_status_t fuse_layer_step(const fuse_layer_desc_t* desc, const fuse_chunks_t
   st = do_stitch(*desc, *chunks, max_len, Kf, Vf, ws, s);
   if (st != FUSE_OK) return st;
   if (score_this_layer) {
-    st = do_score(*desc, *reqs, info, H, Wv, Vf, score, ws, s);
+    st = do_score(*desc, *reqs, info, H, Wv, Vf, score, ws, s, /*reduce=*/false);
     if (st != FUSE_OK) return st;
-    st = do_topk(*desc, *reqs, info, score, idx, ws, s);
+    st = do_reduce_topk(*desc, *reqs, info, score, idx, ws, s);
     if (st != FUSE_OK) return st;
   }
   return do_recompute(*desc, *reqs, info, H, Wq, Wk, Wv, idx, Kf, Vf, O, ws, s);

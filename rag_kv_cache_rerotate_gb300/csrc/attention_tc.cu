@@ -531,6 +531,8 @@ int sm_count() {
 
 }  // namespace
 
+int attention_rtile(const fuse_layer_desc_t& d) { return 128 / (d.n_q_heads / d.n_kv_heads); }
+
 size_t attention_tiles_bytes(int64_t n_out, int n_req) {
   return (size_t)(n_out / 16 + n_req + 1) * sizeof(AttnTile);
 }
@@ -544,7 +546,7 @@ bool tc_attention_supported(const fuse_layer_desc_t& d) {
 cudaError_t launch_attention_tc(const fuse_layer_desc_t& d, const fuse_requests_t& reqs,
                                 int64_t n_out, int64_t n_tok, const WorkRow* rows, const void* Q,
                                 const void* Kf, const void* Vf, void* O, void* tiles_ws,
-                                uint32_t* err, cudaStream_t s) {
+                                bool tiles_ready, uint32_t* err, cudaStream_t s) {
   const int g = d.n_q_heads / d.n_kv_heads;
   const int rtile = 128 / g;
   int n_tiles = 0;
@@ -554,9 +556,12 @@ cudaError_t launch_attention_tc(const fuse_layer_desc_t& d, const fuse_requests_
   }
   if (n_tiles == 0) return cudaSuccess;
   AttnTile* tiles = reinterpret_cast<AttnTile*>(tiles_ws);
-  attn_tiles_kernel<<<1, 32, 0, s>>>(reqs.d_req, reqs.n_req, rtile, tiles);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  if (!tiles_ready) {
+    attn_tiles_kernel<<<1, 32, 0, s>>>(reqs.d_req, reqs.n_req, rtile, tiles);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
 
   CUtensorMap mQ, mK, mV;
   const uint64_t dq[3] = {(uint64_t)kD, (uint64_t)d.n_q_heads, (uint64_t)n_out};

@@ -56,7 +56,9 @@ struct TcArgs {
   int n_kv_heads;
   // deviation
   const __nv_bfloat16* Vf;
-  const int32_t* map;
+  const int32_t* map;            // score slot of every packed row, or null: search reqs
+  const fuse_request_t* reqs;    // sorted by row0, non-overlapping (when map is null)
+  int n_req;
   float* partial;
   // recompute
   const WorkRow* rows;
@@ -87,9 +89,23 @@ __device__ __forceinline__ void abort_kernel(SharedCtl* ctl, uint32_t* err) {
 
 // ---- epilogues (one thread = one row of the tile) -------------------------
 
+// Score slot of packed row m: score0 + t for context token t of its request,
+// -1 for query rows and rows outside every request.
+__device__ __forceinline__ int32_t row_slot(const TcArgs& a, int m) {
+  if (a.map) return a.map[m];
+  int lo = 0, hi = a.n_req - 1;
+  while (lo < hi) {                       // last request with row0 <= m
+    const int mid = (lo + hi + 1) >> 1;
+    if (a.reqs[mid].row0 <= m) lo = mid; else hi = mid - 1;
+  }
+  const fuse_request_t& R = a.reqs[lo];
+  const int64_t t = m - R.row0;
+  return (t >= 0 && t < R.n_ctx) ? (int32_t)(R.score0 + t) : -1;
+}
+
 __device__ __forceinline__ void epi_deviation(const TcArgs& a, uint32_t taddr, int m, int head) {
   const bool valid = m < a.M;
-  const int32_t slot = valid ? a.map[m] : -1;
+  const int32_t slot = valid ? row_slot(a, m) : -1;
   float dot = 0.f, na = 0.f, nb = 0.f;
   const __nv_bfloat16* vrow = a.Vf + ((int64_t)(valid ? m : 0) * a.n_kv_heads + head) * BN;
 #pragma unroll
@@ -386,19 +402,6 @@ cudaError_t launch(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtensor
   return cudaGetLastError();
 }
 
-// Hs[r] = H[rows[r].a_row]: the gathered A operand of the recompute GEMM.
-__global__ void gather_rows_kernel(const __nv_bfloat16* H, const WorkRow* rows, int64_t n_rows,
-                                   int hidden, __nv_bfloat16* Hs) {
-  const int per_row = hidden / 8;           // 16-byte vectors per row
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n_rows * per_row) return;
-  const int64_t r = i / per_row;
-  const int c = (int)(i % per_row);
-  const int64_t src = rows[r].a_row;
-  reinterpret_cast<uint4*>(Hs + r * hidden)[c] =
-      __ldg(reinterpret_cast<const uint4*>(H + src * hidden) + c);
-}
-
 }  // namespace
 
 bool tma_encode_available() { return encode_fn() != nullptr; }
@@ -427,7 +430,8 @@ bool tc_gemm_supported(const fuse_layer_desc_t& d) {
 
 cudaError_t launch_deviation_partials_tc(const fuse_layer_desc_t& d, int64_t n_rows, const void* H,
                                          const void* Wv, const void* Vf, const int32_t* map,
-                                         float* partial, uint32_t* err, cudaStream_t s) {
+                                         const fuse_request_t* d_req, int n_req, float* partial,
+                                         uint32_t* err, cudaStream_t s) {
   if (n_rows == 0) return cudaSuccess;
   CUtensorMap mA, mB;
   if (!make_map(&mA, H, n_rows, d.hidden) ||
@@ -445,6 +449,8 @@ cudaError_t launch_deviation_partials_tc(const fuse_layer_desc_t& d, int64_t n_r
   a.n_kv_heads = d.n_kv_heads;
   a.Vf = reinterpret_cast<const __nv_bfloat16*>(Vf);
   a.map = map;
+  a.reqs = d_req;
+  a.n_req = n_req;
   a.partial = partial;
   a.err = err;
   return launch(mA, mB, mB, mB, a, s);
@@ -456,14 +462,6 @@ cudaError_t launch_project_recompute_tc(const fuse_layer_desc_t& d, int64_t n_ro
                                         void* Kf, void* Vf, void* Hs, uint32_t* err,
                                         cudaStream_t s) {
   if (n_rows == 0) return cudaSuccess;
-  {
-    const int64_t items = n_rows * (d.hidden / 8);
-    gather_rows_kernel<<<(unsigned)((items + 255) / 256), 256, 0, s>>>(
-        reinterpret_cast<const __nv_bfloat16*>(H), rows, n_rows, d.hidden,
-        reinterpret_cast<__nv_bfloat16*>(Hs));
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
   CUtensorMap mA, mQ, mK, mV;
   const int64_t kv = (int64_t)d.n_kv_heads * d.head_dim;
   if (!make_map(&mA, Hs, n_rows, d.hidden) ||

@@ -30,6 +30,18 @@ cudaError_t launch_deviation_partials_simt(const fuse_layer_desc_t& desc, int64_
 cudaError_t launch_deviation_reduce(int64_t n_ctx, int n_kv_heads, const float* partial,
                                     float* score, cudaStream_t s);
 
+// Work rows, RoPE table, gathered Hs and attention tiles of the recomputed rows
+// (tensor-core path), one launch.
+cudaError_t launch_prepare_rows(const fuse_requests_t& reqs, int max_rows, const int32_t* idx,
+                                const RopeFreqs& freqs, int head_dim, const void* H, int hidden,
+                                WorkRow* rows, float2* rope, void* Hs, int rtile, void* tiles,
+                                uint32_t* err, cudaStream_t s);
+
+// score = 1 - mean_h partial, written to score[], then top-k per request.
+cudaError_t launch_reduce_topk(const fuse_requests_t& reqs, int max_ctx, const float* partial,
+                               int n_kv_heads, float* score, int32_t* idx, uint32_t* keys_ws,
+                               uint32_t* err, cudaStream_t s);
+
 // Top-k per request, ascending indices.
 cudaError_t launch_topk(const fuse_requests_t& reqs, int max_ctx, const float* score, int32_t* idx,
                         uint32_t* keys_ws, uint32_t* err, cudaStream_t s);

@@ -59,7 +59,73 @@ __global__ void sel_rows_kernel(const fuse_request_t* reqs, const int32_t* idx, 
   rope[out * half_dim + j] = make_float2(c, sn);
 }
 
+// One block per recomputed row (blockIdx.y = request): the work row, its RoPE
+// table and the gathered copy Hs[out] = H[row0 + s]; block (0, 0) also lays out
+// the attention tiles (rtile rows of one request each).
+__global__ void __launch_bounds__(256) prepare_rows_kernel(const fuse_request_t* reqs, int n_req,
+                                                           const int32_t* idx, RopeFreqs f,
+                                                           int half_dim, const __nv_bfloat16* H,
+                                                           int hidden, WorkRow* rows, float2* rope,
+                                                           __nv_bfloat16* Hs, int rtile,
+                                                           int4* tiles, uint32_t* err) {
+  const int r = blockIdx.y;
+  const fuse_request_t R = reqs[r];
+  const int o = blockIdx.x;
+  const int t = threadIdx.x;
+  if (tiles && o == 0 && r == 0 && t == 0) {
+    int nt = 0;
+    for (int q = 0; q < n_req; ++q) {
+      const int n = reqs[q].k + reqs[q].n_query;
+      for (int r0 = 0; r0 < n; r0 += rtile) tiles[nt++] = make_int4(q, r0, min(rtile, n - r0), 0);
+    }
+  }
+  if (o >= R.k + R.n_query) return;
+  int s;
+  if (o < R.k) {
+    s = idx[R.sel0 + o];
+    if (t == 0) {
+      if (s < 0 || s >= R.n_ctx)
+        report_error(err, FUSE_ERR_DEVICE_BOUNDS, SITE_SEL_RANGE, r);
+      else if (o > 0 && idx[R.sel0 + o - 1] >= s)
+        report_error(err, FUSE_ERR_DEVICE_BOUNDS, SITE_SEL_ORDER, r);
+    }
+    s = min(max(s, 0), max(R.n_ctx - 1, 0));
+  } else {
+    s = R.n_ctx + (o - R.k);
+  }
+  const int64_t out = R.out0 + o;
+  if (t == 0) {
+    WorkRow w;
+    w.a_row = R.row0 + s;
+    w.dst_row = R.row0 + s;
+    w.pos = s;
+    w.aux = r;
+    rows[out] = w;
+  }
+  if (t < half_dim) {
+    float c, sn;
+    rope_cos_sin(s, f.hi[t], f.mid[t], f.lo[t], c, sn);
+    rope[out * half_dim + t] = make_float2(c, sn);
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(H + (R.row0 + s) * (int64_t)hidden);
+  uint4* dst = reinterpret_cast<uint4*>(Hs + out * (int64_t)hidden);
+  for (int c = t; c < hidden / 8; c += 256) dst[c] = __ldg(src + c);
+}
+
 }  // namespace
+
+cudaError_t launch_prepare_rows(const fuse_requests_t& reqs, int max_rows, const int32_t* idx,
+                                const RopeFreqs& freqs, int head_dim, const void* H, int hidden,
+                                WorkRow* rows, float2* rope, void* Hs, int rtile, void* tiles,
+                                uint32_t* err, cudaStream_t s) {
+  if (reqs.n_req == 0 || max_rows == 0) return cudaSuccess;
+  dim3 grid(max_rows, reqs.n_req);
+  prepare_rows_kernel<<<grid, 256, 0, s>>>(reqs.d_req, reqs.n_req, idx, freqs, head_dim / 2,
+                                           reinterpret_cast<const __nv_bfloat16*>(H), hidden, rows,
+                                           rope, reinterpret_cast<__nv_bfloat16*>(Hs), rtile,
+                                           reinterpret_cast<int4*>(tiles), err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_build_score_map(const fuse_requests_t& reqs, int max_tok, int32_t* map,
                                    cudaStream_t s) {

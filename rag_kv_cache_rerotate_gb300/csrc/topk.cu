@@ -54,10 +54,16 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* w
   return before;
 }
 
+// With partial != null the scores are first formed from the per-head cosine
+// partials, score = 1 - (sum_h partial[h]) / Hkv summed in head order (the
+// same expression as deviation_reduce_kernel), and written to score[].
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const fuse_request_t* reqs,
                                                             const float* score, int32_t* idx,
                                                             uint32_t* keys_ws, uint32_t* err,
-                                                            int keys_in_smem) {
+                                                            int keys_in_smem,
+                                                            const float* partial = nullptr,
+                                                            int n_kv_heads = 0,
+                                                            float* score_out = nullptr) {
   extern __shared__ uint32_t dyn[];
   __shared__ uint32_t hist[256];
   __shared__ uint32_t warp_buf[32];
@@ -66,14 +72,35 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const fuse_request_t
   const fuse_request_t R = reqs[r];
   const int n = R.n_ctx;
   const int k = R.k;
-  if (k <= 0 || n <= 0) return;
+  if (n <= 0) return;
   const int t = threadIdx.x;
+  if (k <= 0) {                      // nothing to select; still form the scores
+    if (partial) {
+      for (int i = t; i < n; i += kTopkThreads) {
+        const float* pr = partial + (R.score0 + i) * n_kv_heads;
+        float acc = 0.f;
+        for (int h = 0; h < n_kv_heads; ++h) acc += pr[h];
+        score_out[R.score0 + i] = 1.0f - acc / (float)n_kv_heads;
+      }
+    }
+    return;
+  }
   uint32_t* keys = keys_in_smem ? dyn : keys_ws + R.score0;
 
   bool nan_seen = false;
   for (int i = t; i < n; i += kTopkThreads) {
     bool nn;
-    keys[i] = float_key(score[R.score0 + i], &nn);
+    float v;
+    if (partial) {
+      const float* pr = partial + (R.score0 + i) * n_kv_heads;
+      float acc = 0.f;
+      for (int h = 0; h < n_kv_heads; ++h) acc += pr[h];
+      v = 1.0f - acc / (float)n_kv_heads;
+      score_out[R.score0 + i] = v;
+    } else {
+      v = score[R.score0 + i];
+    }
+    keys[i] = float_key(v, &nn);
     nan_seen |= nn;
   }
   if (nan_seen) report_error(err, FUSE_ERR_DEVICE_BOUNDS, SITE_TOPK_NAN, r);
@@ -148,6 +175,22 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const fuse_request_t
 }
 
 }  // namespace
+
+cudaError_t launch_reduce_topk(const fuse_requests_t& reqs, int max_ctx, const float* partial,
+                               int n_kv_heads, float* score, int32_t* idx, uint32_t* keys_ws,
+                               uint32_t* err, cudaStream_t s) {
+  if (reqs.n_req == 0) return cudaSuccess;
+  const int in_smem = max_ctx <= kTopkSmemKeys;
+  const size_t smem = in_smem ? (size_t)max_ctx * sizeof(uint32_t) : 0;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kTopkSmemKeys * (int)sizeof(uint32_t));
+    if (e != cudaSuccess) return e;
+  }
+  topk_kernel<<<reqs.n_req, kTopkThreads, smem, s>>>(reqs.d_req, nullptr, idx, keys_ws, err, in_smem,
+                                                     partial, n_kv_heads, score);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_topk(const fuse_requests_t& reqs, int max_ctx, const float* score, int32_t* idx,
                         uint32_t* keys_ws, uint32_t* err, cudaStream_t s) {
