@@ -15,7 +15,8 @@ bool tc_gemm_supported(const fuse_layer_desc_t& desc);
 cudaError_t launch_deviation_partials_tc(const fuse_layer_desc_t& desc, int64_t n_rows,
                                          const void* H, const void* Wv, const void* Vf,
                                          const int32_t* map, const fuse_request_t* d_req,
-                                         int n_req, float* partial, uint32_t* err, cudaStream_t s);
+                                         int n_req, float* partial, float* score,
+                                         uint32_t* row_count, uint32_t* err, cudaStream_t s);
 cudaError_t launch_project_recompute_tc(const fuse_layer_desc_t& desc, int64_t n_rows,
                                         const WorkRow* rows, const float2* rope, const void* H,
                                         const void* Wq, const void* Wk, const void* Wv, void* Q,
@@ -140,7 +141,7 @@ fuse_status_t check_chunks(const fuse_layer_desc_t& d, const fuse_chunks_t* c, i
 
 // Workspace regions (each 256-byte aligned).
 struct WsLayout {
-  size_t partial, keys, map, rows, rope, q, hs, tiles, total;
+  size_t partial, keys, map, rows, rope, q, hs, tiles, counts, total;
 };
 
 WsLayout ws_layout(const fuse_layer_desc_t& d, const fuse_totals_t& t, int n_req) {
@@ -160,6 +161,7 @@ WsLayout ws_layout(const fuse_layer_desc_t& d, const fuse_totals_t& t, int n_req
   L.q = take((size_t)t.n_out * d.n_q_heads * d.head_dim * es);
   L.hs = take((size_t)t.n_out * d.hidden * es);
   L.tiles = take(attention_tiles_bytes(t.n_out, n_req));
+  L.counts = take((size_t)t.n_ctx * sizeof(uint32_t));       // zero between calls
   L.total = off;
   return L;
 }
@@ -207,7 +209,8 @@ fuse_status_t do_score(const fuse_layer_desc_t& d, const fuse_requests_t& r, con
     if (tc)
       e = traced("deviation_gemm_tc", s, [&] {
         return launch_deviation_partials_tc(d, info.tot.n_tok, H, Wv, Vf, need_map ? map : nullptr,
-                                            r.d_req, r.n_req, partial, at<uint32_t>(ws, 0), s);
+                                            r.d_req, r.n_req, partial, score,
+                                            at<uint32_t>(ws, L.counts), at<uint32_t>(ws, 0), s);
       });
     else
       e = traced("deviation_gemm_simt", s, [&] {
@@ -215,7 +218,8 @@ fuse_status_t do_score(const fuse_layer_desc_t& d, const fuse_requests_t& r, con
                                               at<uint32_t>(ws, 0), s);
       });
   }
-  if (e == cudaSuccess && reduce)
+  // the tensor-core epilogue writes the scores itself
+  if (e == cudaSuccess && reduce && !tc)
     e = traced("deviation_reduce", s, [&] {
       return launch_deviation_reduce(info.tot.n_ctx, d.n_kv_heads, partial, score, s);
     });
@@ -340,7 +344,7 @@ fuse_status_t fuse_workspace_size(const fuse_layer_desc_t* desc, const fuse_requ
 
 fuse_status_t fuse_workspace_reset(void* ws, size_t ws_bytes, fuse_stream_t stream) {
   if (!ws || ws_bytes < sizeof(WsHeader)) return FUSE_ERR_WORKSPACE;
-  return cuda_status(cudaMemsetAsync(ws, 0, 8, (cudaStream_t)stream));
+  return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes, (cudaStream_t)stream));
 }
 
 fuse_status_t fuse_stitch_rerotate(const fuse_layer_desc_t* desc, const fuse_chunks_t* chunks,
@@ -442,7 +446,17 @@ fuse_status_t fuse_layer_step(const fuse_layer_desc_t* desc, const fuse_chunks_t
   if (score_this_layer) {
     st = do_score(*desc, *reqs, info, H, Wv, Vf, score, ws, s, /*reduce=*/false);
     if (st != FUSE_OK) return st;
-    st = do_reduce_topk(*desc, *reqs, info, score, idx, ws, s);
+    if (tc_gemm_supported(*desc)) {
+      if (info.tot.n_sel > 0) {
+        const WsLayout L = ws_layout(*desc, info.tot, info.n_req);
+        st = cuda_status(traced("topk", s, [&] {
+          return launch_topk(*reqs, info.tot.max_ctx, score, idx, at<uint32_t>(ws, L.keys),
+                             at<uint32_t>(ws, 0), s);
+        }));
+      }
+    } else {
+      st = do_reduce_topk(*desc, *reqs, info, score, idx, ws, s);
+    }
     if (st != FUSE_OK) return st;
   }
   return do_recompute(*desc, *reqs, info, H, Wq, Wk, Wv, idx, Kf, Vf, O, ws, s);

@@ -270,9 +270,7 @@ cudaError_t dispatch(const fuse_layer_desc_t& desc, const GemmArgs& a, int n_tot
 __global__ void deviation_reduce_kernel(int64_t n, int Hkv, const float* partial, float* score) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
-  float s = 0.f;
-  for (int h = 0; h < Hkv; ++h) s += partial[i * Hkv + h];
-  score[i] = 1.0f - s / (float)Hkv;
+  score[i] = head_mean_score(partial + i * Hkv, Hkv);
 }
 
 }  // namespace

@@ -60,6 +60,8 @@ struct TcArgs {
   const fuse_request_t* reqs;    // sorted by row0, non-overlapping (when map is null)
   int n_req;
   float* partial;
+  float* score;                  // written by the last of a row's Hkv cosines
+  uint32_t* row_count;           // [N] zero between calls (each row resets its own)
   // recompute
   const WorkRow* rows;
   const float2* rope;
@@ -130,8 +132,18 @@ __device__ __forceinline__ void epi_deviation(const TcArgs& a, uint32_t taddr, i
       }
     }
   }
-  if (slot >= 0)
-    a.partial[(int64_t)slot * a.n_kv_heads + head] = dot / fmaxf(sqrtf(na) * sqrtf(nb), 1e-30f);
+  if (slot >= 0) {
+    float* pr = a.partial + (int64_t)slot * a.n_kv_heads;
+    pr[head] = dot / fmaxf(sqrtf(na) * sqrtf(nb), 1e-30f);
+    // the thread that writes the row's last cosine forms the score, summing
+    // the cosines in head order (deterministic), and resets the counter
+    __threadfence();
+    if (atomicAdd(a.row_count + slot, 1u) == (uint32_t)a.n_kv_heads - 1) {
+      __threadfence();
+      a.score[slot] = head_mean_score<true>(pr, a.n_kv_heads);
+      a.row_count[slot] = 0u;
+    }
+  }
 }
 
 __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&x)[32]) {
@@ -431,7 +443,8 @@ bool tc_gemm_supported(const fuse_layer_desc_t& d) {
 cudaError_t launch_deviation_partials_tc(const fuse_layer_desc_t& d, int64_t n_rows, const void* H,
                                          const void* Wv, const void* Vf, const int32_t* map,
                                          const fuse_request_t* d_req, int n_req, float* partial,
-                                         uint32_t* err, cudaStream_t s) {
+                                         float* score, uint32_t* row_count, uint32_t* err,
+                                         cudaStream_t s) {
   if (n_rows == 0) return cudaSuccess;
   CUtensorMap mA, mB;
   if (!make_map(&mA, H, n_rows, d.hidden) ||
@@ -452,6 +465,8 @@ cudaError_t launch_deviation_partials_tc(const fuse_layer_desc_t& d, int64_t n_r
   a.reqs = d_req;
   a.n_req = n_req;
   a.partial = partial;
+  a.score = score;
+  a.row_count = row_count;
   a.err = err;
   return launch(mA, mB, mB, mB, a, s);
 }

@@ -7,10 +7,13 @@
 // R^{o_i}.  KVBoost (section 4.5, Eq. 7): x = zero + q * scale, keys with
 // per-channel statistics, values with per-token statistics.
 //
-// Memory-bound.  One CTA moves a tile of rows of one chunk; every thread
-// owns a fixed group of 8 frequency pairs, so it evaluates the 8 (cos, sin)
-// of the chunk offset once and reuses them for every row and head it
-// handles.  Loads and stores are 16 bytes wide.
+// Memory-bound.  One CTA moves a few rows of one chunk; each thread owns one
+// group of 8 key pairs and two groups of 8 values and issues all its 16-byte
+// loads before anything else, so every thread keeps four loads in flight at
+// low register use.  The chunk offset's (cos, sin) of the d/2 frequencies are
+// computed once per CTA into shared memory while those loads are in flight.
+#include <algorithm>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -19,7 +22,8 @@ namespace fusekv {
 namespace {
 
 constexpr int kStitchThreads = 256;
-constexpr int kStitchRows = 8;       // rows of one chunk per CTA
+constexpr int kStitchItems = 2;      // V 16-byte groups per thread at most
+constexpr int kStitchKItems = kStitchItems / 2;   // K pair groups: half as many as V groups
 
 template <typename TS> struct Src8;
 
@@ -59,6 +63,7 @@ template <typename TO> struct Dst8 {
 };
 
 struct StitchArgs {
+  int rows_per_cta;
   const fuse_chunk_t* chunks;
   void* Kf;
   void* Vf;
@@ -97,95 +102,133 @@ __global__ void __launch_bounds__(kStitchThreads) stitch_kernel(const StitchArgs
   const int chunk = blockIdx.x / a.tiles_per_chunk;
   const int tile = blockIdx.x % a.tiles_per_chunk;
   const fuse_chunk_t c = a.chunks[chunk];
-  const int r0 = tile * kStitchRows;
+  const int r0 = tile * a.rows_per_cta;
   if (r0 >= c.len) return;
-  const int nrows = min(kStitchRows, c.len - r0);
+  const int nrows = min(a.rows_per_cta, c.len - r0);
   const int Hkv = a.n_kv_heads;
   const int t = threadIdx.x;
+  const int g = t % PG;                // this thread's pair group (fixed for all its K items)
+  const int j0 = g * 8;
+  const int k_items = nrows * Hkv * PG;
+  const int v_items = nrows * Hkv * VG;
 
-  // ---- keys: rotate by R^{pos} ------------------------------------------
-  {
-    const int g = t % PG;              // this thread's pair group (fixed)
-    const int j0 = g * 8;
-    float cs[8], sn[8];
-    const bool rotate = !(kSame && c.pos == 0);
-    if (rotate) {
+  // 1. issue every load of this thread first, so they are all in flight together
+  float kx[kStitchKItems][8], ky[kStitchKItems][8], vx[kStitchItems][8];
+  int64_t k_tok[kStitchKItems], v_tok[kStitchItems];
+  bool k_ok[kStitchKItems], v_ok[kStitchItems];
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        rope_cos_sin(c.pos, a.freqs.hi[j0 + i], a.freqs.mid[j0 + i], a.freqs.lo[j0 + i], cs[i],
-                     sn[i]);
-    }
-    const int items = nrows * Hkv * PG;
-    for (int it = t; it < items; it += kStitchThreads) {
+  for (int q = 0; q < kStitchKItems; ++q) {
+    const int it = t + q * kStitchThreads;
+    k_ok[q] = false;
+    if (it < k_items) {
       const int rh = it / PG;
       const int r = r0 + rh / Hkv;
       const int h = rh % Hkv;
-      int64_t tok;
-      const int64_t e = chunk_elem<PAGED, D>(c, r, h, j0, Hkv, a.block_size, a.n_pool_blocks, &tok);
+      const int64_t e = chunk_elem<PAGED, D>(c, r, h, j0, Hkv, a.block_size, a.n_pool_blocks, &k_tok[q]);
       if (e < 0) {
         report_error(a.err, FUSE_ERR_DEVICE_BOUNDS, SITE_STITCH_BLOCK, chunk);
-        continue;
-      }
-      float x[8], y[8];
-      if constexpr (kU8) {
-        float sx[8], zx[8], sy[8], zy[8];
-        load_u8(c.k, e, x);
-        load_u8(c.k, e + H2, y);
-        load_h8(c.k_scale, h * D + j0, sx);
-        load_h8(c.k_zero, h * D + j0, zx);
-        load_h8(c.k_scale, h * D + j0 + H2, sy);
-        load_h8(c.k_zero, h * D + j0 + H2, zy);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          x[i] = fmaf(x[i], sx[i], zx[i]);
-          y[i] = fmaf(y[i], sy[i], zy[i]);
-        }
       } else {
-        Src8<TS>::load(c.k, e, x);
-        Src8<TS>::load(c.k, e + H2, y);
-      }
-      if (rotate) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float xr = fmaf(x[i], cs[i], -y[i] * sn[i]);
-          const float yr = fmaf(y[i], cs[i], x[i] * sn[i]);
-          x[i] = xr;
-          y[i] = yr;
+        k_ok[q] = true;
+        if constexpr (kU8) {
+          load_u8(c.k, e, kx[q]);
+          load_u8(c.k, e + H2, ky[q]);
+        } else {
+          Src8<TS>::load(c.k, e, kx[q]);
+          Src8<TS>::load(c.k, e + H2, ky[q]);
         }
       }
-      const int64_t o = ((c.dst_row + r) * Hkv + h) * D + j0;
-      Dst8<TO>::store(a.Kf, o, x);
-      Dst8<TO>::store(a.Kf, o + H2, y);
     }
   }
-
-  // ---- values: copy (dequantise) ----------------------------------------
-  {
-    const int items = nrows * Hkv * VG;
-    for (int it = t; it < items; it += kStitchThreads) {
-      const int g = it % VG;
+#pragma unroll
+  for (int q = 0; q < kStitchItems; ++q) {
+    const int it = t + q * kStitchThreads;
+    v_ok[q] = false;
+    if (it < v_items) {
+      const int gv = it % VG;
       const int rh = it / VG;
       const int r = r0 + rh / Hkv;
       const int h = rh % Hkv;
-      int64_t tok;
-      const int64_t e = chunk_elem<PAGED, D>(c, r, h, g * 8, Hkv, a.block_size, a.n_pool_blocks, &tok);
+      const int64_t e = chunk_elem<PAGED, D>(c, r, h, gv * 8, Hkv, a.block_size, a.n_pool_blocks, &v_tok[q]);
       if (e < 0) {
         report_error(a.err, FUSE_ERR_DEVICE_BOUNDS, SITE_STITCH_BLOCK, chunk);
-        continue;
-      }
-      float x[8];
-      if constexpr (kU8) {
-        load_u8(c.v, e, x);
-        const int64_t sidx = tok * Hkv + h;
-        const float s = __half2float(reinterpret_cast<const __half*>(c.v_scale)[sidx]);
-        const float z = __half2float(reinterpret_cast<const __half*>(c.v_zero)[sidx]);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] = fmaf(x[i], s, z);
       } else {
-        Src8<TS>::load(c.v, e, x);
+        v_ok[q] = true;
+        if constexpr (kU8)
+          load_u8(c.v, e, vx[q]);
+        else
+          Src8<TS>::load(c.v, e, vx[q]);
       }
-      Dst8<TO>::store(a.Vf, ((c.dst_row + r) * Hkv + h) * D + g * 8, x);
     }
+  }
+
+  // 2. the chunk offset's cos/sin of every frequency, once per CTA, while the
+  //    loads fly
+  __shared__ float s_cs[kMaxHalfDim], s_sn[kMaxHalfDim];
+  const bool rotate = !(kSame && c.pos == 0);
+  if (rotate && t < H2) rope_cos_sin(c.pos, a.freqs.hi[t], a.freqs.mid[t], a.freqs.lo[t], s_cs[t], s_sn[t]);
+  __syncthreads();
+  float cs[8], sn[8];
+  if (rotate) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      cs[i] = s_cs[j0 + i];
+      sn[i] = s_sn[j0 + i];
+    }
+  }
+
+  // 3. keys: dequantise, rotate by R^{pos}, store
+#pragma unroll
+  for (int q = 0; q < kStitchKItems; ++q) {
+    if (!k_ok[q]) continue;
+    const int it = t + q * kStitchThreads;
+    const int rh = it / PG;
+    const int r = r0 + rh / Hkv;
+    const int h = rh % Hkv;
+    float* x = kx[q];
+    float* y = ky[q];
+    if constexpr (kU8) {
+      float sx[8], zx[8], sy[8], zy[8];
+      load_h8(c.k_scale, h * D + j0, sx);
+      load_h8(c.k_zero, h * D + j0, zx);
+      load_h8(c.k_scale, h * D + j0 + H2, sy);
+      load_h8(c.k_zero, h * D + j0 + H2, zy);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        x[i] = fmaf(x[i], sx[i], zx[i]);
+        y[i] = fmaf(y[i], sy[i], zy[i]);
+      }
+    }
+    if (rotate) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float xr = fmaf(x[i], cs[i], -y[i] * sn[i]);
+        const float yr = fmaf(y[i], cs[i], x[i] * sn[i]);
+        x[i] = xr;
+        y[i] = yr;
+      }
+    }
+    const int64_t o = ((c.dst_row + r) * Hkv + h) * D + j0;
+    Dst8<TO>::store(a.Kf, o, kx[q]);
+    Dst8<TO>::store(a.Kf, o + H2, ky[q]);
+  }
+
+  // 4. values: dequantise, store
+#pragma unroll
+  for (int q = 0; q < kStitchItems; ++q) {
+    if (!v_ok[q]) continue;
+    const int it = t + q * kStitchThreads;
+    const int gv = it % VG;
+    const int rh = it / VG;
+    const int r = r0 + rh / Hkv;
+    const int h = rh % Hkv;
+    if constexpr (kU8) {
+      const int64_t sidx = v_tok[q] * Hkv + h;
+      const float s = __half2float(reinterpret_cast<const __half*>(c.v_scale)[sidx]);
+      const float z = __half2float(reinterpret_cast<const __half*>(c.v_zero)[sidx]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) vx[q][i] = fmaf(vx[q][i], s, z);
+    }
+    Dst8<TO>::store(a.Vf, ((c.dst_row + r) * Hkv + h) * D + gv * 8, vx[q]);
   }
 }
 
@@ -219,7 +262,10 @@ cudaError_t launch_stitch(const fuse_layer_desc_t& desc, const fuse_chunks_t& ch
   a.n_pool_blocks = chunks.n_pool_blocks;
   a.n_kv_heads = desc.n_kv_heads;
   a.block_size = chunks.block_size > 0 ? chunks.block_size : 1;
-  a.tiles_per_chunk = (max_len + kStitchRows - 1) / kStitchRows;
+  // rows per CTA: every thread gets at most kStitchItems V groups (D/8 per
+  // head-row) and, as K groups are half as many, at most that many K groups
+  a.rows_per_cta = std::max(1, (kStitchThreads * kStitchItems) / (desc.n_kv_heads * (desc.head_dim / 8)));
+  a.tiles_per_chunk = (max_len + a.rows_per_cta - 1) / a.rows_per_cta;
   a.freqs = freqs;
   const bool paged = chunks.kv_layout == FUSE_KV_PAGED;
   const int D = desc.head_dim;

@@ -76,43 +76,72 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const fuse_request_t
   const int t = threadIdx.x;
   if (k <= 0) {                      // nothing to select; still form the scores
     if (partial) {
-      for (int i = t; i < n; i += kTopkThreads) {
-        const float* pr = partial + (R.score0 + i) * n_kv_heads;
-        float acc = 0.f;
-        for (int h = 0; h < n_kv_heads; ++h) acc += pr[h];
-        score_out[R.score0 + i] = 1.0f - acc / (float)n_kv_heads;
-      }
+      for (int i = t; i < n; i += kTopkThreads)
+        score_out[R.score0 + i] = head_mean_score(partial + (R.score0 + i) * n_kv_heads, n_kv_heads);
     }
     return;
   }
   uint32_t* keys = keys_in_smem ? dyn : keys_ws + R.score0;
 
   bool nan_seen = false;
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
   for (int i = t; i < n; i += kTopkThreads) {
     bool nn;
     float v;
     if (partial) {
-      const float* pr = partial + (R.score0 + i) * n_kv_heads;
-      float acc = 0.f;
-      for (int h = 0; h < n_kv_heads; ++h) acc += pr[h];
-      v = 1.0f - acc / (float)n_kv_heads;
+      v = head_mean_score(partial + (R.score0 + i) * n_kv_heads, n_kv_heads);
       score_out[R.score0 + i] = v;
     } else {
       v = score[R.score0 + i];
     }
-    keys[i] = float_key(v, &nn);
+    const uint32_t key = float_key(v, &nn);
+    keys[i] = key;
+    kmin = min(kmin, key);
+    kmax = max(kmax, key);
     nan_seen |= nn;
   }
   if (nan_seen) report_error(err, FUSE_ERR_DEVICE_BOUNDS, SITE_TOPK_NAN, r);
+  // the keys' common leading bits decide nothing: start below them
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  }
+  if ((t & 31) == 0) {
+    warp_buf[t >> 5] = kmin;
+    hist[t >> 5] = kmax;
+  }
   __syncthreads();
-
-  uint32_t prefix = 0, mask = 0, remaining = (uint32_t)k;
-  for (int shift = 24; shift >= 0; shift -= 8) {
+  if (t < 32) {
+    uint32_t a = warp_buf[t], b = hist[t];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      a = min(a, __shfl_xor_sync(0xffffffffu, a, o));
+      b = max(b, __shfl_xor_sync(0xffffffffu, b, o));
+    }
+    if (t == 0) {
+      sel_digit = a;
+      sel_remaining = b;
+    }
+  }
+  __syncthreads();
+  kmin = sel_digit;
+  kmax = sel_remaining;
+  __syncthreads();
+  int lo = 32 - __clz(kmin ^ kmax);      // bits [0, lo) still differ between keys
+  uint32_t mask = lo >= 32 ? 0u : ~((1u << lo) - 1u);
+  uint32_t prefix = kmin & mask;
+  uint32_t remaining = (uint32_t)k;
+  // radix rounds of at most 8 bits over the differing bits, highest first
+  while (lo > 0) {
+    const int w = min(8, lo);
+    const int shift = lo - w;
+    const uint32_t dmask = (1u << w) - 1u;
     for (int b = t; b < 256; b += kTopkThreads) hist[b] = 0u;
     __syncthreads();
     for (int i = t; i < n; i += kTopkThreads) {
       const uint32_t key = keys[i];
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 0xFFu], 1u);
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & dmask], 1u);
     }
     __syncthreads();
     if (t < 32) {
@@ -135,16 +164,22 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const fuse_request_t
         if (cum < remaining && cum + c[q] >= remaining) {
           sel_digit = 255 - (t * 8 + q);
           sel_remaining = remaining - cum;
+          warp_buf[0] = c[q];                      // keys in the chosen bin
         }
         cum += c[q];
       }
     }
     __syncthreads();
     prefix |= sel_digit << shift;
-    mask |= 0xFFu << shift;
+    mask |= dmask << shift;
     remaining = sel_remaining;
+    const uint32_t in_bin = warp_buf[0];
+    lo = shift;
     __syncthreads();
+    if (in_bin == remaining) break;      // every key of the chosen bin is taken
   }
+  // keys above the prefix are taken; of the keys equal to it under the mask,
+  // the lowest-indexed `remaining` ones
   const uint32_t tau = prefix;
   const uint32_t need_eq = remaining;
 
@@ -154,7 +189,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const fuse_request_t
   const int i1 = min(n, i0 + per);
   uint32_t n_gt = 0, n_eq = 0;
   for (int i = i0; i < i1; ++i) {
-    const uint32_t key = keys[i];
+    const uint32_t key = keys[i] & mask;
     n_gt += key > tau;
     n_eq += key == tau;
   }
@@ -165,7 +200,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const fuse_request_t
   int32_t* out = idx + R.sel0;
   uint32_t o = out_before, eq_taken = 0;
   for (int i = i0; i < i1; ++i) {
-    const uint32_t key = keys[i];
+    const uint32_t key = keys[i] & mask;
     if (key > tau || (key == tau && eq_taken < take_eq)) {
       eq_taken += key == tau;
       if (o < (uint32_t)k) out[o] = i;
