@@ -240,6 +240,32 @@ fuse_status_t fuse_layer_step(const fuse_layer_desc_t* desc, const fuse_chunks_t
                               int32_t* idx, void* Kf, void* Vf, void* O, float* score,
                               void* ws, size_t ws_bytes, fuse_stream_t stream);
 
+/* The buffers of one layer of a stack (every pointer as in fuse_layer_step;
+ * chunks points at this layer's chunk table, in host memory). */
+typedef struct {
+  const fuse_chunks_t* chunks;
+  const void* H;
+  const void* Wq;
+  const void* Wk;
+  const void* Wv;
+  void* Kf;
+  void* Vf;
+  void* O;
+} fuse_layer_io_t;
+
+/* A stack of n_layers attention layers sharing one selection ([QCFuse]
+ * section 3.4 scores critical layers only; the selection is made at one
+ * layer and reused by every layer): the scoring layer is stitched, scored
+ * and its top-k written to idx first; then every layer l = 0 .. n_layers-1
+ * is stitched (the scoring layer only once) and recomputed with that idx.
+ * layers: host array [n_layers]; all layers share desc and reqs; score
+ * receives the scoring layer's scores.  One workspace serves every layer
+ * (the calls run in stream order). */
+fuse_status_t fuse_stack_step(const fuse_layer_desc_t* desc, const fuse_requests_t* reqs,
+                              int32_t n_layers, int32_t score_layer, const fuse_layer_io_t* layers,
+                              int32_t* idx, float* score, void* ws, size_t ws_bytes,
+                              fuse_stream_t stream);
+
 /* Position-independent chunk caches, [QCFuse] Eq. 3 with one projection layer
  * standing in for the model: for every chunk i and local row r,
  *   K_i[r] = R^r W_K x,  V_i[r] = W_V x,   x = H_clean[dst_row_i + r].

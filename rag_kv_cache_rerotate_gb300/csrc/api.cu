@@ -3,6 +3,7 @@
 // 4-7; KVBoost Alg. 2: stitch, probe/deviation, select, patch).
 #include <cmath>
 #include <cstring>
+#include <vector>
 
 #include "common.cuh"
 #include "launch.h"
@@ -287,6 +288,48 @@ fuse_status_t do_recompute(const fuse_layer_desc_t& d, const fuse_requests_t& r,
   return cuda_status(e);
 }
 
+struct LayerArgs {
+  const fuse_chunks_t* chunks;
+  const void* H;
+  const void* Wq;
+  const void* Wk;
+  const void* Wv;
+  void* Kf;
+  void* Vf;
+  void* O;
+};
+
+// Validation of one layer of fuse_layer_step / fuse_stack_step.
+fuse_status_t check_layer(const fuse_layer_desc_t& d, const ReqInfo& info, const LayerArgs& a,
+                          bool scoring, const int32_t* idx, const float* score, void* ws,
+                          size_t ws_bytes, int* max_len) {
+  fuse_status_t st = check_chunks(d, a.chunks, info.tot.n_tok, max_len);
+  if (st != FUSE_OK) return st;
+  if (info.tot.n_out > 0 && (!a.H || !a.Wq || !a.Wk || !a.Wv || !a.Kf || !a.Vf || !a.O))
+    return FUSE_ERR_INVALID_ARG;
+  if (info.tot.n_sel > 0 && !idx) return FUSE_ERR_INVALID_ARG;
+  if (scoring && info.tot.n_ctx > 0 && !score) return FUSE_ERR_INVALID_ARG;
+  if (!aligned16(a.H) || !aligned16(a.Wq) || !aligned16(a.Wk) || !aligned16(a.Wv) ||
+      !aligned16(a.Kf) || !aligned16(a.Vf) || !aligned16(a.O) || !aligned16(score))
+    return FUSE_ERR_MISALIGNED;
+  return check_ws(ws, ws_bytes, ws_layout(d, info.tot, info.n_req).total);
+}
+
+// Deviation scores and the top-k selection of one (scoring) layer.
+fuse_status_t do_score_select(const fuse_layer_desc_t& d, const fuse_requests_t& r,
+                              const ReqInfo& info, const void* H, const void* Wv, const void* Vf,
+                              float* score, int32_t* idx, void* ws, cudaStream_t s) {
+  fuse_status_t st = do_score(d, r, info, H, Wv, Vf, score, ws, s, /*reduce=*/false);
+  if (st != FUSE_OK) return st;
+  if (!tc_gemm_supported(d)) return do_reduce_topk(d, r, info, score, idx, ws, s);
+  if (info.tot.n_sel == 0) return FUSE_OK;
+  const WsLayout L = ws_layout(d, info.tot, info.n_req);
+  return cuda_status(traced("topk", s, [&] {
+    return launch_topk(r, info.tot.max_ctx, score, idx, at<uint32_t>(ws, L.keys),
+                       at<uint32_t>(ws, 0), s);
+  }));
+}
+
 }  // namespace
 }  // namespace fusekv
 
@@ -428,38 +471,54 @@ fuse_status_t fuse_layer_step(const fuse_layer_desc_t* desc, const fuse_chunks_t
   ReqInfo info;
   st = check_reqs(reqs, &info);
   if (st != FUSE_OK) return st;
+  LayerArgs la{chunks, H, Wq, Wk, Wv, Kf, Vf, O};
   int max_len;
-  st = check_chunks(*desc, chunks, info.tot.n_tok, &max_len);
-  if (st != FUSE_OK) return st;
-  if (info.tot.n_out > 0 && (!H || !Wq || !Wk || !Wv || !Kf || !Vf || !O))
-    return FUSE_ERR_INVALID_ARG;
-  if (info.tot.n_sel > 0 && !idx) return FUSE_ERR_INVALID_ARG;
-  if (score_this_layer && info.tot.n_ctx > 0 && !score) return FUSE_ERR_INVALID_ARG;
-  if (!aligned16(H) || !aligned16(Wq) || !aligned16(Wk) || !aligned16(Wv) || !aligned16(Kf) ||
-      !aligned16(Vf) || !aligned16(O) || !aligned16(score))
-    return FUSE_ERR_MISALIGNED;
-  st = check_ws(ws, ws_bytes, ws_layout(*desc, info.tot, info.n_req).total);
+  st = check_layer(*desc, info, la, score_this_layer != 0, idx, score, ws, ws_bytes, &max_len);
   if (st != FUSE_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
   st = do_stitch(*desc, *chunks, max_len, Kf, Vf, ws, s);
   if (st != FUSE_OK) return st;
   if (score_this_layer) {
-    st = do_score(*desc, *reqs, info, H, Wv, Vf, score, ws, s, /*reduce=*/false);
-    if (st != FUSE_OK) return st;
-    if (tc_gemm_supported(*desc)) {
-      if (info.tot.n_sel > 0) {
-        const WsLayout L = ws_layout(*desc, info.tot, info.n_req);
-        st = cuda_status(traced("topk", s, [&] {
-          return launch_topk(*reqs, info.tot.max_ctx, score, idx, at<uint32_t>(ws, L.keys),
-                             at<uint32_t>(ws, 0), s);
-        }));
-      }
-    } else {
-      st = do_reduce_topk(*desc, *reqs, info, score, idx, ws, s);
-    }
+    st = do_score_select(*desc, *reqs, info, H, Wv, Vf, score, idx, ws, s);
     if (st != FUSE_OK) return st;
   }
   return do_recompute(*desc, *reqs, info, H, Wq, Wk, Wv, idx, Kf, Vf, O, ws, s);
+}
+
+fuse_status_t fuse_stack_step(const fuse_layer_desc_t* desc, const fuse_requests_t* reqs,
+                              int32_t n_layers, int32_t score_layer, const fuse_layer_io_t* layers,
+                              int32_t* idx, float* score, void* ws, size_t ws_bytes,
+                              fuse_stream_t stream) {
+  fuse_status_t st = check_desc(desc);
+  if (st != FUSE_OK) return st;
+  ReqInfo info;
+  st = check_reqs(reqs, &info);
+  if (st != FUSE_OK) return st;
+  if (n_layers <= 0 || !layers || score_layer < 0 || score_layer >= n_layers)
+    return FUSE_ERR_INVALID_ARG;
+  std::vector<int> max_len(n_layers);
+  for (int l = 0; l < n_layers; ++l) {
+    const fuse_layer_io_t& L = layers[l];
+    LayerArgs la{L.chunks, L.H, L.Wq, L.Wk, L.Wv, L.Kf, L.Vf, L.O};
+    st = check_layer(*desc, info, la, l == score_layer, idx, score, ws, ws_bytes, &max_len[l]);
+    if (st != FUSE_OK) return st;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  const fuse_layer_io_t& S = layers[score_layer];
+  st = do_stitch(*desc, *S.chunks, max_len[score_layer], S.Kf, S.Vf, ws, s);
+  if (st != FUSE_OK) return st;
+  st = do_score_select(*desc, *reqs, info, S.H, S.Wv, S.Vf, score, idx, ws, s);
+  if (st != FUSE_OK) return st;
+  for (int l = 0; l < n_layers; ++l) {
+    const fuse_layer_io_t& L = layers[l];
+    if (l != score_layer) {
+      st = do_stitch(*desc, *L.chunks, max_len[l], L.Kf, L.Vf, ws, s);
+      if (st != FUSE_OK) return st;
+    }
+    st = do_recompute(*desc, *reqs, info, L.H, L.Wq, L.Wk, L.Wv, idx, L.Kf, L.Vf, L.O, ws, s);
+    if (st != FUSE_OK) return st;
+  }
+  return FUSE_OK;
 }
 
 fuse_status_t fuse_pic_precompute(const fuse_layer_desc_t* desc, const fuse_chunks_t* chunks,

@@ -65,6 +65,12 @@ class Requests(_c.Structure):
     _fields_ = [("n_req", _c.c_int32), ("h_req", _c.c_void_p), ("d_req", _c.c_void_p)]
 
 
+class LayerIO(_c.Structure):
+    _fields_ = [("chunks", _c.c_void_p), ("H", _c.c_void_p), ("Wq", _c.c_void_p),
+                ("Wk", _c.c_void_p), ("Wv", _c.c_void_p), ("Kf", _c.c_void_p), ("Vf", _c.c_void_p),
+                ("O", _c.c_void_p)]
+
+
 class Totals(_c.Structure):
     _fields_ = [("n_tok", _c.c_int64), ("n_ctx", _c.c_int64), ("n_sel", _c.c_int64),
                 ("n_out", _c.c_int64), ("max_ctx", _c.c_int32), ("max_tok", _c.c_int32)]
@@ -96,6 +102,7 @@ _SIGS = {
     "fuse_layer_step": (_c.c_int, [_P, _P, _P, _P, _P, _P, _P, _c.c_int32, _P, _P, _P, _P, _P,
                                    _P, _c.c_size_t, _P]),
     "fuse_pic_precompute": (_c.c_int, [_P, _P, _P, _P, _P, _P, _c.c_size_t, _P]),
+    "fuse_stack_step": (_c.c_int, [_P, _P, _c.c_int32, _c.c_int32, _P, _P, _P, _P, _c.c_size_t, _P]),
     "fuse_check_errors": (_c.c_int, [_P, _P, _c.POINTER(_c.c_uint32)]),
     "fuse_trace_begin": (_c.c_int, [_c.c_int32]),
     "fuse_trace_end": (_c.c_int, [_P, _c.c_int32, _c.POINTER(_c.c_int32)]),
@@ -267,6 +274,18 @@ def layer_step(desc, chunks: ChunkTable, reqs: RequestTable, H, Wq, Wk, Wv, scor
                                   _ptr(Wq), _ptr(Wk), _ptr(Wv), int(bool(score_this_layer)),
                                   _ptr(idx), _ptr(Kf), _ptr(Vf), _ptr(O), _ptr(score), _ptr(ws),
                                   ws.numel(), _stream(stream)), "fuse_layer_step")
+
+
+def stack_step(desc, reqs: RequestTable, layers, score_layer: int, idx, score, ws, stream=None):
+    """``layers``: objects with ``chunks`` (ChunkTable), ``H``, ``Wq``, ``Wk``, ``Wv``,
+    ``Kf``, ``Vf``, ``O`` (one per layer)."""
+    arr = (LayerIO * len(layers))()
+    for i, b in enumerate(layers):
+        arr[i] = LayerIO(_c.addressof(b.chunks.c), _ptr(b.H), _ptr(b.Wq), _ptr(b.Wk), _ptr(b.Wv),
+                         _ptr(b.Kf), _ptr(b.Vf), _ptr(b.O))
+    _check(load().fuse_stack_step(_c.byref(desc), _c.byref(reqs.c), len(layers), int(score_layer),
+                                  arr, _ptr(idx), _ptr(score), _ptr(ws), ws.numel(),
+                                  _stream(stream)), "fuse_stack_step")
 
 
 def pic_precompute(desc, chunks: ChunkTable, H_clean, Wk, Wv, ws, stream=None):
