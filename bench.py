@@ -52,6 +52,37 @@ def _peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+# ncu DRAM traffic per launch recorded under profiles/, valid only while the
+# kernel's sources are unchanged (hash of the files that define it)
+_PROFILED = {
+    "attention_tc": ("attn_tc_kernel_qwen3_8b_layer.md",
+                     ["attention_tc.cu", "tc_ptx.cuh", "common.cuh"]),
+}
+
+
+def _traffic(kernel):
+    import hashlib
+    if kernel not in _PROFILED:
+        return None
+    md, srcs = _PROFILED[kernel]
+    path = os.path.join(ROOT, "profiles", md)
+    if not os.path.exists(path):
+        return None
+    h = hashlib.sha256()
+    for f in srcs:
+        with open(os.path.join(ROOT, "rag_kv_cache_rerotate_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    vals = {}
+    with open(path) as fh:
+        for line in fh:
+            if ":" in line and line.split(":")[0].strip() in ("traffic_bytes_per_launch", "sources_sha256_16"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("sources_sha256_16") != h.hexdigest()[:16]:
+        return None
+    return float(vals["traffic_bytes_per_launch"])
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -352,7 +383,7 @@ def native_run(args, ws, rank, local):
         else:
             ach, peak, unit = amount / avg_s / 1e12, bf16_tf_sus, "TFLOP/s"
         roof = {"bound": bound, "kernel": dom, "achieved": ach, "peak": peak, "unit": unit,
-                "frac": ach / peak, "traffic": None,
+                "frac": ach / peak, "traffic": _traffic(dom),
                 "peak_source": f"{peak_src} ({'sustained bf16' if bound == 'tensor' else 'HBM copy'})"}
 
     # end to end through the C ABI with host buffers
