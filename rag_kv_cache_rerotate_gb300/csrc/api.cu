@@ -26,9 +26,10 @@ bool tc_attention_supported(const fuse_layer_desc_t& desc);
 int attention_rtile(const fuse_layer_desc_t& d);
 size_t attention_tiles_bytes(int64_t n_out, int n_req);
 cudaError_t launch_attention_tc(const fuse_layer_desc_t& d, const fuse_requests_t& reqs,
-                                int64_t n_out, int64_t n_tok, const WorkRow* rows, const void* Q,
-                                const void* Kf, const void* Vf, void* O, void* tiles_ws,
-                                bool tiles_ready, uint32_t* err, cudaStream_t s);
+                                int64_t n_out, int64_t n_tok, const WorkRow* rows,
+                                const int32_t* idx, const void* Q, const void* Kf, const void* Vf,
+                                void* O, void* tiles_ws, bool tiles_ready, uint32_t* err,
+                                cudaStream_t s);
 
 namespace {
 
@@ -280,8 +281,8 @@ fuse_status_t do_recompute(const fuse_layer_desc_t& d, const fuse_requests_t& r,
   if (e != cudaSuccess) return FUSE_ERR_CUDA;
   if (tc_attn)
     e = traced("attention_tc", s, [&] {
-      return launch_attention_tc(d, r, R, info.tot.n_tok, rows, Q, Kf, Vf, O, at<void>(ws, L.tiles),
-                                 /*tiles_ready=*/tc_gemm, err, s);
+      return launch_attention_tc(d, r, R, info.tot.n_tok, rows, idx, Q, Kf, Vf, O,
+                                 at<void>(ws, L.tiles), /*tiles_ready=*/tc_gemm, err, s);
     });
   else
     e = traced("attention_simt", s, [&] { return launch_attention_simt(d, R, rows, Q, Kf, Vf, O, s); });

@@ -154,4 +154,34 @@ struct WorkRow {
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+#ifdef __CUDACC__
+// Tile records of the tensor-core attention: the recomputed rows of each
+// request cut into tiles of rtile rows, in request order, each recorded as
+// (first output row, the request's first fused row, rows, key blocks), the
+// key blocks being those up to the position of the tile's last row (selected
+// index, clamped to the request like the row tables, or n_ctx + query row).
+// Run by every thread of one block (the caller's branch must be block-uniform).
+__device__ inline void build_attn_tiles(const fuse_request_t* reqs, int n_req, const int32_t* idx,
+                                        int rtile, int4* tiles) {
+  __shared__ int s_nt;
+  if (threadIdx.x == 0) {
+    int nt = 0;
+    for (int q = 0; q < n_req; ++q) {
+      const int n = reqs[q].k + reqs[q].n_query;
+      for (int r0 = 0; r0 < n; r0 += rtile) tiles[nt++] = make_int4(q, r0, min(rtile, n - r0), 0);
+    }
+    s_nt = nt;
+  }
+  __syncthreads();
+  const int nt = s_nt;
+  for (int t = threadIdx.x; t < nt; t += blockDim.x) {
+    const int4 x = tiles[t];
+    const fuse_request_t R = reqs[x.x];
+    const int o = x.y + x.z - 1;
+    const int pos = o < R.k ? min(max(idx[R.sel0 + o], 0), max(R.n_ctx - 1, 0)) : R.n_ctx + (o - R.k);
+    tiles[t] = make_int4((int)R.out0 + x.y, (int)R.row0, x.z, pos / 128 + 1);
+  }
+}
+#endif
+
 }  // namespace fusekv

@@ -60,8 +60,8 @@ __global__ void sel_rows_kernel(const fuse_request_t* reqs, const int32_t* idx, 
 }
 
 // One block per recomputed row (blockIdx.y = request): the work row, its RoPE
-// table and the gathered copy Hs[out] = H[row0 + s]; block (0, 0) also lays out
-// the attention tiles (rtile rows of one request each).
+// table and the gathered copy Hs[out] = H[row0 + s]; block (0, 0) also writes
+// the attention tile records (build_attn_tiles).
 __global__ void __launch_bounds__(256) prepare_rows_kernel(const fuse_request_t* reqs, int n_req,
                                                            const int32_t* idx, RopeFreqs f,
                                                            int half_dim, const __nv_bfloat16* H,
@@ -72,13 +72,7 @@ __global__ void __launch_bounds__(256) prepare_rows_kernel(const fuse_request_t*
   const fuse_request_t R = reqs[r];
   const int o = blockIdx.x;
   const int t = threadIdx.x;
-  if (tiles && o == 0 && r == 0 && t == 0) {
-    int nt = 0;
-    for (int q = 0; q < n_req; ++q) {
-      const int n = reqs[q].k + reqs[q].n_query;
-      for (int r0 = 0; r0 < n; r0 += rtile) tiles[nt++] = make_int4(q, r0, min(rtile, n - r0), 0);
-    }
-  }
+  if (tiles && o == 0 && r == 0) build_attn_tiles(reqs, n_req, idx, rtile, tiles);
   if (o >= R.k + R.n_query) return;
   int s;
   if (o < R.k) {

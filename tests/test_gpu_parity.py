@@ -28,6 +28,11 @@ SMALL = {
     "paged3": synth.scaled(C["llama3_8b_paged_batch16"], n_requests=3),
     # four 1024-token chunks of the int8 long-context workload
     "int8_4x1024": synth.scaled(C["llama3_70b_int8_long"], chunks_per_request=4, query_len=64),
+    # 8192 context tokens, 1 % selected: row tiles span thousands of positions,
+    # so the attention plan splits their key ranges into up to five pieces and
+    # some rows lie wholly before the first key of a piece
+    "sparse_long_bf16": synth.scaled(C["qwen3_8b_layer"], chunks_per_request=16, ratio=0.01,
+                                     seed=21),
     # ragged: odd chunk lengths, 1-token chunks, a short query, fp32
     "ragged_fp32": synth.scaled(C["tiny_fp32"], chunks_per_request=None, chunk_len=None,
                                 query_len=None, chunk_count_range=(1, 6),
@@ -254,7 +259,7 @@ def test_recompute_selected(name):
 # fp64 dequantise-and-rotate) moves them by more than 2e-2, so that recipe is
 # checked step by step instead (stitch, score/top-k, recompute above).
 @pytest.mark.parametrize("name", ["tiny_fp32", "qwen3_8b_layer", "paged3", "ragged_fp32",
-                                  "ragged_paged_bf16_d64"])
+                                  "ragged_paged_bf16_d64", "sparse_long_bf16"])
 def test_layer_step(name):
     case = case_of(name)
     b = buffers(case)
