@@ -9,21 +9,28 @@
 // one request, whose g query heads share that KV head, packed as the M = 128
 // rows of the MMA (row r, head hh -> M row r * g + hh).  Keys stream in
 // blocks of 128 up to the tile's last position.  Per block b of unit i:
-//   S = Q K_b^T          tcgen05.mma into TMEM buffer b & 1 (columns
-//                        [128 (b & 1), 128 (b & 1) + 128)), so the next
-//                        block's scores are formed during this block's softmax
-//   P = 2^(S - m)        one warpgroup, each thread one M row and all 128 keys:
-//                        a pass for the row maximum, a pass for the
-//                        probabilities, written back as bf16 over S
-//   O_i += P V_b         tcgen05.mma with A = P in TMEM, V read from shared
-//                        memory as an MN-major operand, O in TMEM buffer i & 1
-//                        (columns [256 + 128 (i & 1), ...))
+//   S = Q K_b^T          tcgen05.mma into TMEM buffer b % 3 (columns
+//                        [128 (b % 3), 128 (b % 3) + 128)), so the scores of
+//                        the next blocks are formed during this block's
+//                        softmax
+//   P = 2^(S - m)        eight warps; each thread holds two M rows x 32 keys
+//                        of the block in registers (TMEM shape 16x256b: rows
+//                        t/4 and t/4 + 8 of the warp's 16 lanes, key pairs
+//                        8q + 2(t%4) + {0, 1}), the four threads of a row
+//                        exchange maxima by shuffles, and each key pair is
+//                        one bf16x2 column of P (shape 16x128b: column
+//                        4q + t%4), written back over S
+//   O += P V_b           tcgen05.mma with A = P in TMEM, V read from shared
+//                        memory as an MN-major operand, O in TMEM columns
+//                        [384, 512)
 // The running maximum m is raised only when a block exceeds it by more than
-// 2^8 (then O and the running sum l are rescaled).  A second warpgroup writes
-// O / l of unit i while the first works on unit i + 1.
-// Roles, each behind its own mbarriers: warp 0 loads Q and K blocks (3-stage
+// 2^8 (then O and the running sum l are rescaled).  A separate warpgroup
+// writes O / l of a unit while the softmax starts on the next one (whose
+// first P.V waits until O has been read).
+// Roles, each behind its own mbarriers: warp 0 loads Q (two buffers, so the
+// next unit's Q lands while this one's scores are formed) and K blocks (3-stage
 // ring), warp 2 V blocks (2-stage ring), warp 1 issues the S MMAs, warp 3 the
-// P.V MMAs, warps 4-7 the softmax, warps 8-11 the output.  Every role reads
+// P.V MMAs, warps 4-11 the softmax, warps 12-15 the output.  Every role reads
 // the unit's tile record (first output row, first fused row, rows, key
 // blocks) one unit ahead.  The kernel is persistent; units are taken heaviest
 // first, snake-ordered over the CTAs (round r visits the CTAs upwards when r
@@ -48,10 +55,12 @@ constexpr int kHalf = 128 * 64 * 2;           // one 64-column half of a 128-row
 constexpr int kTile = 2 * kHalf;              // 32 KB
 constexpr int kKStages = 3;
 constexpr int kVStages = 2;
-constexpr int kWarpQK = 0, kWarpS = 1, kWarpV = 2, kWarpPV = 3, kWarpSoft = 4, kWarpOut = 8;
-constexpr int kThreads = 12 * 32;             // 3 warps per SM sub-partition: up to 168 registers
-constexpr int kTmemCols = 512;                // S0 | S1 | O0 | O1
-constexpr int kColO = 256;
+constexpr int kWarpQK = 0, kWarpS = 1, kWarpV = 2, kWarpPV = 3, kWarpSoft = 4, kWarpOut = 12;
+constexpr int kSoftThreads = 256;
+constexpr int kThreads = 16 * 32;
+constexpr int kTmemCols = 512;                // S0 | S1 | S2 | O
+constexpr int kSBufs = 3;
+constexpr int kColO = 384;
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
 // Reference maximum of a row none of whose keys so far was visible (log2
 // units): above every masked score (-1e30 * scale) and below every real one,
@@ -73,16 +82,16 @@ struct AttnArgs {
 };
 
 struct Ctl {
-  uint64_t q_full, q_empty;
+  uint64_t q_full[2], q_empty[2];
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
-  uint64_t s_full[2], p_full[2], pv_done[2];   // [block parity]
-  uint64_t o_full[2], o_empty[2], l_full[2];   // [unit parity]
+  uint64_t s_full[kSBufs], p_full[kSBufs], pv_done[kSBufs];   // [block % 3]
+  uint64_t o_full, o_empty, l_full;                            // once per unit
   uint32_t tmem_base;
   volatile int abort_flag;
-  float xl[2][128];       // [unit parity][row] softmax row sum
+  float xl[128];          // [row] softmax row sum of the unit being written
 };
-constexpr int kSmemBytes = (1 + kKStages + kVStages) * kTile + 1024 + (int)sizeof(Ctl);
+constexpr int kSmemBytes = (2 + kKStages + kVStages) * kTile + 1024 + (int)sizeof(Ctl);
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ctl* ctl) {
@@ -180,16 +189,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap mapV, const AttnArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sK = smem + kTile;                       // K stage s at sK + s * kTile
+  uint8_t* sQ = smem;                               // Q buffer q at sQ + q * kTile
+  uint8_t* sK = smem + 2 * kTile;                   // K stage s at sK + s * kTile
   uint8_t* sV = sK + kKStages * kTile;              // V stage s at sV + s * kTile
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + (1 + kKStages + kVStages) * kTile);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + (2 + kKStages + kVStages) * kTile);
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
-    tc::mbar_init(&ctl->q_full, 1);
-    tc::mbar_init(&ctl->q_empty, 1);
+    for (int q = 0; q < 2; ++q) {
+      tc::mbar_init(&ctl->q_full[q], 1);
+      tc::mbar_init(&ctl->q_empty[q], 1);
+    }
     for (int s = 0; s < kKStages; ++s) {
       tc::mbar_init(&ctl->k_full[s], 1);
       tc::mbar_init(&ctl->k_empty[s], 1);
@@ -198,14 +209,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(&ctl->v_full[s], 1);
       tc::mbar_init(&ctl->v_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kSBufs; ++s) {
       tc::mbar_init(&ctl->s_full[s], 1);
-      tc::mbar_init(&ctl->p_full[s], 128);
+      tc::mbar_init(&ctl->p_full[s], kSoftThreads);
       tc::mbar_init(&ctl->pv_done[s], 1);
-      tc::mbar_init(&ctl->o_full[s], 1);
-      tc::mbar_init(&ctl->o_empty[s], 128);
-      tc::mbar_init(&ctl->l_full[s], 128);
     }
+    tc::mbar_init(&ctl->o_full, 1);
+    tc::mbar_init(&ctl->o_empty, 128);
+    tc::mbar_init(&ctl->l_full, kSoftThreads);
     ctl->abort_flag = 0;
     tc::fence_barrier_init();
     tc::tma_prefetch_desc(&mapQ);
@@ -231,13 +242,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int4 cur = T;
         if (unit_at(i + 1) < n_units) T = tile_of(a, unit_at(i + 1));   // next unit's record
         const int kvh = u % a.Hkv;
-        if (!wait_or_abort(&ctl->q_empty, (i & 1) ^ 1, ctl)) {
+        const int qb = i & 1;
+        if (!wait_or_abort(&ctl->q_empty[qb], ((i >> 1) & 1) ^ 1, ctl)) {
           abort_kernel(ctl, a.err, W_Q_EMPTY, 0);
           break;
         }
-        tc::mbar_arrive_expect_tx(&ctl->q_full, kTile);
-        tc::tma_load_3d(sQ, &mapQ, &ctl->q_full, 0, kvh * a.g, cur.x);
-        tc::tma_load_3d(sQ + kHalf, &mapQ, &ctl->q_full, 64, kvh * a.g, cur.x);
+        uint8_t* q = sQ + qb * kTile;
+        tc::mbar_arrive_expect_tx(&ctl->q_full[qb], kTile);
+        tc::tma_load_3d(q, &mapQ, &ctl->q_full[qb], 0, kvh * a.g, cur.x);
+        tc::tma_load_3d(q + kHalf, &mapQ, &ctl->q_full[qb], 64, kvh * a.g, cur.x);
         for (int j = 0; j < cur.w; ++j, ++kc) {
           const int st = kc % kKStages;
           if (!wait_or_abort(&ctl->k_empty[st], ((kc / kKStages) & 1) ^ 1, ctl)) {
@@ -253,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // let copies in flight land before the CTA may exit
-      if (i > 0) tc::mbar_wait(&ctl->q_full, (i - 1) & 1);
+      for (int k = (i > 2 ? i - 2 : 0); k < i; ++k) tc::mbar_wait(&ctl->q_full[k & 1], (k >> 1) & 1);
       for (uint32_t c = (kc > (uint32_t)kKStages ? kc - kKStages : 0); c < kc; ++c)
         tc::mbar_wait(&ctl->k_full[c % kKStages], (c / kKStages) & 1);
     }
@@ -289,17 +302,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------ S = Q K^T ------------------------------
     if (lane == 0) {
       const uint32_t idesc_s = tc::idesc_bf16_f32(128, kKB);
-      const uint32_t q_addr = tc::smem_u32(sQ);
       uint32_t kc = 0, b = 0;
       bool ok = true;
       int4 T = unit_at(0) < n_units ? tile_of(a, unit_at(0)) : make_int4(0, 0, 0, 0);
       for (int i = 0; unit_at(i) < n_units && ok; ++i) {
         const int nkb = T.w;
         if (unit_at(i + 1) < n_units) T = tile_of(a, unit_at(i + 1));
-        if (!wait_or_abort(&ctl->q_full, i & 1, ctl)) {
+        const int qb = i & 1;
+        if (!wait_or_abort(&ctl->q_full[qb], (i >> 1) & 1, ctl)) {
           abort_kernel(ctl, a.err, W_Q_FULL, 0);
           break;
         }
+        const uint32_t q_addr = tc::smem_u32(sQ + qb * kTile);
         for (int j = 0; j < nkb; ++j, ++kc, ++b) {
           const int st = kc % kKStages;
           if (!wait_or_abort(&ctl->k_full[st], (kc / kKStages) & 1, ctl)) {
@@ -307,23 +321,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          // buffer b & 1 holds P of block b - 2 until that block's P.V is done
-          if (!wait_or_abort(&ctl->pv_done[b & 1], ((b >> 1) & 1) ^ 1, ctl)) {
+          // buffer b % 3 holds P of block b - 3 until that block's P.V is done
+          const uint32_t sb = b % kSBufs;
+          if (!wait_or_abort(&ctl->pv_done[sb], ((b / kSBufs) & 1) ^ 1, ctl)) {
             abort_kernel(ctl, a.err, W_S_FREE, j);
             ok = false;
             break;
           }
           tc::tc_fence_after();
           const uint32_t kaddr = tc::smem_u32(sK + st * kTile);
-          const uint32_t d = tmem + (b & 1) * kKB;
+          const uint32_t d = tmem + sb * kKB;
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk)
             tc::mma_bf16(d, kmajor_step(q_addr, kk), kmajor_step(kaddr, kk), idesc_s, kk != 0);
-          tc::mma_commit(&ctl->s_full[b & 1]);
+          tc::mma_commit(&ctl->s_full[sb]);
           tc::mma_commit(&ctl->k_empty[st]);
         }
         if (!ok) break;
-        tc::mma_commit(&ctl->q_empty);
+        tc::mma_commit(&ctl->q_empty[qb]);
       }
     }
   } else if (warp == kWarpPV) {
@@ -336,14 +351,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; unit_at(i) < n_units && ok; ++i) {
         const int nkb = T.w;
         if (unit_at(i + 1) < n_units) T = tile_of(a, unit_at(i + 1));
-        const uint32_t o = tmem + kColO + (i & 1) * kD;
-        // O_(i & 1) was last read by the output warps for unit i - 2
-        if (!wait_or_abort(&ctl->o_empty[i & 1], ((i >> 1) & 1) ^ 1, ctl)) {
+        const uint32_t o = tmem + kColO;
+        // O was last read by the output warps for unit i - 1
+        if (!wait_or_abort(&ctl->o_empty, (i & 1) ^ 1, ctl)) {
           abort_kernel(ctl, a.err, W_O_EMPTY, 0);
           break;
         }
         for (int j = 0; j < nkb; ++j, ++vc, ++b) {
-          if (!wait_or_abort(&ctl->p_full[b & 1], (b >> 1) & 1, ctl)) {
+          const uint32_t sb = b % kSBufs;
+          if (!wait_or_abort(&ctl->p_full[sb], (b / kSBufs) & 1, ctl)) {
             abort_kernel(ctl, a.err, W_P_FULL, j);
             ok = false;
             break;
@@ -356,145 +372,164 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc::tc_fence_after();
           const uint32_t vaddr = tc::smem_u32(sV + st * kTile);
-          const uint32_t pa = tmem + (b & 1) * kKB;
+          const uint32_t pa = tmem + sb * kKB;
 #pragma unroll
           for (int kk = 0; kk < kKB / 16; ++kk)
             tc::mma_bf16_ts(o, pa + kk * 8, tc::smem_desc_mn128(vaddr + kk * 16 * 128, kHalf),
                             idesc_o, (j | kk) != 0 ? 1u : 0u);
-          tc::mma_commit(&ctl->pv_done[b & 1]);
+          tc::mma_commit(&ctl->pv_done[sb]);
           tc::mma_commit(&ctl->v_empty[st]);
         }
         if (!ok) break;
-        tc::mma_commit(&ctl->o_full[i & 1]);
+        tc::mma_commit(&ctl->o_full);
       }
     }
   } else if (warp < kWarpOut) {
     // ------------------------------- softmax -------------------------------
-    const int quarter = warp & 3;                      // TMEM lane quarter
-    const int m = quarter * 32 + lane;                 // M row = TMEM lane
-    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    // warp w: TMEM lane quarter w % 4, half (w - 4) / 4 of it: 16 M rows
+    const int base = (warp & 3) * 32 + ((warp - kWarpSoft) >> 2) * 16;
+    const uint32_t lane_off = (uint32_t)base << 16;
+    const int c4 = lane & 3;
+    const int R0 = base + (lane >> 2), R1 = R0 + 8;    // this thread's two M rows
+    const int rl0 = R0 / a.g, rl1 = R1 / a.g;
     const float scale = a.scale_log2;
-    const int rl = m / a.g;
     uint32_t b = 0;
     // this unit's record and positions, read one unit ahead
     int4 T = unit_at(0) < n_units ? tile_of(a, unit_at(0)) : make_int4(0, 0, 1, 0);
-    int p_next = 0, pf_next = 0;
+    int p0n = 0, p1n = 0, pfn = 0;
     if (unit_at(0) < n_units) {
-      p_next = a.rows[T.x + min(rl, T.z - 1)].pos;
-      pf_next = a.rows[T.x].pos;
+      p0n = a.rows[T.x + min(rl0, T.z - 1)].pos;
+      p1n = a.rows[T.x + min(rl1, T.z - 1)].pos;
+      pfn = a.rows[T.x].pos;
     }
     for (int i = 0; unit_at(i) < n_units; ++i) {
       const int nkb = T.w;
-      const int p = p_next;
-      const int p_first = pf_next;                     // rows ascend: the tile's smallest
+      const int p0 = p0n, p1 = p1n;
+      const int p_first = pfn;                         // rows ascend: the tile's smallest
       const bool more = unit_at(i + 1) < n_units;
       if (more) T = tile_of(a, unit_at(i + 1));
-      const uint32_t tO = tmem + lane_off + kColO + (i & 1) * kD;
-      float mu = kFloor, l = 0.f;                      // running max (log2 units), sum
+      const uint32_t tO = tmem + lane_off + kColO;
+      float mu0 = kFloor, mu1 = kFloor;                // running maxima (log2 units)
+      float l0 = 0.f, l1 = 0.f;                        // this thread's part of the row sums
       bool ok = true;
       for (int j = 0; j < nkb; ++j, ++b) {
-        if (!warp_wait_or_abort(&ctl->s_full[b & 1], (b >> 1) & 1, ctl)) {
+        const uint32_t sb = b % kSBufs;
+        if (!warp_wait_or_abort(&ctl->s_full[sb], (b / kSBufs) & 1, ctl)) {
           abort_kernel(ctl, a.err, W_S_FULL, j);
           ok = false;
           break;
         }
         tc::tc_fence_after();
-        const uint32_t tS = tmem + lane_off + (b & 1) * kKB;
+        const uint32_t tS = tmem + lane_off + sb * kKB;
         const int key0 = j * kKB;
-        const bool mask = key0 + kKB - 1 > p_first;     // warp-uniform
-        // the whole row of scores in registers: one TMEM round trip
-        uint32_t r[128];
-        tc::tmem_ld_32x32b_x32(tS, *reinterpret_cast<uint32_t(*)[32]>(r));
-        tc::tmem_ld_32x32b_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
-        tc::tmem_ld_32x32b_x32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(r + 64));
-        tc::tmem_ld_32x32b_x32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(r + 96));
+        uint32_t r[64];
+        tc::tmem_ld_16x256b_x8(tS, *reinterpret_cast<uint32_t(*)[32]>(r));
+        tc::tmem_ld_16x256b_x8(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
         tc::tmem_ld_wait();
-        if (mask) {
+        if (key0 + kKB - 1 > p_first) {                // warp-uniform: some key may be masked
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (key0 + c > p) r[c] = __float_as_uint(-1e30f);
-        }
-        float mx;
-        {                                              // four running maxima, then one
-          float t0 = __uint_as_float(r[0]), t1 = __uint_as_float(r[1]);
-          float t2 = __uint_as_float(r[2]), t3 = __uint_as_float(r[3]);
-#pragma unroll
-          for (int q = 4; q < 128; q += 8) {
-            t0 = max3(t0, __uint_as_float(r[q]), __uint_as_float(r[q + 4]));
-            t1 = max3(t1, __uint_as_float(r[q + 1]), __uint_as_float(r[q + 5]));
-            t2 = max3(t2, __uint_as_float(r[q + 2]), __uint_as_float(r[q + 6]));
-            t3 = max3(t3, __uint_as_float(r[q + 3]), __uint_as_float(r[q + 7]));
+          for (int q = 0; q < 16; ++q) {
+            const int k = key0 + 8 * q + 2 * c4;
+            if (k > p0) r[4 * q] = __float_as_uint(-1e30f);
+            if (k + 1 > p0) r[4 * q + 1] = __float_as_uint(-1e30f);
+            if (k > p1) r[4 * q + 2] = __float_as_uint(-1e30f);
+            if (k + 1 > p1) r[4 * q + 3] = __float_as_uint(-1e30f);
           }
-          t0 = max3(t0, __uint_as_float(r[124]), __uint_as_float(r[125]));
-          t1 = max3(t1, __uint_as_float(r[126]), __uint_as_float(r[127]));
-          mx = fmaxf(max3(t0, t1, t2), t3);
         }
-        const float mxs = mx * scale;
-        float mnew = mu;
-        bool rescale = false;
+        float m0, m1;
+        {
+          float a0 = __uint_as_float(r[0]), a1 = __uint_as_float(r[1]);
+          float b0 = __uint_as_float(r[2]), b1 = __uint_as_float(r[3]);
+#pragma unroll
+          for (int q = 1; q < 15; q += 2) {                // repeats 1 .. 14 in pairs
+            a0 = max3(a0, __uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 4]));
+            a1 = max3(a1, __uint_as_float(r[4 * q + 1]), __uint_as_float(r[4 * q + 5]));
+            b0 = max3(b0, __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 6]));
+            b1 = max3(b1, __uint_as_float(r[4 * q + 3]), __uint_as_float(r[4 * q + 7]));
+          }
+          m0 = max3(a0, a1, fmaxf(__uint_as_float(r[60]), __uint_as_float(r[61])));   // repeat 15
+          m1 = max3(b0, b1, fmaxf(__uint_as_float(r[62]), __uint_as_float(r[63])));
+          m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
+          m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
+          m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
+          m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
+        }
+        const float ms0 = m0 * scale, ms1 = m1 * scale;
+        float mn0 = mu0, mn1 = mu1;
+        bool rs0 = false, rs1 = false;
         if (j == 0) {
-          mnew = fmaxf(mxs, kFloor);
-        } else if (mxs > mu + kRescaleThreshold) {
-          mnew = mxs;
-          rescale = true;
+          mn0 = fmaxf(ms0, kFloor);
+          mn1 = fmaxf(ms1, kFloor);
+        } else {
+          if (ms0 > mu0 + kRescaleThreshold) { mn0 = ms0; rs0 = true; }
+          if (ms1 > mu1 + kRescaleThreshold) { mn1 = ms1; rs1 = true; }
         }
-        const float alpha = rescale ? ex2(mu - mnew) : 1.f;
-        // probabilities, written as bf16 over the scores
-        const float neg = -mnew;
-        float sum = 0.f;
+        const float al0 = rs0 ? ex2(mu0 - mn0) : 1.f, al1 = rs1 ? ex2(mu1 - mn1) : 1.f;
+        // probabilities: key pairs packed as bf16x2, in place over the scores
+        const float ng0 = -mn0, ng1 = -mn1;
+        float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t pk[16];
-          float e[32];
-#pragma unroll
-          for (int q = 0; q < 32; ++q) e[q] = ex2(fmaf(__uint_as_float(r[32 * c + q]), scale, neg));
-#pragma unroll
-          for (int q = 0; q < 32; q += 2) pk[q / 2] = pack_bf16x2(e[q], e[q + 1]);
-#pragma unroll
-          for (int w = 16; w >= 1; w >>= 1)
-#pragma unroll
-            for (int q = 0; q < w; ++q) e[q] += e[q + w];
-          sum += e[0];
-          tc::tmem_st_32x32b_x16(tS + 16 * c, pk);
+        for (int q = 0; q < 16; ++q) {
+          const float e0 = ex2(fmaf(__uint_as_float(r[4 * q]), scale, ng0));
+          const float e1 = ex2(fmaf(__uint_as_float(r[4 * q + 1]), scale, ng0));
+          const float e2 = ex2(fmaf(__uint_as_float(r[4 * q + 2]), scale, ng1));
+          const float e3 = ex2(fmaf(__uint_as_float(r[4 * q + 3]), scale, ng1));
+          s0 += e0 + e1;
+          s1 += e2 + e3;
+          r[2 * q] = pack_bf16x2(e0, e1);
+          r[2 * q + 1] = pack_bf16x2(e2, e3);
         }
+        tc::tmem_st_16x128b_x16(tS, *reinterpret_cast<uint32_t(*)[32]>(r));
         // tcgen05.ld/st are warp-collective (.sync.aligned): the whole warp
-        // rescales its rows of O when any of them needs it (alpha is 1 for the
-        // others); O must hold the previous block's P.V
-        if (__any_sync(0xffffffffu, rescale)) {
-          if (!warp_wait_or_abort(&ctl->pv_done[(b - 1) & 1], ((b - 1) >> 1) & 1, ctl)) {
+        // rescales its rows of O when any of them needs it (the factor is 1
+        // for the others); O must hold the previous block's P.V
+        if (__any_sync(0xffffffffu, rs0 || rs1)) {
+          if (!warp_wait_or_abort(&ctl->pv_done[(b - 1) % kSBufs], ((b - 1) / kSBufs) & 1, ctl)) {
             abort_kernel(ctl, a.err, W_PV_DONE, j);
             ok = false;
             break;
           }
           tc::tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < kD; c += 32) {
+          for (int c = 0; c < kD; c += 64) {
             uint32_t o[32];
-            tc::tmem_ld_32x32b_x32(tO + c, o);
+            tc::tmem_ld_16x256b_x8(tO + c, o);
             tc::tmem_ld_wait();
 #pragma unroll
-            for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha);
-            tc::tmem_st_32x32b_x32(tO + c, o);
+            for (int q = 0; q < 32; ++q)
+              o[q] = __float_as_uint(__uint_as_float(o[q]) * ((q & 2) ? al1 : al0));
+            tc::tmem_st_16x256b_x8(tO + c, o);
           }
         }
         tc::tmem_st_wait();
         tc::tc_fence_before();
-        tc::mbar_arrive(&ctl->p_full[b & 1]);
-        l = l * alpha + sum;
-        mu = mnew;
+        tc::mbar_arrive(&ctl->p_full[sb]);
+        l0 = l0 * al0 + s0;
+        l1 = l1 * al1 + s1;
+        mu0 = mn0;
+        mu1 = mn1;
       }
       if (!ok) break;
       if (more) {
-        p_next = a.rows[T.x + min(rl, T.z - 1)].pos;
-        pf_next = a.rows[T.x].pos;
+        p0n = a.rows[T.x + min(rl0, T.z - 1)].pos;
+        p1n = a.rows[T.x + min(rl1, T.z - 1)].pos;
+        pfn = a.rows[T.x].pos;
       }
-      // the row sum of unit i, once the output warps have read that of unit i - 2
-      if (!warp_wait_or_abort(&ctl->o_empty[i & 1], ((i >> 1) & 1) ^ 1, ctl)) {
+      // row sums: the four threads of a row, in a fixed order
+      l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+      l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+      // the row sums of unit i, once the output warps are done with unit i - 1
+      if (!warp_wait_or_abort(&ctl->o_empty, (i & 1) ^ 1, ctl)) {
         abort_kernel(ctl, a.err, W_L_FREE, nkb);
         break;
       }
-      ctl->xl[i & 1][m] = l;
-      tc::mbar_arrive(&ctl->l_full[i & 1]);
+      if (c4 == 0) {
+        ctl->xl[R0] = l0;
+        ctl->xl[R1] = l1;
+      }
+      tc::mbar_arrive(&ctl->l_full);
     }
   } else {
     // ---------------------------- output O / l ----------------------------
@@ -509,19 +544,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int4 cur = T;
       if (unit_at(i + 1) < n_units) T = tile_of(a, unit_at(i + 1));
       const int kvh = u % a.Hkv;
-      if (!warp_wait_or_abort(&ctl->o_full[i & 1], (i >> 1) & 1, ctl)) {
+      if (!warp_wait_or_abort(&ctl->o_full, i & 1, ctl)) {
         abort_kernel(ctl, a.err, W_O_FULL, cur.w);
         break;
       }
-      if (!warp_wait_or_abort(&ctl->l_full[i & 1], (i >> 1) & 1, ctl)) {
+      if (!warp_wait_or_abort(&ctl->l_full, i & 1, ctl)) {
         abort_kernel(ctl, a.err, W_L_FULL, cur.w);
         break;
       }
       tc::tc_fence_after();
-      const float inv = 1.f / ctl->xl[i & 1][m];
+      const float inv = 1.f / ctl->xl[m];
       const bool valid = rl < cur.z;
       __nv_bfloat16* dst = a.O + ((int64_t)(cur.x + rl) * a.Hq + kvh * a.g + hh) * kD;
-      const uint32_t tO = tmem + lane_off + kColO + (i & 1) * kD;
+      const uint32_t tO = tmem + lane_off + kColO;
 #pragma unroll 1
       for (int c = 0; c < kD; c += 32) {
         uint32_t r[32];
@@ -540,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc::tc_fence_before();
-      tc::mbar_arrive(&ctl->o_empty[i & 1]);
+      tc::mbar_arrive(&ctl->o_empty);
     }
   }
 
