@@ -195,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + (2 + kKStages + kVStages) * kTile);
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
+  pdl_trigger();
 
   if (threadIdx.x == 0) {
     for (int q = 0; q < 2; ++q) {
@@ -229,6 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   const int n_units = a.n_units;
+  pdl_wait();                 // inputs of the previous kernel complete and visible
 
   if (warp == kWarpQK) {
     // --------------------------- Q and K loads ---------------------------
@@ -587,6 +589,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 __global__ void attn_tiles_kernel(const fuse_request_t* reqs, int n_req, const int32_t* idx,
                                   int rtile, int4* tiles) {
+  pdl_trigger();
+  pdl_wait();
   build_attn_tiles(reqs, n_req, idx, rtile, tiles);
 }
 
@@ -627,8 +631,8 @@ cudaError_t launch_attention_tc(const fuse_layer_desc_t& d, const fuse_requests_
   int4* tiles = reinterpret_cast<int4*>(tiles_ws);
   cudaError_t e = cudaSuccess;
   if (!tiles_ready) {
-    attn_tiles_kernel<<<1, 128, 0, s>>>(reqs.d_req, reqs.n_req, idx, rtile, tiles);
-    e = cudaGetLastError();
+    e = launch_pdl(attn_tiles_kernel, dim3(1), dim3(128), 0, s, reqs.d_req, reqs.n_req, idx, rtile,
+                   tiles);
     if (e != cudaSuccess) return e;
   }
 
@@ -659,8 +663,7 @@ cudaError_t launch_attention_tc(const fuse_layer_desc_t& d, const fuse_requests_
   e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = a.n_units < sm_count() ? a.n_units : sm_count();
-  attn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(mQ, mK, mV, a);
-  return cudaGetLastError();
+  return launch_pdl(attn_tc_kernel, dim3(grid), dim3(kThreads), kSmemBytes, s, mQ, mK, mV, a);
 }
 
 }  // namespace fusekv

@@ -41,6 +41,19 @@ __device__ __forceinline__ void report_error(uint32_t* err, fuse_status_t code, 
 }
 
 // ----------------------------------------------------------------------------
+// Programmatic dependent launch: every kernel of a call sequence is launched so
+// that it may start while the previous one drains (launch_pdl).  A kernel lets
+// the next one start once all of its own CTAs are running (pdl_trigger) and
+// waits for the previous kernel to complete, with its writes visible, before
+// it touches global memory (pdl_wait); only on-chip set-up runs before that.
+// Both are no-ops for a kernel launched without the attribute.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ----------------------------------------------------------------------------
 // Element types
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

@@ -217,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x % 32;
   const int total = a.m_tiles * a.n_tiles;
   const int k_blocks = a.K / BK;
+  pdl_trigger();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -239,6 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
+  pdl_wait();                 // inputs of the previous kernel complete and visible
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -410,8 +412,7 @@ cudaError_t launch(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtensor
                                        kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = total < sm_count() ? total : sm_count();
-  gemm_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(mA, mB0, mB1, mB2, a);
-  return cudaGetLastError();
+  return launch_pdl(gemm_tc_kernel, dim3(grid), dim3(kThreads), kSmemBytes, s, mA, mB0, mB1, mB2, a);
 }
 
 }  // namespace

@@ -3,9 +3,28 @@
 
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "common.cuh"
 
 namespace fusekv {
+
+// Launch with programmatic stream serialisation (see pdl_trigger/pdl_wait).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Stitch + re-rotate (+ dequantise, + paged gather) every chunk.
 cudaError_t launch_stitch(const fuse_layer_desc_t& desc, const fuse_chunks_t& chunks,

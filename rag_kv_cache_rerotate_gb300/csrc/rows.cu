@@ -68,6 +68,8 @@ __global__ void __launch_bounds__(256) prepare_rows_kernel(const fuse_request_t*
                                                            int hidden, WorkRow* rows, float2* rope,
                                                            __nv_bfloat16* Hs, int rtile,
                                                            int4* tiles, uint32_t* err) {
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.y;
   const fuse_request_t R = reqs[r];
   const int o = blockIdx.x;
@@ -114,11 +116,10 @@ cudaError_t launch_prepare_rows(const fuse_requests_t& reqs, int max_rows, const
                                 uint32_t* err, cudaStream_t s) {
   if (reqs.n_req == 0 || max_rows == 0) return cudaSuccess;
   dim3 grid(max_rows, reqs.n_req);
-  prepare_rows_kernel<<<grid, 256, 0, s>>>(reqs.d_req, reqs.n_req, idx, freqs, head_dim / 2,
-                                           reinterpret_cast<const __nv_bfloat16*>(H), hidden, rows,
-                                           rope, reinterpret_cast<__nv_bfloat16*>(Hs), rtile,
-                                           reinterpret_cast<int4*>(tiles), err);
-  return cudaGetLastError();
+  return launch_pdl(prepare_rows_kernel, grid, dim3(256), 0, s, reqs.d_req, reqs.n_req, idx, freqs,
+                    head_dim / 2, reinterpret_cast<const __nv_bfloat16*>(H), hidden, rows, rope,
+                    reinterpret_cast<__nv_bfloat16*>(Hs), rtile, reinterpret_cast<int4*>(tiles),
+                    err);
 }
 
 cudaError_t launch_build_score_map(const fuse_requests_t& reqs, int max_tok, int32_t* map,

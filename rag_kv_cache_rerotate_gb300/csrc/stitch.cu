@@ -99,6 +99,8 @@ __global__ void __launch_bounds__(kStitchThreads) stitch_kernel(const StitchArgs
   constexpr int VG = D / 8;            // 8-element groups per head (V)
   constexpr bool kU8 = sizeof(TS) == 1;
   constexpr bool kSame = sizeof(TS) == sizeof(TO) && !kU8;
+  pdl_trigger();
+  pdl_wait();
   const int chunk = blockIdx.x / a.tiles_per_chunk;
   const int tile = blockIdx.x % a.tiles_per_chunk;
   const fuse_chunk_t c = a.chunks[chunk];
@@ -236,8 +238,7 @@ template <typename TS, typename TO, int D, bool PAGED>
 cudaError_t launch_t(const StitchArgs& a, int n_chunks, cudaStream_t s) {
   const int grid = n_chunks * a.tiles_per_chunk;
   if (grid == 0) return cudaSuccess;
-  stitch_kernel<TS, TO, D, PAGED><<<grid, kStitchThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(stitch_kernel<TS, TO, D, PAGED>, dim3(grid), dim3(kStitchThreads), 0, s, a);
 }
 
 template <typename TS, typename TO>

@@ -68,6 +68,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const fuse_request_t
   __shared__ uint32_t hist[256];
   __shared__ uint32_t warp_buf[32];
   __shared__ uint32_t sel_digit, sel_remaining;
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   const fuse_request_t R = reqs[r];
   const int n = R.n_ctx;
@@ -222,9 +224,8 @@ cudaError_t launch_reduce_topk(const fuse_requests_t& reqs, int max_ctx, const f
                                          kTopkSmemKeys * (int)sizeof(uint32_t));
     if (e != cudaSuccess) return e;
   }
-  topk_kernel<<<reqs.n_req, kTopkThreads, smem, s>>>(reqs.d_req, nullptr, idx, keys_ws, err, in_smem,
-                                                     partial, n_kv_heads, score);
-  return cudaGetLastError();
+  return launch_pdl(topk_kernel, dim3(reqs.n_req), dim3(kTopkThreads), smem, s, reqs.d_req,
+                    (const float*)nullptr, idx, keys_ws, err, in_smem, partial, n_kv_heads, score);
 }
 
 cudaError_t launch_topk(const fuse_requests_t& reqs, int max_ctx, const float* score, int32_t* idx,
@@ -237,8 +238,8 @@ cudaError_t launch_topk(const fuse_requests_t& reqs, int max_ctx, const float* s
                                          kTopkSmemKeys * (int)sizeof(uint32_t));
     if (e != cudaSuccess) return e;
   }
-  topk_kernel<<<reqs.n_req, kTopkThreads, smem, s>>>(reqs.d_req, score, idx, keys_ws, err, in_smem);
-  return cudaGetLastError();
+  return launch_pdl(topk_kernel, dim3(reqs.n_req), dim3(kTopkThreads), smem, s, reqs.d_req, score,
+                    idx, keys_ws, err, in_smem, (const float*)nullptr, 0, (float*)nullptr);
 }
 
 }  // namespace fusekv
