@@ -16,8 +16,8 @@ bool tc_gemm_supported(const fuse_layer_desc_t& desc);
 cudaError_t launch_deviation_partials_tc(const fuse_layer_desc_t& desc, int64_t n_rows,
                                          const void* H, const void* Wv, const void* Vf,
                                          const int32_t* map, const fuse_request_t* d_req,
-                                         int n_req, float* partial, float* score,
-                                         uint32_t* row_count, uint32_t* err, cudaStream_t s);
+                                         int n_req, float* partial, uint32_t* err,
+                                         cudaStream_t s);
 cudaError_t launch_project_recompute_tc(const fuse_layer_desc_t& desc, int64_t n_rows,
                                         const WorkRow* rows, const float2* rope, const void* H,
                                         const void* Wq, const void* Wk, const void* Wv, void* Q,
@@ -143,7 +143,7 @@ fuse_status_t check_chunks(const fuse_layer_desc_t& d, const fuse_chunks_t* c, i
 
 // Workspace regions (each 256-byte aligned).
 struct WsLayout {
-  size_t partial, keys, map, rows, rope, q, hs, tiles, counts, total;
+  size_t partial, keys, map, rows, rope, q, hs, tiles, total;
 };
 
 WsLayout ws_layout(const fuse_layer_desc_t& d, const fuse_totals_t& t, int n_req) {
@@ -163,9 +163,15 @@ WsLayout ws_layout(const fuse_layer_desc_t& d, const fuse_totals_t& t, int n_req
   L.q = take((size_t)t.n_out * d.n_q_heads * d.head_dim * es);
   L.hs = take((size_t)t.n_out * d.hidden * es);
   L.tiles = take(attention_tiles_bytes(t.n_out, n_req));
-  L.counts = take((size_t)t.n_ctx * sizeof(uint32_t));       // zero between calls
   L.total = off;
   return L;
+}
+
+// Cosine partials per context token: one per pair of KV heads on the
+// tensor-core path (the two heads of a tile are summed in its epilogue), one
+// per KV head otherwise.
+int score_parts(const fuse_layer_desc_t& d) {
+  return tc_gemm_supported(d) ? d.n_kv_heads / 2 : d.n_kv_heads;
 }
 
 template <typename T> T* at(void* ws, size_t off) {
@@ -211,8 +217,7 @@ fuse_status_t do_score(const fuse_layer_desc_t& d, const fuse_requests_t& r, con
     if (tc)
       e = traced("deviation_gemm_tc", s, [&] {
         return launch_deviation_partials_tc(d, info.tot.n_tok, H, Wv, Vf, need_map ? map : nullptr,
-                                            r.d_req, r.n_req, partial, score,
-                                            at<uint32_t>(ws, L.counts), at<uint32_t>(ws, 0), s);
+                                            r.d_req, r.n_req, partial, at<uint32_t>(ws, 0), s);
       });
     else
       e = traced("deviation_gemm_simt", s, [&] {
@@ -220,10 +225,10 @@ fuse_status_t do_score(const fuse_layer_desc_t& d, const fuse_requests_t& r, con
                                               at<uint32_t>(ws, 0), s);
       });
   }
-  // the tensor-core epilogue writes the scores itself
-  if (e == cudaSuccess && reduce && !tc)
+  if (e == cudaSuccess && reduce)
     e = traced("deviation_reduce", s, [&] {
-      return launch_deviation_reduce(info.tot.n_ctx, d.n_kv_heads, partial, score, s);
+      return launch_deviation_reduce(info.tot.n_ctx, score_parts(d), d.n_kv_heads, partial, score,
+                                     s);
     });
   return cuda_status(e);
 }
@@ -235,8 +240,9 @@ fuse_status_t do_reduce_topk(const fuse_layer_desc_t& d, const fuse_requests_t& 
   const WsLayout L = ws_layout(d, info.tot, info.n_req);
   if (info.tot.n_ctx == 0) return FUSE_OK;
   return cuda_status(traced("reduce_topk", s, [&] {
-    return launch_reduce_topk(r, info.tot.max_ctx, at<float>(ws, L.partial), d.n_kv_heads, score,
-                              idx, at<uint32_t>(ws, L.keys), at<uint32_t>(ws, 0), s);
+    return launch_reduce_topk(r, info.tot.max_ctx, at<float>(ws, L.partial), score_parts(d),
+                              d.n_kv_heads, score, idx, at<uint32_t>(ws, L.keys),
+                              at<uint32_t>(ws, 0), s);
   }));
 }
 
@@ -322,13 +328,7 @@ fuse_status_t do_score_select(const fuse_layer_desc_t& d, const fuse_requests_t&
                               float* score, int32_t* idx, void* ws, cudaStream_t s) {
   fuse_status_t st = do_score(d, r, info, H, Wv, Vf, score, ws, s, /*reduce=*/false);
   if (st != FUSE_OK) return st;
-  if (!tc_gemm_supported(d)) return do_reduce_topk(d, r, info, score, idx, ws, s);
-  if (info.tot.n_sel == 0) return FUSE_OK;
-  const WsLayout L = ws_layout(d, info.tot, info.n_req);
-  return cuda_status(traced("topk", s, [&] {
-    return launch_topk(r, info.tot.max_ctx, score, idx, at<uint32_t>(ws, L.keys),
-                       at<uint32_t>(ws, 0), s);
-  }));
+  return do_reduce_topk(d, r, info, score, idx, ws, s);
 }
 
 }  // namespace

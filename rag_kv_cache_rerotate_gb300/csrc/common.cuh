@@ -127,32 +127,29 @@ __device__ __forceinline__ void rope_cos_sin(int p, float hi, float mid, float l
 }
 
 // ----------------------------------------------------------------------------
-// Deviation score of one token from its per-KV-head cosines.
+// Deviation score of one token from its cosine partials.
 // ----------------------------------------------------------------------------
-// 1 - (sum_h partial[h]) / Hkv, the sum taken in head order (the same
-// expression everywhere a score is formed); 16-byte loads when Hkv % 4 == 0.
-// kCoherent reads through L2 (partials written by other CTAs of the running
-// kernel); otherwise through the read-only path.
-template <bool kCoherent = false>
-__device__ __forceinline__ float head_mean_score(const float* pr, int n_kv_heads) {
+// The partials of a token are n_parts sums of its per-KV-head cosines (one
+// per head, or one per pair of heads); the score is
+// 1 - (sum_p partial[p]) / n_heads, the sum taken in partial order; 16-byte
+// loads when n_parts % 4 == 0.
+__device__ __forceinline__ float head_mean_score(const float* pr, int n_parts, int n_heads) {
   float acc = 0.f;
-  if ((n_kv_heads & 3) == 0) {
+  if ((n_parts & 3) == 0) {
     float4 v[4];
-    for (int h0 = 0; h0 < n_kv_heads; h0 += 16) {
-      const int nq = min(4, (n_kv_heads - h0) / 4);
+    for (int h0 = 0; h0 < n_parts; h0 += 16) {
+      const int nq = min(4, (n_parts - h0) / 4);
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        if (q < nq)
-          v[q] = kCoherent ? __ldcg(reinterpret_cast<const float4*>(pr + h0) + q)
-                           : __ldg(reinterpret_cast<const float4*>(pr + h0) + q);
+        if (q < nq) v[q] = __ldg(reinterpret_cast<const float4*>(pr + h0) + q);
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         if (q < nq) acc = (((acc + v[q].x) + v[q].y) + v[q].z) + v[q].w;
     }
   } else {
-    for (int h = 0; h < n_kv_heads; ++h) acc += kCoherent ? __ldcg(pr + h) : pr[h];
+    for (int h = 0; h < n_parts; ++h) acc += pr[h];
   }
-  return 1.0f - acc / (float)n_kv_heads;
+  return 1.0f - acc / (float)n_heads;
 }
 
 // ----------------------------------------------------------------------------

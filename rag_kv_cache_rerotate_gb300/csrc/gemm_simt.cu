@@ -267,10 +267,11 @@ cudaError_t dispatch(const fuse_layer_desc_t& desc, const GemmArgs& a, int n_tot
   return run<float>(a, n_total, desc.head_dim, s);
 }
 
-__global__ void deviation_reduce_kernel(int64_t n, int Hkv, const float* partial, float* score) {
+__global__ void deviation_reduce_kernel(int64_t n, int n_parts, int Hkv, const float* partial,
+                                        float* score) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
-  score[i] = head_mean_score(partial + i * Hkv, Hkv);
+  score[i] = head_mean_score(partial + i * n_parts, n_parts, Hkv);
 }
 
 }  // namespace
@@ -296,11 +297,12 @@ cudaError_t launch_deviation_partials_simt(const fuse_layer_desc_t& desc, int64_
   return dispatch(desc, a, a.n0, s);
 }
 
-cudaError_t launch_deviation_reduce(int64_t n_ctx, int n_kv_heads, const float* partial,
-                                    float* score, cudaStream_t s) {
+cudaError_t launch_deviation_reduce(int64_t n_ctx, int n_parts, int n_kv_heads,
+                                    const float* partial, float* score, cudaStream_t s) {
   if (n_ctx == 0) return cudaSuccess;
-  deviation_reduce_kernel<<<(unsigned)((n_ctx + 255) / 256), 256, 0, s>>>(n_ctx, n_kv_heads,
-                                                                          partial, score);
+  deviation_reduce_kernel<<<(unsigned)((n_ctx + 255) / 256), 256, 0, s>>>(n_ctx, n_parts,
+                                                                          n_kv_heads, partial,
+                                                                          score);
   return cudaGetLastError();
 }
 

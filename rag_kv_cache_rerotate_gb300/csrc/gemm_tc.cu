@@ -4,7 +4,9 @@
 //
 //   deviation (KVBoost Alg. 2 step 2, on V):  C = H W_V^T, and per (token,
 //     KV head) the cosine between the fresh V row of the tile and the cached
-//     V row -> partial[slot, h];
+//     V row, the two heads of a tile summed -> partial[slot, h / 2] (the
+//     score, 1 - the sum of a token's partials / Hkv, is formed by the top-k
+//     kernel);
 //   recompute (QCFuse Eqs. 6-7; KVBoost Eqs. 1-3):  C = Hs [W_Q; W_K; W_V]^T
 //     over the gathered rows S, RoPE at each row's request position on Q and
 //     K heads, Q to a compact buffer, K and V scattered into the fused cache.
@@ -17,7 +19,9 @@
 // 4-stage shared-memory ring, warp 1 issues tcgen05.mma into one of two TMEM
 // accumulators, warps 2-9 (one warpgroup per head of the tile) drain the other
 // accumulator through tcgen05.ld and run the epilogue, so the epilogue of tile
-// i overlaps the main loop of tile i + 1.
+// i overlaps the main loop of tile i + 1.  The epilogue warps load what they
+// read from global memory (cached V rows; work rows and RoPE factors) before
+// they wait for the accumulator, so those loads overlap the main loop.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -60,8 +64,6 @@ struct TcArgs {
   const fuse_request_t* reqs;    // sorted by row0, non-overlapping (when map is null)
   int n_req;
   float* partial;
-  float* score;                  // written by the last of a row's Hkv cosines
-  uint32_t* row_count;           // [N] zero between calls (each row resets its own)
   // recompute
   const WorkRow* rows;
   const float2* rope;
@@ -76,6 +78,8 @@ struct SharedCtl {
   uint64_t empty[STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
+  uint64_t xc_bar[2];          // [accumulator]: the second head's cosines written
+  float xc[2][BM];             // [accumulator][row]: cosine of the tile's second head
   uint32_t tmem_base;
   volatile int abort_flag;
 };
@@ -105,20 +109,34 @@ __device__ __forceinline__ int32_t row_slot(const TcArgs& a, int m) {
   return (t >= 0 && t < R.n_ctx) ? (int32_t)(R.score0 + t) : -1;
 }
 
-__device__ __forceinline__ void epi_deviation(const TcArgs& a, uint32_t taddr, int m, int head) {
-  const bool valid = m < a.M;
-  const int32_t slot = valid ? row_slot(a, m) : -1;
+// Operands of the deviation epilogue of one row and head, loaded before the
+// accumulator is ready: the score slot and the cached V row.
+struct DevPre {
+  int32_t slot;
+  uint4 v[BN / 8];
+};
+
+__device__ __forceinline__ void pre_deviation(const TcArgs& a, int m, int head, DevPre& p) {
+  p.slot = m < a.M ? row_slot(a, m) : -1;
+  if (p.slot >= 0) {
+    const uint4* vrow = reinterpret_cast<const uint4*>(a.Vf + ((int64_t)m * a.n_kv_heads + head) * BN);
+#pragma unroll
+    for (int q = 0; q < BN / 8; ++q) p.v[q] = __ldg(vrow + q);
+  }
+}
+
+// Cosine of this row and head (0 for rows without a score slot).
+__device__ __forceinline__ float epi_deviation(uint32_t taddr, const DevPre& p) {
   float dot = 0.f, na = 0.f, nb = 0.f;
-  const __nv_bfloat16* vrow = a.Vf + ((int64_t)(valid ? m : 0) * a.n_kv_heads + head) * BN;
 #pragma unroll
   for (int c0 = 0; c0 < BN; c0 += 32) {
     uint32_t r[32];
     tc::tmem_ld_32x32b_x32(taddr + c0, r);
     tc::tmem_ld_wait();
-    if (slot >= 0) {
+    if (p.slot >= 0) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const uint4 w = __ldg(reinterpret_cast<const uint4*>(vrow + c0 + 8 * q));
+        const uint4 w = p.v[c0 / 8 + q];
         const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -132,17 +150,18 @@ __device__ __forceinline__ void epi_deviation(const TcArgs& a, uint32_t taddr, i
       }
     }
   }
-  if (slot >= 0) {
-    float* pr = a.partial + (int64_t)slot * a.n_kv_heads;
-    pr[head] = dot / fmaxf(sqrtf(na) * sqrtf(nb), 1e-30f);
-    // the thread that writes the row's last cosine forms the score, summing
-    // the cosines in head order (deterministic), and resets the counter
-    __threadfence();
-    if (atomicAdd(a.row_count + slot, 1u) == (uint32_t)a.n_kv_heads - 1) {
-      __threadfence();
-      a.score[slot] = head_mean_score<true>(pr, a.n_kv_heads);
-      a.row_count[slot] = 0u;
-    }
+  return p.slot >= 0 ? dot / fmaxf(sqrtf(na) * sqrtf(nb), 1e-30f) : 0.f;
+}
+
+__device__ __forceinline__ void store_bf16x16(__nv_bfloat16* dst, const float (&x)[16]) {
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    uint4 w;
+    w.x = pack_bf16x2(x[8 * q + 0], x[8 * q + 1]);
+    w.y = pack_bf16x2(x[8 * q + 2], x[8 * q + 3]);
+    w.z = pack_bf16x2(x[8 * q + 4], x[8 * q + 5]);
+    w.w = pack_bf16x2(x[8 * q + 6], x[8 * q + 7]);
+    reinterpret_cast<uint4*>(dst)[q] = w;
   }
 }
 
@@ -158,54 +177,83 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&
   }
 }
 
-__device__ __forceinline__ void epi_recompute(const TcArgs& a, uint32_t taddr, int m, int head) {
-  const bool valid = m < a.M;
+// Operands of the recompute epilogue of one row and head loaded before the
+// accumulator is ready: the destination row and the first RoPE factors.
+constexpr int kRopeChunk = 16;                     // rotation pairs per step
+struct RecPre {
+  __nv_bfloat16* dst;    // null for rows past the end
+  bool rot;
+  float4 cs[kRopeChunk / 2];                       // (cos, sin) of pairs 0 .. 15
+};
+
+__device__ __forceinline__ void pre_recompute(const TcArgs& a, int m, int head, RecPre& p) {
   const int Hq = a.n_q_heads, Hkv = a.n_kv_heads;
-  __nv_bfloat16* dst = nullptr;
-  bool rot = true;
-  if (valid) {
+  p.dst = nullptr;
+  p.rot = head < Hq + Hkv;
+  if (m >= a.M) return;
+  if (head < Hq) {
+    p.dst = a.Q + ((int64_t)m * Hq + head) * BN;
+  } else {
     const WorkRow w = a.rows[m];
-    if (head < Hq) {
-      dst = a.Q + ((int64_t)m * Hq + head) * BN;
-    } else if (head < Hq + Hkv) {
-      dst = a.Kf + (w.dst_row * Hkv + (head - Hq)) * BN;
-    } else {
-      dst = a.Vout + (w.dst_row * Hkv + (head - Hq - Hkv)) * BN;
-      rot = false;
-    }
+    p.dst = head < Hq + Hkv ? a.Kf + (w.dst_row * Hkv + (head - Hq)) * BN
+                            : a.Vout + (w.dst_row * Hkv + (head - Hq - Hkv)) * BN;
   }
+  if (p.rot) {
+    const float4* cs = reinterpret_cast<const float4*>(a.rope + (int64_t)m * (BN / 2));
 #pragma unroll
-  for (int j0 = 0; j0 < BN / 2; j0 += 32) {
-    uint32_t rx[32], ry[32];
-    tc::tmem_ld_32x32b_x32(taddr + j0, rx);
-    tc::tmem_ld_32x32b_x32(taddr + j0 + BN / 2, ry);
-    tc::tmem_ld_wait();
-    if (!valid) continue;
-    float x[32], y[32];
-    if (rot) {
-      const float4* cs = reinterpret_cast<const float4*>(a.rope + (int64_t)m * (BN / 2) + j0);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float4 c = __ldg(cs + i);        // (cos, sin) of pairs j0+2i, j0+2i+1
-        const float x0 = __uint_as_float(rx[2 * i]), y0 = __uint_as_float(ry[2 * i]);
-        const float x1 = __uint_as_float(rx[2 * i + 1]), y1 = __uint_as_float(ry[2 * i + 1]);
-        x[2 * i] = fmaf(x0, c.x, -y0 * c.y);
-        y[2 * i] = fmaf(y0, c.x, x0 * c.y);
-        x[2 * i + 1] = fmaf(x1, c.z, -y1 * c.w);
-        y[2 * i + 1] = fmaf(y1, c.z, x1 * c.w);
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        x[i] = __uint_as_float(rx[i]);
-        y[i] = __uint_as_float(ry[i]);
-      }
-    }
-    store_bf16x32(dst + j0, x);
-    store_bf16x32(dst + j0 + BN / 2, y);
+    for (int i = 0; i < kRopeChunk / 2; ++i) p.cs[i] = __ldg(cs + i);
   }
 }
 
+__device__ __forceinline__ void epi_recompute(const TcArgs& a, uint32_t taddr, int m,
+                                              const RecPre& p) {
+  const float4* csrow = reinterpret_cast<const float4*>(a.rope + (int64_t)m * (BN / 2));
+  float4 cs[kRopeChunk / 2];
+#pragma unroll
+  for (int i = 0; i < kRopeChunk / 2; ++i) cs[i] = p.cs[i];
+#pragma unroll
+  for (int j0 = 0; j0 < BN / 2; j0 += kRopeChunk) {
+    // the next chunk's factors are on their way while this one is rotated
+    float4 nx[kRopeChunk / 2];
+    if (p.rot && p.dst && j0 + kRopeChunk < BN / 2) {
+#pragma unroll
+      for (int i = 0; i < kRopeChunk / 2; ++i) nx[i] = __ldg(csrow + (j0 + kRopeChunk) / 2 + i);
+    }
+    uint32_t rx[kRopeChunk], ry[kRopeChunk];
+    tc::tmem_ld_32x32b_x16(taddr + j0, rx);
+    tc::tmem_ld_32x32b_x16(taddr + j0 + BN / 2, ry);
+    tc::tmem_ld_wait();
+    if (p.dst) {
+      float x[kRopeChunk], y[kRopeChunk];
+      if (p.rot) {
+#pragma unroll
+        for (int i = 0; i < kRopeChunk / 2; ++i) {
+          const float4 c = cs[i];                    // (cos, sin) of pairs j0+2i, j0+2i+1
+          const float x0 = __uint_as_float(rx[2 * i]), y0 = __uint_as_float(ry[2 * i]);
+          const float x1 = __uint_as_float(rx[2 * i + 1]), y1 = __uint_as_float(ry[2 * i + 1]);
+          x[2 * i] = fmaf(x0, c.x, -y0 * c.y);
+          y[2 * i] = fmaf(y0, c.x, x0 * c.y);
+          x[2 * i + 1] = fmaf(x1, c.z, -y1 * c.w);
+          y[2 * i + 1] = fmaf(y1, c.z, x1 * c.w);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < kRopeChunk; ++i) {
+          x[i] = __uint_as_float(rx[i]);
+          y[i] = __uint_as_float(ry[i]);
+        }
+      }
+      store_bf16x16(p.dst + j0, x);
+      store_bf16x16(p.dst + j0 + BN / 2, y);
+    }
+    if (j0 + kRopeChunk < BN / 2) {
+#pragma unroll
+      for (int i = 0; i < kRopeChunk / 2; ++i) cs[i] = nx[i];
+    }
+  }
+}
+
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB0,
                    const __grid_constant__ CUtensorMap mapB1, const __grid_constant__ CUtensorMap mapB2,
@@ -227,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&ctl->tfull[b], 1);
       tc::mbar_init(&ctl->tempty[b], kEpiThreads);
+      tc::mbar_init(&ctl->xc_bar[b], kEpiThreads / 2);
     }
     ctl->abort_flag = 0;
     tc::fence_barrier_init();
@@ -343,6 +392,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const int mt = tile % a.m_tiles;
       const int nt = tile / a.m_tiles;
+      const int m = mt * BM + row;
+      const int head = 2 * nt + hb;
+      // one of the two is used (MODE is a compile-time constant)
+      DevPre dp;
+      RecPre rp;
+      if constexpr (MODE == MODE_DEVIATION)
+        pre_deviation(a, m, head, dp);
+      else
+        pre_recompute(a, m, head, rp);
       if (!tc::mbar_wait_warp(&ctl->tfull[acc], acc_ph, &ctl->abort_flag)) {
         abort_kernel(ctl, a.err);
         break;
@@ -350,11 +408,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tc_fence_after();
       const uint32_t taddr =
           tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * kAccCols + hb * BN;
-      const int m = mt * BM + row;
-      if (a.mode == MODE_DEVIATION)
-        epi_deviation(a, taddr, m, 2 * nt + hb);
-      else
-        epi_recompute(a, taddr, m, 2 * nt + hb);
+      if constexpr (MODE == MODE_DEVIATION) {
+        const float c = epi_deviation(taddr, dp);
+        if (hb == 1) {
+          ctl->xc[acc][row] = c;
+          tc::mbar_arrive(&ctl->xc_bar[acc]);
+        } else {
+          // the pair's sum, first head first; xc[acc] is rewritten only after
+          // this warpgroup has released the accumulator (tempty) below
+          if (!tc::mbar_wait_warp(&ctl->xc_bar[acc], acc_ph, &ctl->abort_flag)) {
+            abort_kernel(ctl, a.err);
+            break;
+          }
+          if (dp.slot >= 0) a.partial[(int64_t)dp.slot * (a.n_kv_heads / 2) + nt] = c + ctl->xc[acc][row];
+        }
+      } else {
+        epi_recompute(a, taddr, m, rp);
+      }
       tc::tc_fence_before();
       tc::mbar_arrive(&ctl->tempty[acc]);
       acc ^= 1;
@@ -408,11 +478,11 @@ cudaError_t launch(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtensor
                    const CUtensorMap& mB2, const TcArgs& a, cudaStream_t s) {
   const int total = a.m_tiles * a.n_tiles;
   if (total == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kSmemBytes);
+  auto kernel = a.mode == MODE_DEVIATION ? gemm_tc_kernel<MODE_DEVIATION> : gemm_tc_kernel<MODE_RECOMPUTE>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = total < sm_count() ? total : sm_count();
-  return launch_pdl(gemm_tc_kernel, dim3(grid), dim3(kThreads), kSmemBytes, s, mA, mB0, mB1, mB2, a);
+  return launch_pdl(kernel, dim3(grid), dim3(kThreads), kSmemBytes, s, mA, mB0, mB1, mB2, a);
 }
 
 }  // namespace
@@ -444,7 +514,7 @@ bool tc_gemm_supported(const fuse_layer_desc_t& d) {
 cudaError_t launch_deviation_partials_tc(const fuse_layer_desc_t& d, int64_t n_rows, const void* H,
                                          const void* Wv, const void* Vf, const int32_t* map,
                                          const fuse_request_t* d_req, int n_req, float* partial,
-                                         float* score, uint32_t* row_count, uint32_t* err,
+                                         uint32_t* err,
                                          cudaStream_t s) {
   if (n_rows == 0) return cudaSuccess;
   CUtensorMap mA, mB;
@@ -466,8 +536,6 @@ cudaError_t launch_deviation_partials_tc(const fuse_layer_desc_t& d, int64_t n_r
   a.reqs = d_req;
   a.n_req = n_req;
   a.partial = partial;
-  a.score = score;
-  a.row_count = row_count;
   a.err = err;
   return launch(mA, mB, mB, mB, a, s);
 }

@@ -45,9 +45,9 @@ cudaError_t launch_deviation_partials_simt(const fuse_layer_desc_t& desc, int64_
                                       const void* Wv, const void* Vf, const int32_t* map,
                                       float* partial, uint32_t* err, cudaStream_t s);
 
-// score[i] = 1 - mean_h partial[i, h].
-cudaError_t launch_deviation_reduce(int64_t n_ctx, int n_kv_heads, const float* partial,
-                                    float* score, cudaStream_t s);
+// score[i] = 1 - (sum_p partial[i, p]) / n_kv_heads over n_parts partials.
+cudaError_t launch_deviation_reduce(int64_t n_ctx, int n_parts, int n_kv_heads,
+                                    const float* partial, float* score, cudaStream_t s);
 
 // Work rows, RoPE table, gathered Hs and attention tiles of the recomputed rows
 // (tensor-core path), one launch.
@@ -56,10 +56,11 @@ cudaError_t launch_prepare_rows(const fuse_requests_t& reqs, int max_rows, const
                                 WorkRow* rows, float2* rope, void* Hs, int rtile, void* tiles,
                                 uint32_t* err, cudaStream_t s);
 
-// score = 1 - mean_h partial, written to score[], then top-k per request.
+// score = 1 - (sum_p partial[p]) / n_kv_heads, written to score[], then
+// top-k per request.
 cudaError_t launch_reduce_topk(const fuse_requests_t& reqs, int max_ctx, const float* partial,
-                               int n_kv_heads, float* score, int32_t* idx, uint32_t* keys_ws,
-                               uint32_t* err, cudaStream_t s);
+                               int n_parts, int n_kv_heads, float* score, int32_t* idx,
+                               uint32_t* keys_ws, uint32_t* err, cudaStream_t s);
 
 // Top-k per request, ascending indices.
 cudaError_t launch_topk(const fuse_requests_t& reqs, int max_ctx, const float* score, int32_t* idx,

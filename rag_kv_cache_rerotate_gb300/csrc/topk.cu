@@ -54,15 +54,15 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* w
   return before;
 }
 
-// With partial != null the scores are first formed from the per-head cosine
-// partials, score = 1 - (sum_h partial[h]) / Hkv summed in head order (the
-// same expression as deviation_reduce_kernel), and written to score[].
+// With partial != null the scores are first formed from the cosine partials
+// (n_parts per token), score = 1 - (sum_p partial[p]) / Hkv summed in order
+// (the same expression as deviation_reduce_kernel), and written to score[].
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const fuse_request_t* reqs,
                                                             const float* score, int32_t* idx,
                                                             uint32_t* keys_ws, uint32_t* err,
                                                             int keys_in_smem,
                                                             const float* partial = nullptr,
-                                                            int n_kv_heads = 0,
+                                                            int n_parts = 0, int n_kv_heads = 0,
                                                             float* score_out = nullptr) {
   extern __shared__ uint32_t dyn[];
   __shared__ uint32_t hist[256];
@@ -79,7 +79,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const fuse_request_t
   if (k <= 0) {                      // nothing to select; still form the scores
     if (partial) {
       for (int i = t; i < n; i += kTopkThreads)
-        score_out[R.score0 + i] = head_mean_score(partial + (R.score0 + i) * n_kv_heads, n_kv_heads);
+        score_out[R.score0 + i] =
+            head_mean_score(partial + (R.score0 + i) * n_parts, n_parts, n_kv_heads);
     }
     return;
   }
@@ -91,7 +92,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const fuse_request_t
     bool nn;
     float v;
     if (partial) {
-      v = head_mean_score(partial + (R.score0 + i) * n_kv_heads, n_kv_heads);
+      v = head_mean_score(partial + (R.score0 + i) * n_parts, n_parts, n_kv_heads);
       score_out[R.score0 + i] = v;
     } else {
       v = score[R.score0 + i];
@@ -214,8 +215,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const fuse_request_t
 }  // namespace
 
 cudaError_t launch_reduce_topk(const fuse_requests_t& reqs, int max_ctx, const float* partial,
-                               int n_kv_heads, float* score, int32_t* idx, uint32_t* keys_ws,
-                               uint32_t* err, cudaStream_t s) {
+                               int n_parts, int n_kv_heads, float* score, int32_t* idx,
+                               uint32_t* keys_ws, uint32_t* err, cudaStream_t s) {
   if (reqs.n_req == 0) return cudaSuccess;
   const int in_smem = max_ctx <= kTopkSmemKeys;
   const size_t smem = in_smem ? (size_t)max_ctx * sizeof(uint32_t) : 0;
@@ -225,7 +226,8 @@ cudaError_t launch_reduce_topk(const fuse_requests_t& reqs, int max_ctx, const f
     if (e != cudaSuccess) return e;
   }
   return launch_pdl(topk_kernel, dim3(reqs.n_req), dim3(kTopkThreads), smem, s, reqs.d_req,
-                    (const float*)nullptr, idx, keys_ws, err, in_smem, partial, n_kv_heads, score);
+                    (const float*)nullptr, idx, keys_ws, err, in_smem, partial, n_parts,
+                    n_kv_heads, score);
 }
 
 cudaError_t launch_topk(const fuse_requests_t& reqs, int max_ctx, const float* score, int32_t* idx,
@@ -239,7 +241,7 @@ cudaError_t launch_topk(const fuse_requests_t& reqs, int max_ctx, const float* s
     if (e != cudaSuccess) return e;
   }
   return launch_pdl(topk_kernel, dim3(reqs.n_req), dim3(kTopkThreads), smem, s, reqs.d_req, score,
-                    idx, keys_ws, err, in_smem, (const float*)nullptr, 0, (float*)nullptr);
+                    idx, keys_ws, err, in_smem, (const float*)nullptr, 0, 0, (float*)nullptr);
 }
 
 }  // namespace fusekv
