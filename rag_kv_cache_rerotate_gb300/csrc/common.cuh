@@ -68,6 +68,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <typename T> struct Vec8;
 
 template <> struct Vec8<float> {
+  static __device__ __forceinline__ void load_shared(const float* p, float (&x)[8]) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0];
+    const float4 b = reinterpret_cast<const float4*>(p)[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  }
   static __device__ __forceinline__ void load(const float* p, float (&x)[8]) {
     float4 a = __ldg(reinterpret_cast<const float4*>(p));
     float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
@@ -81,6 +87,11 @@ template <> struct Vec8<float> {
 };
 
 template <> struct Vec8<__nv_bfloat16> {
+  static __device__ __forceinline__ void load_shared(const __nv_bfloat16* p, float (&x)[8]) {
+    const uint4 a = *reinterpret_cast<const uint4*>(p);
+    x[0] = bf16_lo(a.x); x[1] = bf16_hi(a.x); x[2] = bf16_lo(a.y); x[3] = bf16_hi(a.y);
+    x[4] = bf16_lo(a.z); x[5] = bf16_hi(a.z); x[6] = bf16_lo(a.w); x[7] = bf16_hi(a.w);
+  }
   static __device__ __forceinline__ void load(const __nv_bfloat16* p, float (&x)[8]) {
     uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
     x[0] = bf16_lo(a.x); x[1] = bf16_hi(a.x); x[2] = bf16_lo(a.y); x[3] = bf16_hi(a.y);

@@ -7,15 +7,21 @@
 // R^{o_i}.  KVBoost (section 4.5, Eq. 7): x = zero + q * scale, keys with
 // per-channel statistics, values with per-token statistics.
 //
-// Memory-bound.  One CTA moves a few rows of one chunk; each thread owns one
+// Memory-bound.  When the chunk caches have the layer's element type (no
+// dequantisation), stitch_bulk_kernel streams them: persistent CTAs (two per
+// SM), each working through a contiguous range of row tiles with a 3-stage
+// shared-memory ring filled by 1-D bulk copies; the threads rotate the key
+// tile in place and bulk stores write both tiles to the fused cache (values
+// pass through untouched).  Otherwise (int8 codes, or a type change)
+// stitch_kernel: one CTA moves a few rows of one chunk; each thread owns one
 // group of 8 key pairs and two groups of 8 values and issues all its 16-byte
-// loads before anything else, so every thread keeps four loads in flight at
-// low register use.  The chunk offset's (cos, sin) of the d/2 frequencies are
-// computed once per CTA into shared memory while those loads are in flight.
+// loads before anything else.  Either way the chunk offset's (cos, sin) of the
+// d/2 frequencies are computed once per CTA (and chunk) into shared memory.
 #include <algorithm>
 
 #include "common.cuh"
 #include "launch.h"
+#include "tc_ptx.cuh"
 
 namespace fusekv {
 
@@ -234,6 +240,170 @@ __global__ void __launch_bounds__(kStitchThreads) stitch_kernel(const StitchArgs
   }
 }
 
+// ---- streamed path (chunk storage type == layer type) ------------------------
+constexpr int kBulkThreads = 256;
+constexpr int kBulkStages = 3;
+constexpr int kBulkTileBytes = 16384;              // K tile or V tile, at most
+constexpr int kBulkSmem = kBulkStages * 2 * kBulkTileBytes;
+
+struct BulkArgs {
+  const fuse_chunk_t* chunks;
+  void* Kf;
+  void* Vf;
+  uint32_t* err;
+  int64_t n_pool_blocks;
+  int32_t n_kv_heads;
+  int32_t block_size;
+  int32_t rt;                 // rows per tile; divides block_size when paged
+  int32_t tiles_per_chunk;
+  int32_t total_tiles;
+  RopeFreqs freqs;
+};
+
+struct BulkTile {
+  int chunk, r0, nrows;       // nrows 0: nothing to do
+  int64_t src_row;            // first source row (pool row when paged)
+};
+
+template <bool PAGED>
+__device__ __forceinline__ BulkTile bulk_tile(const BulkArgs& a, int tile, const fuse_chunk_t& c) {
+  BulkTile x;
+  x.chunk = tile / a.tiles_per_chunk;
+  x.r0 = (tile % a.tiles_per_chunk) * a.rt;
+  x.nrows = max(0, min(a.rt, c.len - x.r0));
+  x.src_row = x.r0;
+  if (PAGED && x.nrows > 0) {
+    const int32_t b = __ldg(c.block_table + x.r0 / a.block_size);
+    if (b < 0 || b >= a.n_pool_blocks) {
+      x.nrows = 0;            // reported by the caller
+      x.src_row = -1;
+    } else {
+      x.src_row = (int64_t)b * a.block_size + x.r0 % a.block_size;
+    }
+  }
+  return x;
+}
+
+template <typename T, int D, bool PAGED>
+__global__ void __launch_bounds__(kBulkThreads) stitch_bulk_kernel(const BulkArgs a) {
+  constexpr int H2 = D / 2;
+  constexpr int PG = H2 / 8;                         // 8-pair groups per head
+  extern __shared__ __align__(128) uint8_t ring[];   // stage s: K tile, then V tile
+  __shared__ __align__(8) uint64_t full[kBulkStages];
+  __shared__ float s_cs[kMaxHalfDim], s_sn[kMaxHalfDim];
+  __shared__ int s_abort;
+  const int t = threadIdx.x;
+  const int Hkv = a.n_kv_heads;
+  const int64_t row_elems = (int64_t)Hkv * D;
+  const uint32_t row_bytes = (uint32_t)(row_elems * sizeof(T));
+  const int per = (a.total_tiles + gridDim.x - 1) / gridDim.x;
+  const int t0 = blockIdx.x * per;
+  const int t1 = min(a.total_tiles, t0 + per);
+  pdl_trigger();
+  if (t == 0) {
+    for (int s = 0; s < kBulkStages; ++s) tc::mbar_init(&full[s], 1);
+    s_abort = 0;
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+  pdl_wait();
+  // thread 0 fills stage (i % 3) with tile t0 + i; a stage's barrier completes
+  // one phase per non-empty tile, so both sides count phases per stage
+  uint32_t issued[kBulkStages] = {0, 0, 0}, used[kBulkStages] = {0, 0, 0};
+  auto fill = [&](int i) {
+    const int tile = t0 + i;
+    const fuse_chunk_t c = a.chunks[tile / a.tiles_per_chunk];
+    const BulkTile x = bulk_tile<PAGED>(a, tile, c);
+    if (x.src_row < 0) report_error(a.err, FUSE_ERR_DEVICE_BOUNDS, SITE_STITCH_BLOCK, x.chunk);
+    if (x.nrows == 0) return;
+    const int s = i % kBulkStages;
+    const uint32_t bytes = (uint32_t)x.nrows * row_bytes;
+    uint8_t* st = ring + s * 2 * kBulkTileBytes;
+    ++issued[s];
+    tc::mbar_arrive_expect_tx(&full[s], 2 * bytes);
+    tc::bulk_g2s(st, reinterpret_cast<const T*>(c.k) + x.src_row * row_elems, bytes, &full[s]);
+    tc::bulk_g2s(st + kBulkTileBytes, reinterpret_cast<const T*>(c.v) + x.src_row * row_elems, bytes,
+                 &full[s]);
+  };
+  if (t == 0)
+    for (int i = 0; i < kBulkStages && t0 + i < t1; ++i) fill(i);
+  int table_chunk = -1;
+  for (int i = 0; t0 + i < t1; ++i) {
+    const int tile = t0 + i;
+    const fuse_chunk_t c = a.chunks[tile / a.tiles_per_chunk];
+    const BulkTile x = bulk_tile<PAGED>(a, tile, c);
+    const int s = i % kBulkStages;
+    uint8_t* st = ring + s * 2 * kBulkTileBytes;
+    if (x.nrows > 0) {
+      if (!tc::mbar_wait(&full[s], used[s] & 1, &s_abort)) {
+        if (atomicExch(&s_abort, 1) == 0)
+          report_error(a.err, FUSE_ERR_TIMEOUT, SITE_STITCH_TIMEOUT, blockIdx.x);
+      }
+      ++used[s];
+      __syncthreads();
+      if (s_abort) break;                               // block-uniform after the barrier
+      if (c.pos != 0) {
+        if (x.chunk != table_chunk) {                  // block-uniform
+          if (t < H2) rope_cos_sin(c.pos, a.freqs.hi[t], a.freqs.mid[t], a.freqs.lo[t], s_cs[t], s_sn[t]);
+          __syncthreads();
+          table_chunk = x.chunk;
+        }
+        T* k = reinterpret_cast<T*>(st);
+        const int items = x.nrows * Hkv * PG;
+        for (int it = t; it < items; it += kBulkThreads) {
+          const int g = it % PG;
+          T* p = k + (int64_t)(it / PG) * D + g * 8;   // (row, head) base + pair group
+          float xv[8], yv[8];
+          Vec8<T>::load_shared(p, xv);
+          Vec8<T>::load_shared(p + H2, yv);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float cs = s_cs[g * 8 + q], sn = s_sn[g * 8 + q];
+            const float xr = fmaf(xv[q], cs, -yv[q] * sn);
+            const float yr = fmaf(yv[q], cs, xv[q] * sn);
+            xv[q] = xr;
+            yv[q] = yr;
+          }
+          Vec8<T>::store(p, xv);
+          Vec8<T>::store(p + H2, yv);
+        }
+        tc::fence_proxy_async_smem();
+      }
+      __syncthreads();                                  // the tile is final in shared memory
+      if (t == 0) {
+        const uint32_t bytes = (uint32_t)x.nrows * row_bytes;
+        const int64_t dst = (c.dst_row + x.r0) * row_elems;
+        tc::bulk_s2g(reinterpret_cast<T*>(a.Kf) + dst, st, bytes);
+        tc::bulk_s2g(reinterpret_cast<T*>(a.Vf) + dst, st + kBulkTileBytes, bytes);
+        tc::bulk_commit();
+      }
+    }
+    if (t == 0 && t0 + i + kBulkStages < t1) {
+      tc::bulk_wait_read_all();                         // stage s is read out
+      fill(i + kBulkStages);
+    }
+  }
+  if (t == 0) {
+    tc::bulk_wait_all();
+    // after an abort, let loads still in flight land before the CTA exits
+    for (int s = 0; s < kBulkStages; ++s)
+      if (issued[s] > 0) tc::mbar_wait(&full[s], (issued[s] - 1) & 1);
+  }
+}
+
+template <typename T, int D, bool PAGED>
+cudaError_t launch_bulk_t(const BulkArgs& a, cudaStream_t s) {
+  if (a.total_tiles == 0) return cudaSuccess;
+  auto k = stitch_bulk_kernel<T, D, PAGED>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kBulkSmem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int grid = std::min(a.total_tiles, 2 * std::max(sms, 1));
+  return launch_pdl(k, dim3(grid), dim3(kBulkThreads), kBulkSmem, s, a);
+}
+
 template <typename TS, typename TO, int D, bool PAGED>
 cudaError_t launch_t(const StitchArgs& a, int n_chunks, cudaStream_t s) {
   const int grid = n_chunks * a.tiles_per_chunk;
@@ -255,6 +425,36 @@ cudaError_t launch_d(const StitchArgs& a, int n_chunks, int D, bool paged, cudaS
 cudaError_t launch_stitch(const fuse_layer_desc_t& desc, const fuse_chunks_t& chunks,
                           const RopeFreqs& freqs, int max_len, void* Kf, void* Vf, uint32_t* err,
                           cudaStream_t s) {
+  const bool paged = chunks.kv_layout == FUSE_KV_PAGED;
+  const int D = desc.head_dim;
+  const bool same = chunks.kv_storage == desc.dtype;   // F32 / BF16 codes are the dtypes
+  const int64_t row_bytes = (int64_t)desc.n_kv_heads * D * (desc.dtype == FUSE_F32 ? 4 : 2);
+  if (same && row_bytes <= kBulkTileBytes) {
+    BulkArgs b;
+    b.chunks = chunks.d_chunks;
+    b.Kf = Kf;
+    b.Vf = Vf;
+    b.err = err;
+    b.n_pool_blocks = chunks.n_pool_blocks;
+    b.n_kv_heads = desc.n_kv_heads;
+    b.block_size = chunks.block_size > 0 ? chunks.block_size : 1;
+    int rt = (int)(kBulkTileBytes / row_bytes);
+    if (paged)
+      while (b.block_size % rt != 0) --rt;     // a tile never leaves its page
+    b.rt = rt;
+    b.tiles_per_chunk = (max_len + rt - 1) / rt;
+    b.total_tiles = chunks.n_chunks * b.tiles_per_chunk;
+    b.freqs = freqs;
+    if (desc.dtype == FUSE_BF16)
+      return D == 128 ? (paged ? launch_bulk_t<__nv_bfloat16, 128, true>(b, s)
+                               : launch_bulk_t<__nv_bfloat16, 128, false>(b, s))
+                      : (paged ? launch_bulk_t<__nv_bfloat16, 64, true>(b, s)
+                               : launch_bulk_t<__nv_bfloat16, 64, false>(b, s));
+    return D == 128 ? (paged ? launch_bulk_t<float, 128, true>(b, s)
+                             : launch_bulk_t<float, 128, false>(b, s))
+                    : (paged ? launch_bulk_t<float, 64, true>(b, s)
+                             : launch_bulk_t<float, 64, false>(b, s));
+  }
   StitchArgs a;
   a.chunks = chunks.d_chunks;
   a.Kf = Kf;
@@ -268,8 +468,6 @@ cudaError_t launch_stitch(const fuse_layer_desc_t& desc, const fuse_chunks_t& ch
   a.rows_per_cta = std::max(1, (kStitchThreads * kStitchItems) / (desc.n_kv_heads * (desc.head_dim / 8)));
   a.tiles_per_chunk = (max_len + a.rows_per_cta - 1) / a.rows_per_cta;
   a.freqs = freqs;
-  const bool paged = chunks.kv_layout == FUSE_KV_PAGED;
-  const int D = desc.head_dim;
   const bool out_bf16 = desc.dtype == FUSE_BF16;
   switch (chunks.kv_storage) {
     case FUSE_F32:
