@@ -660,7 +660,7 @@ cudaError_t launch_attention_tc(const fuse_layer_desc_t& d, const fuse_requests_
   a.rtile = rtile;
   a.scale_log2 = 1.4426950408889634f / sqrtf((float)kD);
   a.err = err;
-  e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  e = set_dyn_smem_once(reinterpret_cast<const void*>(attn_tc_kernel), kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = a.n_units < sm_count() ? a.n_units : sm_count();
   return launch_pdl(attn_tc_kernel, dim3(grid), dim3(kThreads), kSmemBytes, s, mQ, mK, mV, a);

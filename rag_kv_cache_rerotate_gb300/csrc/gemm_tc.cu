@@ -479,7 +479,7 @@ cudaError_t launch(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtensor
   const int total = a.m_tiles * a.n_tiles;
   if (total == 0) return cudaSuccess;
   auto kernel = a.mode == MODE_DEVIATION ? gemm_tc_kernel<MODE_DEVIATION> : gemm_tc_kernel<MODE_RECOMPUTE>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e = set_dyn_smem_once(reinterpret_cast<const void*>(kernel), kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = total < sm_count() ? total : sm_count();
   return launch_pdl(kernel, dim3(grid), dim3(kThreads), kSmemBytes, s, mA, mB0, mB1, mB2, a);

@@ -3,11 +3,30 @@
 
 #include <cuda_runtime.h>
 
+#include <mutex>
+#include <set>
+#include <tuple>
 #include <utility>
 
 #include "common.cuh"
 
 namespace fusekv {
+
+// Raise a kernel's dynamic shared-memory limit to `bytes`, once per device
+// (the call costs host time on every launch otherwise).
+inline cudaError_t set_dyn_smem_once(const void* kernel, int bytes) {
+  static std::mutex mu;
+  static std::set<std::tuple<int, const void*, int>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const auto key = std::make_tuple(dev, kernel, bytes);
+  std::lock_guard<std::mutex> g(mu);
+  if (done.count(key)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert(key);
+  return e;
+}
 
 // Launch with programmatic stream serialisation (see pdl_trigger/pdl_wait).
 template <typename... KArgs, typename... Args>

@@ -395,7 +395,7 @@ template <typename T, int D, bool PAGED>
 cudaError_t launch_bulk_t(const BulkArgs& a, cudaStream_t s) {
   if (a.total_tiles == 0) return cudaSuccess;
   auto k = stitch_bulk_kernel<T, D, PAGED>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kBulkSmem);
+  cudaError_t e = set_dyn_smem_once(reinterpret_cast<const void*>(k), kBulkSmem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
