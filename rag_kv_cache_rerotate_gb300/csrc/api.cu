@@ -1,6 +1,7 @@
 // The exported C ABI of libfusekv: argument validation, workspace carving,
 // and the order of launches of one layer-step (QCFuse section 2.1, Eqs.
 // 4-7; KVBoost Alg. 2: stitch, probe/deviation, select, patch).
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <vector>
@@ -16,8 +17,10 @@ bool tc_gemm_supported(const fuse_layer_desc_t& desc);
 cudaError_t launch_deviation_partials_tc(const fuse_layer_desc_t& desc, int64_t n_rows,
                                          const void* H, const void* Wv, const void* Vf,
                                          const int32_t* map, const fuse_request_t* d_req,
-                                         int n_req, float* partial, uint32_t* err,
+                                         int n_req, float* partial,
+                                         const fuse_chunks_t* v_chunks, uint32_t* err,
                                          cudaStream_t s);
+int deviation_tc_ctas(const fuse_layer_desc_t& d, int64_t n_rows);
 cudaError_t launch_project_recompute_tc(const fuse_layer_desc_t& desc, int64_t n_rows,
                                         const WorkRow* rows, const float2* rope, const void* H,
                                         const void* Wq, const void* Wk, const void* Wv, void* Q,
@@ -190,17 +193,24 @@ fuse_status_t check_ws(void* ws, size_t ws_bytes, size_t need) {
 // ---- the steps (validated arguments) ------------------------------------
 
 fuse_status_t do_stitch(const fuse_layer_desc_t& d, const fuse_chunks_t& c, int max_len, void* Kf,
-                        void* Vf, void* ws, cudaStream_t s) {
+                        void* Vf, void* ws, cudaStream_t s, int free_sms = -1) {
   if (c.n_chunks == 0 || max_len == 0) return FUSE_OK;
   const RopeFreqs f = make_freqs(d);
   return cuda_status(traced("stitch_rerotate", s, [&] {
-    return launch_stitch(d, c, f, max_len, Kf, Vf, at<uint32_t>(ws, 0), s);
+    return launch_stitch(d, c, f, max_len, Kf, Vf, at<uint32_t>(ws, 0), s, free_sms);
   }));
+}
+
+// Chunks placed in ascending, non-overlapping fused rows (host table).
+bool chunks_sorted(const fuse_chunks_t& c) {
+  for (int i = 1; i < c.n_chunks; ++i)
+    if (c.h_chunks[i].dst_row < c.h_chunks[i - 1].dst_row + c.h_chunks[i - 1].len) return false;
+  return true;
 }
 
 fuse_status_t do_score(const fuse_layer_desc_t& d, const fuse_requests_t& r, const ReqInfo& info,
                        const void* H, const void* Wv, const void* Vf, float* score, void* ws,
-                       cudaStream_t s, bool reduce = true) {
+                       cudaStream_t s, bool reduce = true, const fuse_chunks_t* v_chunks = nullptr) {
   const WsLayout L = ws_layout(d, info.tot, info.n_req);
   if (info.tot.n_ctx == 0) return FUSE_OK;
   int32_t* map = at<int32_t>(ws, L.map);
@@ -217,7 +227,8 @@ fuse_status_t do_score(const fuse_layer_desc_t& d, const fuse_requests_t& r, con
     if (tc)
       e = traced("deviation_gemm_tc", s, [&] {
         return launch_deviation_partials_tc(d, info.tot.n_tok, H, Wv, Vf, need_map ? map : nullptr,
-                                            r.d_req, r.n_req, partial, at<uint32_t>(ws, 0), s);
+                                            r.d_req, r.n_req, partial, v_chunks,
+                                            at<uint32_t>(ws, 0), s);
       });
     else
       e = traced("deviation_gemm_simt", s, [&] {
@@ -327,6 +338,32 @@ fuse_status_t do_score_select(const fuse_layer_desc_t& d, const fuse_requests_t&
                               const ReqInfo& info, const void* H, const void* Wv, const void* Vf,
                               float* score, int32_t* idx, void* ws, cudaStream_t s) {
   fuse_status_t st = do_score(d, r, info, H, Wv, Vf, score, ws, s, /*reduce=*/false);
+  if (st != FUSE_OK) return st;
+  return do_reduce_topk(d, r, info, score, idx, ws, s);
+}
+
+// Stitch and score/select of one layer.  On the tensor-core path with
+// same-type chunk caches placed in order, the deviation GEMM reads the cached
+// V rows from the chunks themselves and the stitch runs on the SMs the GEMM
+// leaves free (it waits for the GEMM only at its end); otherwise in sequence.
+fuse_status_t do_stitch_score_select(const fuse_layer_desc_t& d, const fuse_chunks_t& c,
+                                     int max_len, const fuse_requests_t& r, const ReqInfo& info,
+                                     const void* H, const void* Wv, void* Kf, void* Vf,
+                                     float* score, int32_t* idx, void* ws, cudaStream_t s) {
+  const bool together = tc_gemm_supported(d) && info.tot.n_ctx > 0 && c.n_chunks > 0 &&
+                        max_len > 0 && stitch_streamed(d, c) && chunks_sorted(c);
+  if (!together) {
+    fuse_status_t st = do_stitch(d, c, max_len, Kf, Vf, ws, s);
+    if (st != FUSE_OK) return st;
+    return do_score_select(d, r, info, H, Wv, Vf, score, idx, ws, s);
+  }
+  fuse_status_t st = do_score(d, r, info, H, Wv, Vf, score, ws, s, /*reduce=*/false, &c);
+  if (st != FUSE_OK) return st;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int free_sms = std::max(0, sms - deviation_tc_ctas(d, info.tot.n_tok));
+  st = do_stitch(d, c, max_len, Kf, Vf, ws, s, free_sms);
   if (st != FUSE_OK) return st;
   return do_reduce_topk(d, r, info, score, idx, ws, s);
 }
@@ -477,12 +514,11 @@ fuse_status_t fuse_layer_step(const fuse_layer_desc_t* desc, const fuse_chunks_t
   st = check_layer(*desc, info, la, score_this_layer != 0, idx, score, ws, ws_bytes, &max_len);
   if (st != FUSE_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  st = do_stitch(*desc, *chunks, max_len, Kf, Vf, ws, s);
+  if (score_this_layer)
+    st = do_stitch_score_select(*desc, *chunks, max_len, *reqs, info, H, Wv, Kf, Vf, score, idx, ws, s);
+  else
+    st = do_stitch(*desc, *chunks, max_len, Kf, Vf, ws, s);
   if (st != FUSE_OK) return st;
-  if (score_this_layer) {
-    st = do_score_select(*desc, *reqs, info, H, Wv, Vf, score, idx, ws, s);
-    if (st != FUSE_OK) return st;
-  }
   return do_recompute(*desc, *reqs, info, H, Wq, Wk, Wv, idx, Kf, Vf, O, ws, s);
 }
 
@@ -506,9 +542,8 @@ fuse_status_t fuse_stack_step(const fuse_layer_desc_t* desc, const fuse_requests
   }
   cudaStream_t s = (cudaStream_t)stream;
   const fuse_layer_io_t& S = layers[score_layer];
-  st = do_stitch(*desc, *S.chunks, max_len[score_layer], S.Kf, S.Vf, ws, s);
-  if (st != FUSE_OK) return st;
-  st = do_score_select(*desc, *reqs, info, S.H, S.Wv, S.Vf, score, idx, ws, s);
+  st = do_stitch_score_select(*desc, *S.chunks, max_len[score_layer], *reqs, info, S.H, S.Wv, S.Kf,
+                              S.Vf, score, idx, ws, s);
   if (st != FUSE_OK) return st;
   for (int l = 0; l < n_layers; ++l) {
     const fuse_layer_io_t& L = layers[l];

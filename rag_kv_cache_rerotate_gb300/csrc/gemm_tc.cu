@@ -24,6 +24,7 @@
 // they wait for the accumulator, so those loads overlap the main loop.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -60,6 +61,13 @@ struct TcArgs {
   int n_kv_heads;
   // deviation
   const __nv_bfloat16* Vf;
+  // cached V read from the chunk caches (bf16, same type as the layer) instead
+  // of Vf, so that the stitch may run alongside; null: read Vf
+  const fuse_chunk_t* chunks;    // sorted by dst_row, non-overlapping
+  int n_chunks;
+  int kv_paged;
+  int block_size;
+  int64_t n_pool_blocks;
   const int32_t* map;            // score slot of every packed row, or null: search reqs
   const fuse_request_t* reqs;    // sorted by row0, non-overlapping (when map is null)
   int n_req;
@@ -116,12 +124,35 @@ struct DevPre {
   uint4 v[BN / 8];
 };
 
+// Where the cached V row of packed row m lives: in the chunk cache whose
+// fused rows hold m (what the stitch copies to Vf[m]), else in Vf itself (a
+// row no chunk covers keeps its contents).
+__device__ __forceinline__ const __nv_bfloat16* cached_v_row(const TcArgs& a, int m, int head) {
+  const int64_t fused = ((int64_t)m * a.n_kv_heads + head) * BN;
+  if (!a.chunks || a.n_chunks == 0) return a.Vf + fused;
+  int lo = 0, hi = a.n_chunks - 1;
+  while (lo < hi) {                       // last chunk with dst_row <= m
+    const int mid = (lo + hi + 1) >> 1;
+    if (a.chunks[mid].dst_row <= m) lo = mid; else hi = mid - 1;
+  }
+  const fuse_chunk_t& c = a.chunks[lo];
+  const int64_t r = m - c.dst_row;
+  if (r < 0 || r >= c.len) return a.Vf + fused;
+  int64_t tok = r;
+  if (a.kv_paged) {
+    const int32_t b = __ldg(c.block_table + r / a.block_size);
+    if (b < 0 || b >= a.n_pool_blocks) return nullptr;   // reported by the stitch
+    tok = (int64_t)b * a.block_size + r % a.block_size;
+  }
+  return reinterpret_cast<const __nv_bfloat16*>(c.v) + (tok * a.n_kv_heads + head) * BN;
+}
+
 __device__ __forceinline__ void pre_deviation(const TcArgs& a, int m, int head, DevPre& p) {
   p.slot = m < a.M ? row_slot(a, m) : -1;
   if (p.slot >= 0) {
-    const uint4* vrow = reinterpret_cast<const uint4*>(a.Vf + ((int64_t)m * a.n_kv_heads + head) * BN);
+    const uint4* vrow = reinterpret_cast<const uint4*>(cached_v_row(a, m, head));
 #pragma unroll
-    for (int q = 0; q < BN / 8; ++q) p.v[q] = __ldg(vrow + q);
+    for (int q = 0; q < BN / 8; ++q) p.v[q] = vrow ? __ldg(vrow + q) : make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
@@ -265,7 +296,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x % 32;
   const int total = a.m_tiles * a.n_tiles;
   const int k_blocks = a.K / BK;
-  pdl_trigger();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -290,6 +320,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
   pdl_wait();                 // inputs of the previous kernel complete and visible
+  // the next kernel may start once every CTA is here: the kernels before this
+  // one are complete by now (a stitch launched next may write the fused cache)
+  pdl_trigger();
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -514,7 +547,7 @@ bool tc_gemm_supported(const fuse_layer_desc_t& d) {
 cudaError_t launch_deviation_partials_tc(const fuse_layer_desc_t& d, int64_t n_rows, const void* H,
                                          const void* Wv, const void* Vf, const int32_t* map,
                                          const fuse_request_t* d_req, int n_req, float* partial,
-                                         uint32_t* err,
+                                         const fuse_chunks_t* v_chunks, uint32_t* err,
                                          cudaStream_t s) {
   if (n_rows == 0) return cudaSuccess;
   CUtensorMap mA, mB;
@@ -536,8 +569,20 @@ cudaError_t launch_deviation_partials_tc(const fuse_layer_desc_t& d, int64_t n_r
   a.reqs = d_req;
   a.n_req = n_req;
   a.partial = partial;
+  if (v_chunks) {
+    a.chunks = v_chunks->d_chunks;
+    a.n_chunks = v_chunks->n_chunks;
+    a.kv_paged = v_chunks->kv_layout == FUSE_KV_PAGED;
+    a.block_size = v_chunks->block_size > 0 ? v_chunks->block_size : 1;
+    a.n_pool_blocks = v_chunks->n_pool_blocks;
+  }
   a.err = err;
   return launch(mA, mB, mB, mB, a, s);
+}
+
+int deviation_tc_ctas(const fuse_layer_desc_t& d, int64_t n_rows) {
+  const int64_t tiles = ((n_rows + BM - 1) / BM) * (d.n_kv_heads / 2);
+  return (int)std::min<int64_t>(tiles, sm_count());
 }
 
 cudaError_t launch_project_recompute_tc(const fuse_layer_desc_t& d, int64_t n_rows,

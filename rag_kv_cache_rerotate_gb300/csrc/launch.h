@@ -45,10 +45,14 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// Stitch + re-rotate (+ dequantise, + paged gather) every chunk.
+// Stitch + re-rotate (+ dequantise, + paged gather) every chunk.  free_sms
+// < 0: after the previous kernel; otherwise alongside it (the previous kernel
+// reads no output of the stitch and leaves free_sms SMs free), which needs
+// stitch_streamed().
 cudaError_t launch_stitch(const fuse_layer_desc_t& desc, const fuse_chunks_t& chunks,
                           const RopeFreqs& freqs, int max_len, void* Kf, void* Vf, uint32_t* err,
-                          cudaStream_t s);
+                          cudaStream_t s, int free_sms = -1);
+bool stitch_streamed(const fuse_layer_desc_t& desc, const fuse_chunks_t& chunks);
 
 // Score slot of every packed row: score0 + t for context rows, -1 for query rows.
 cudaError_t launch_build_score_map(const fuse_requests_t& reqs, int max_tok, int32_t* map,

@@ -257,6 +257,8 @@ struct BulkArgs {
   int32_t rt;                 // rows per tile; divides block_size when paged
   int32_t tiles_per_chunk;
   int32_t total_tiles;
+  int32_t wait_first;         // 0: the previous kernel (which reads no output of
+                              // this one) is waited for only at the end
   RopeFreqs freqs;
 };
 
@@ -306,7 +308,7 @@ __global__ void __launch_bounds__(kBulkThreads) stitch_bulk_kernel(const BulkArg
     tc::fence_barrier_init();
   }
   __syncthreads();
-  pdl_wait();
+  if (a.wait_first) pdl_wait();
   // thread 0 fills stage (i % 3) with tile t0 + i; a stage's barrier completes
   // one phase per non-empty tile, so both sides count phases per stage
   uint32_t issued[kBulkStages] = {0, 0, 0}, used[kBulkStages] = {0, 0, 0};
@@ -389,10 +391,12 @@ __global__ void __launch_bounds__(kBulkThreads) stitch_bulk_kernel(const BulkArg
     for (int s = 0; s < kBulkStages; ++s)
       if (issued[s] > 0) tc::mbar_wait(&full[s], (issued[s] - 1) & 1);
   }
+  // completing implies the previous kernel completed, for the kernels after
+  if (!a.wait_first) pdl_wait();
 }
 
 template <typename T, int D, bool PAGED>
-cudaError_t launch_bulk_t(const BulkArgs& a, cudaStream_t s) {
+cudaError_t launch_bulk_t(const BulkArgs& a, int free_sms, cudaStream_t s) {
   if (a.total_tiles == 0) return cudaSuccess;
   auto k = stitch_bulk_kernel<T, D, PAGED>;
   cudaError_t e = set_dyn_smem_once(reinterpret_cast<const void*>(k), kBulkSmem);
@@ -400,7 +404,9 @@ cudaError_t launch_bulk_t(const BulkArgs& a, cudaStream_t s) {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int grid = std::min(a.total_tiles, 2 * std::max(sms, 1));
+  // alongside a kernel that holds the other SMs, two CTAs on each free SM
+  const int ctas = free_sms >= 8 ? 2 * free_sms : 2 * std::max(sms, 1);
+  const int grid = std::min(a.total_tiles, ctas);
   return launch_pdl(k, dim3(grid), dim3(kBulkThreads), kBulkSmem, s, a);
 }
 
@@ -422,9 +428,15 @@ cudaError_t launch_d(const StitchArgs& a, int n_chunks, int D, bool paged, cudaS
 
 }  // namespace
 
+bool stitch_streamed(const fuse_layer_desc_t& desc, const fuse_chunks_t& chunks) {
+  const int64_t row_bytes =
+      (int64_t)desc.n_kv_heads * desc.head_dim * (desc.dtype == FUSE_F32 ? 4 : 2);
+  return chunks.kv_storage == desc.dtype && row_bytes <= kBulkTileBytes;
+}
+
 cudaError_t launch_stitch(const fuse_layer_desc_t& desc, const fuse_chunks_t& chunks,
                           const RopeFreqs& freqs, int max_len, void* Kf, void* Vf, uint32_t* err,
-                          cudaStream_t s) {
+                          cudaStream_t s, int free_sms) {
   const bool paged = chunks.kv_layout == FUSE_KV_PAGED;
   const int D = desc.head_dim;
   const bool same = chunks.kv_storage == desc.dtype;   // F32 / BF16 codes are the dtypes
@@ -444,16 +456,17 @@ cudaError_t launch_stitch(const fuse_layer_desc_t& desc, const fuse_chunks_t& ch
     b.rt = rt;
     b.tiles_per_chunk = (max_len + rt - 1) / rt;
     b.total_tiles = chunks.n_chunks * b.tiles_per_chunk;
+    b.wait_first = free_sms < 0;
     b.freqs = freqs;
     if (desc.dtype == FUSE_BF16)
-      return D == 128 ? (paged ? launch_bulk_t<__nv_bfloat16, 128, true>(b, s)
-                               : launch_bulk_t<__nv_bfloat16, 128, false>(b, s))
-                      : (paged ? launch_bulk_t<__nv_bfloat16, 64, true>(b, s)
-                               : launch_bulk_t<__nv_bfloat16, 64, false>(b, s));
-    return D == 128 ? (paged ? launch_bulk_t<float, 128, true>(b, s)
-                             : launch_bulk_t<float, 128, false>(b, s))
-                    : (paged ? launch_bulk_t<float, 64, true>(b, s)
-                             : launch_bulk_t<float, 64, false>(b, s));
+      return D == 128 ? (paged ? launch_bulk_t<__nv_bfloat16, 128, true>(b, free_sms, s)
+                               : launch_bulk_t<__nv_bfloat16, 128, false>(b, free_sms, s))
+                      : (paged ? launch_bulk_t<__nv_bfloat16, 64, true>(b, free_sms, s)
+                               : launch_bulk_t<__nv_bfloat16, 64, false>(b, free_sms, s));
+    return D == 128 ? (paged ? launch_bulk_t<float, 128, true>(b, free_sms, s)
+                             : launch_bulk_t<float, 128, false>(b, free_sms, s))
+                    : (paged ? launch_bulk_t<float, 64, true>(b, free_sms, s)
+                             : launch_bulk_t<float, 64, false>(b, free_sms, s));
   }
   StitchArgs a;
   a.chunks = chunks.d_chunks;
