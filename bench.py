@@ -56,11 +56,17 @@ def _peaks():
 # kernel's sources are unchanged (hash of the files that define it)
 _PROFILED = {
     "attention_tc": ("attn_tc_kernel_qwen3_8b_layer.md",
-                     ["attention_tc.cu", "tc_ptx.cuh", "common.cuh"]),
+                     ["attention_tc.cu", "tc_ptx.cuh", "common.cuh", "launch.h"]),
+    "qkv_gemm_tc": ("gemm_tc_kernel_qwen3_8b_layer.md",
+                    ["gemm_tc.cu", "tc_ptx.cuh", "common.cuh", "launch.h"]),
+    "deviation_gemm_tc": ("gemm_tc_kernel_qwen3_8b_layer.md",
+                          ["gemm_tc.cu", "tc_ptx.cuh", "common.cuh", "launch.h"]),
 }
 
 
 def _traffic(kernel):
+    """DRAM bytes per launch of `kernel` from its committed ncu summary, or None
+    when there is none or the kernel's sources changed since the capture."""
     import hashlib
     if kernel not in _PROFILED:
         return None
@@ -75,12 +81,13 @@ def _traffic(kernel):
     vals = {}
     with open(path) as fh:
         for line in fh:
-            if ":" in line and line.split(":")[0].strip() in ("traffic_bytes_per_launch", "sources_sha256_16"):
+            if ":" in line:
                 k, v = line.split(":", 1)
                 vals[k.strip()] = v.strip()
     if vals.get("sources_sha256_16") != h.hexdigest()[:16]:
         return None
-    return float(vals["traffic_bytes_per_launch"])
+    v = vals.get("traffic_bytes_per_launch." + kernel, vals.get("traffic_bytes_per_launch"))
+    return float(v) if v is not None else None
 
 
 def _dist():
