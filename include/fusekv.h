@@ -176,9 +176,10 @@ fuse_status_t fuse_plan_requests(int32_t n_req, const int32_t* n_ctx, const int3
 /* Workspace bytes needed by every call below for the given request table
  * (host copy read) and layer shape.  The workspace is caller-owned device
  * memory, 256-byte aligned, zero-filled before its first use (for example by
- * fuse_workspace_reset), and reusable across calls on one stream: the calls
- * leave the counters they use at zero.  It begins with the error word that
- * fuse_check_errors() reads. */
+ * fuse_workspace_reset) and reusable across calls on one stream; calls on
+ * different streams need their own.  It begins with the error word that
+ * fuse_check_errors() reads; the rest is scratch that every call writes
+ * before it reads. */
 fuse_status_t fuse_workspace_size(const fuse_layer_desc_t* desc, const fuse_requests_t* reqs,
                                   size_t* bytes);
 
