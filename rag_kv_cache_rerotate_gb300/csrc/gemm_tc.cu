@@ -11,20 +11,26 @@
 //     over the gathered rows S, RoPE at each row's request position on Q and
 //     K heads, Q to a compact buffer, K and V scattered into the fused cache.
 //
-// One 128 x 256 output tile is two heads of 128 rows, so every epilogue sees
-// whole heads; its 256 B rows are loaded as two 128-row halves, each from the
-// weight matrix of its own head.  The wide tile halves the operand bytes each
-// SM must take in per flop compared with 128 x 128.  The kernel is persistent
-// (one CTA per SM) and warp specialised: warp 0 issues TMA loads into a
-// 4-stage shared-memory ring, warp 1 issues tcgen05.mma into one of two TMEM
-// accumulators, warps 2-9 (one warpgroup per head of the tile) drain the other
-// accumulator through tcgen05.ld and run the epilogue, so the epilogue of tile
-// i overlaps the main loop of tile i + 1.  The epilogue warps load what they
+// A CTA pair (cluster of two) computes a 256 x 256 output tile with 2-SM MMAs
+// (tcgen05.mma.cta_group::2): each CTA holds 128 rows of A and the 128 weight
+// rows of one head (the tile's two heads, each from the weight matrix of its
+// own head), and the pair's MMA gives each CTA its 128 rows x both heads in
+// its own TMEM.  Each SM thus takes in 32 KB of operands per 64-deep step
+// instead of the 48 KB a single-SM 128 x 256 tile needs, which is what one
+// SM's L2 port can feed at the MMA rate.  The kernel is persistent (one pair
+// per two SMs) and warp specialised: warp 0 of each CTA issues TMA loads into
+// a 6-stage ring; in the even CTA warp 1 issues the MMAs into one of two TMEM
+// accumulators, in the odd CTA warp 1 tells the even one (remote mbarrier
+// arrivals) when its stages have landed and its accumulator has been read;
+// warps 2-9 (one warpgroup per head) drain the other accumulator through
+// tcgen05.ld and run the epilogue, so the epilogue of tile i overlaps the main
+// loop of tile i + 1.  The epilogue warps load what they
 // read from global memory (cached V rows; work rows and RoPE factors) before
 // they wait for the accumulator, so those loads overlap the main loop.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <map>
 #include <mutex>
 
 #include "common.cuh"
@@ -35,25 +41,26 @@ namespace fusekv {
 
 namespace {
 
-constexpr int BM = 128;
+constexpr int BM = 128;                             // rows of A per CTA (256 per pair)
+constexpr int BMP = 2 * BM;                         // rows of a pair tile
 constexpr int BN = 128;                             // one head
 constexpr int BN2 = 2 * BN;                         // one tile: two heads
 constexpr int BK = 64;
-constexpr int STAGES = 4;
-constexpr int kTileBytes = BM * BK * 2;             // 16 KB: A, or one head's B half
-constexpr int kStageBytes = 3 * kTileBytes;         // A + two B halves
+constexpr int STAGES = 6;
+constexpr int kTileBytes = BM * BK * 2;             // 16 KB: A, or one head's B rows
+constexpr int kStageBytes = 2 * kTileBytes;         // this CTA's A rows + its head's B rows
 constexpr int kAccCols = BN2;
 constexpr int kTmemCols = 2 * kAccCols;             // two accumulators: all 512 columns
 constexpr int kEpiThreads = 256;                    // two warpgroups, one per head
 constexpr int kThreads = 64 + kEpiThreads;
-constexpr int kSmemBytes = STAGES * kStageBytes + 1024 + 256;
+constexpr int kSmemBytes = STAGES * kStageBytes + 1024 + 512;
 
 enum Mode : int { MODE_DEVIATION = 0, MODE_RECOMPUTE = 1 };
 
 struct TcArgs {
   int M;                 // rows of A
   int K;                 // hidden
-  int m_tiles;
+  int m_tiles;           // pair tiles of 256 rows
   int n_tiles;
   int h0, h1;            // heads taken by B map 0 and 1 (map 2 takes the rest)
   int mode;
@@ -86,6 +93,7 @@ struct SharedCtl {
   uint64_t empty[STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
+  uint64_t peer_tempty[2];     // even CTA: the odd CTA's epilogue has read the accumulator
   uint64_t xc_bar[2];          // [accumulator]: the second head's cosines written
   float xc[2][BM];             // [accumulator][row]: cosine of the tile's second head
   uint32_t tmem_base;
@@ -294,7 +302,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + STAGES * kStageBytes);
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
+  const uint32_t rank = tc::cluster_rank();          // 0: issues the pair's MMAs
   const int total = a.m_tiles * a.n_tiles;
+  const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
   const int k_blocks = a.K / BK;
 
   if (threadIdx.x == 0) {
@@ -305,18 +315,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&ctl->tfull[b], 1);
       tc::mbar_init(&ctl->tempty[b], kEpiThreads);
+      tc::mbar_init(&ctl->peer_tempty[b], 1);
       tc::mbar_init(&ctl->xc_bar[b], kEpiThreads / 2);
     }
     ctl->abort_flag = 0;
-    tc::fence_barrier_init();
+    tc::fence_barrier_init_cluster();
     tc::tma_prefetch_desc(&mapA);
     tc::tma_prefetch_desc(&mapB0);
     tc::tma_prefetch_desc(&mapB1);
     tc::tma_prefetch_desc(&mapB2);
   }
-  if (warp == 1) tc::tmem_alloc(&ctl->tmem_base, kTmemCols);
+  if (warp == 1) tc::tmem_alloc_pair(&ctl->tmem_base, kTmemCols);
   tc::tc_fence_before();
-  __syncthreads();
+  tc::cluster_sync_all();      // both CTAs' barriers exist before any remote arrival
   tc::tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
   pdl_wait();                 // inputs of the previous kernel complete and visible
@@ -325,32 +336,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_trigger();
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
+    // ---------------- TMA producer: this CTA's A rows and its head's B rows ----------------
     if (lane == 0) {
+      const uint32_t leader_full = tc::peer_smem(&ctl->full[0], 0);
       int s = 0;
       uint32_t ph = 0;
       bool armed[STAGES];
       uint32_t armed_ph[STAGES];
       for (int i = 0; i < STAGES; ++i) armed[i] = false;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = pair; tile < total && ok; tile += n_pairs) {
         const int mt = tile % a.m_tiles;
         const int nt = tile / a.m_tiles;
-        const CUtensorMap* mb[2];
-        int nrow[2];
-        for (int hb = 0; hb < 2; ++hb) {
-          const int head = 2 * nt + hb;
-          if (head < a.h0) {
-            mb[hb] = &mapB0;
-            nrow[hb] = head * BN;
-          } else if (head < a.h0 + a.h1) {
-            mb[hb] = &mapB1;
-            nrow[hb] = (head - a.h0) * BN;
-          } else {
-            mb[hb] = &mapB2;
-            nrow[hb] = (head - a.h0 - a.h1) * BN;
-          }
+        const int head = 2 * nt + (int)rank;
+        const CUtensorMap* mb;
+        int nrow;
+        if (head < a.h0) {
+          mb = &mapB0;
+          nrow = head * BN;
+        } else if (head < a.h0 + a.h1) {
+          mb = &mapB1;
+          nrow = (head - a.h0) * BN;
+        } else {
+          mb = &mapB2;
+          nrow = (head - a.h0 - a.h1) * BN;
         }
+        const int arow = mt * BMP + (int)rank * BM;
         for (int kb = 0; kb < k_blocks; ++kb) {
           if (!wait_or_abort(&ctl->empty[s], ph ^ 1, ctl)) {
             abort_kernel(ctl, a.err);
@@ -358,10 +369,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           uint8_t* sa = smem + s * kStageBytes;
-          tc::mbar_arrive_expect_tx(&ctl->full[s], kStageBytes);
-          tc::tma_load_2d(sa, &mapA, &ctl->full[s], kb * BK, mt * BM);
-          tc::tma_load_2d(sa + kTileBytes, mb[0], &ctl->full[s], kb * BK, nrow[0]);
-          tc::tma_load_2d(sa + 2 * kTileBytes, mb[1], &ctl->full[s], kb * BK, nrow[1]);
+          if (rank == 0) {
+            // the stage is full once both CTAs' bytes have landed
+            tc::mbar_arrive_expect_tx(&ctl->full[s], 2 * kStageBytes);
+            tc::tma_load_2d(sa, &mapA, &ctl->full[s], kb * BK, arow);
+            tc::tma_load_2d(sa + kTileBytes, mb, &ctl->full[s], kb * BK, nrow);
+          } else {
+            const uint32_t lf = leader_full + s * (uint32_t)sizeof(uint64_t);
+            tc::tma_load_2d_pair(sa, &mapA, lf, kb * BK, arow);
+            tc::tma_load_2d_pair(sa + kTileBytes, mb, lf, kb * BK, nrow);
+          }
           armed[s] = true;
           armed_ph[s] = ph;
           if (++s == STAGES) {
@@ -370,21 +387,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // copies still in flight land before the CTA can exit
-      for (int i = 0; i < STAGES; ++i)
-        if (armed[i]) tc::mbar_wait(&ctl->full[i], armed_ph[i]);
+      // copies still in flight land before the CTA can exit: the even CTA's
+      // full barriers count both CTAs' bytes, and the odd CTA leaves only
+      // after the even one (cluster barrier at the end)
+      if (rank == 0)
+        for (int i = 0; i < STAGES; ++i)
+          if (armed[i]) tc::mbar_wait(&ctl->full[i], armed_ph[i]);
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      const uint32_t idesc = tc::idesc_bf16_f32(BM, BN2);
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer of the pair ----------------
+      const uint32_t idesc = tc::idesc_bf16_f32(BMP, BN2);
       int s = 0;
       uint32_t ph = 0;
       int acc = 0;
       uint32_t acc_ph = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        if (!wait_or_abort(&ctl->tempty[acc], acc_ph ^ 1, ctl)) {
+      for (int tile = pair; tile < total && ok; tile += n_pairs) {
+        // both CTAs' epilogues have read this accumulator (previous use)
+        if (!wait_or_abort(&ctl->tempty[acc], acc_ph ^ 1, ctl) ||
+            !tc::mbar_wait_cluster(&ctl->peer_tempty[acc], acc_ph, &ctl->abort_flag)) {
           abort_kernel(ctl, a.err);
           break;
         }
@@ -402,15 +424,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t db = tc::smem_desc_k128(sa + kTileBytes);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            tc::mma_bf16(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
-          tc::mma_commit(&ctl->empty[s]);
+            tc::mma_bf16_pair(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+          tc::mma_commit_pair(&ctl->empty[s], 0x3);
           if (++s == STAGES) {
             s = 0;
             ph ^= 1;
           }
         }
         if (!ok) break;
-        tc::mma_commit(&ctl->tfull[acc]);
+        tc::mma_commit_pair(&ctl->tfull[acc], 0x3);
+        acc ^= 1;
+        if (acc == 0) acc_ph ^= 1;
+      }
+    } else if (lane == 0) {
+      // ---------------- odd CTA: report its epilogue's reads of each accumulator ----------------
+      const uint32_t leader_tempty = tc::peer_smem(&ctl->peer_tempty[0], 0);
+      int acc = 0;
+      uint32_t acc_ph = 0;
+      for (int tile = pair; tile < total; tile += n_pairs) {
+        if (!wait_or_abort(&ctl->tempty[acc], acc_ph ^ 1, ctl)) {
+          abort_kernel(ctl, a.err);
+          break;
+        }
+        tc::mbar_arrive_remote(leader_tempty + acc * (uint32_t)sizeof(uint64_t));
         acc ^= 1;
         if (acc == 0) acc_ph ^= 1;
       }
@@ -422,10 +458,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = quarter * 32 + lane;
     int acc = 0;
     uint32_t acc_ph = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    for (int tile = pair; tile < total; tile += n_pairs) {
       const int mt = tile % a.m_tiles;
       const int nt = tile / a.m_tiles;
-      const int m = mt * BM + row;
+      const int m = mt * BMP + (int)rank * BM + row;
       const int head = 2 * nt + hb;
       // one of the two is used (MODE is a compile-time constant)
       DevPre dp;
@@ -466,9 +502,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   tc::tc_fence_before();
-  __syncthreads();
+  __syncwarp();               // the cluster barrier is warp-aligned
+  tc::cluster_sync_all();     // the pair's MMAs are done with both CTAs' memory
   tc::tc_fence_after();
-  if (warp == 1) tc::tmem_dealloc(tmem_base, kTmemCols);
+  if (warp == 1) tc::tmem_dealloc_pair(tmem_base, kTmemCols);
 }
 
 // ---- host side ---------------------------------------------------------------
@@ -500,6 +537,40 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// CTA pairs of this kernel that can be resident at once (clusters of two
+// need two free SMs of one GPC), cached per device and kernel.
+int resident_pairs(const void* kernel) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, int> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> g(mu);
+  auto it = cache.find({dev, kernel});
+  if (it != cache.end()) return it->second;
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int n = std::max(1, sms / 2);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * n);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (set_dyn_smem_once(kernel, kSmemBytes) == cudaSuccess &&
+      cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) == cudaSuccess && clusters > 0)
+    n = std::min(n, clusters);
+  else
+    cudaGetLastError();
+  cache[{dev, kernel}] = n;
+  return n;
+}
+
 int sm_count() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);
@@ -514,8 +585,9 @@ cudaError_t launch(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtensor
   auto kernel = a.mode == MODE_DEVIATION ? gemm_tc_kernel<MODE_DEVIATION> : gemm_tc_kernel<MODE_RECOMPUTE>;
   cudaError_t e = set_dyn_smem_once(reinterpret_cast<const void*>(kernel), kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int grid = total < sm_count() ? total : sm_count();
-  return launch_pdl(kernel, dim3(grid), dim3(kThreads), kSmemBytes, s, mA, mB0, mB1, mB2, a);
+  const int pairs = std::min(total, resident_pairs(reinterpret_cast<const void*>(kernel)));
+  return launch_pdl_pairs(kernel, dim3(2 * pairs), dim3(kThreads), kSmemBytes, s, mA, mB0, mB1,
+                          mB2, a);
 }
 
 }  // namespace
@@ -557,7 +629,7 @@ cudaError_t launch_deviation_partials_tc(const fuse_layer_desc_t& d, int64_t n_r
   TcArgs a = {};
   a.M = (int)n_rows;
   a.K = d.hidden;
-  a.m_tiles = (int)((n_rows + BM - 1) / BM);
+  a.m_tiles = (int)((n_rows + BMP - 1) / BMP);
   a.n_tiles = d.n_kv_heads / 2;
   a.h0 = d.n_kv_heads;
   a.h1 = 0;
@@ -581,8 +653,10 @@ cudaError_t launch_deviation_partials_tc(const fuse_layer_desc_t& d, int64_t n_r
 }
 
 int deviation_tc_ctas(const fuse_layer_desc_t& d, int64_t n_rows) {
-  const int64_t tiles = ((n_rows + BM - 1) / BM) * (d.n_kv_heads / 2);
-  return (int)std::min<int64_t>(tiles, sm_count());
+  const int64_t tiles = ((n_rows + BMP - 1) / BMP) * (d.n_kv_heads / 2);
+  const int pairs =
+      resident_pairs(reinterpret_cast<const void*>(gemm_tc_kernel<MODE_DEVIATION>));
+  return 2 * (int)std::min<int64_t>(tiles, pairs);
 }
 
 cudaError_t launch_project_recompute_tc(const fuse_layer_desc_t& d, int64_t n_rows,
@@ -600,7 +674,7 @@ cudaError_t launch_project_recompute_tc(const fuse_layer_desc_t& d, int64_t n_ro
   TcArgs a = {};
   a.M = (int)n_rows;
   a.K = d.hidden;
-  a.m_tiles = (int)((n_rows + BM - 1) / BM);
+  a.m_tiles = (int)((n_rows + BMP - 1) / BMP);
   a.n_tiles = (d.n_q_heads + 2 * d.n_kv_heads) / 2;
   a.h0 = d.n_q_heads;
   a.h1 = d.n_kv_heads;
