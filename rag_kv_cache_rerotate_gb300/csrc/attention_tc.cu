@@ -136,6 +136,34 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Packed pairs of floats for the f32x2 arithmetic of sm_100 and later: one
+// instruction does the operation on both halves.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 unpack2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -146,42 +174,6 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 // 64-column halves
 __device__ __forceinline__ uint64_t kmajor_step(uint32_t tile, int kk) {
   return tc::smem_desc_k128(tile + (kk >> 2) * kHalf + (kk & 3) * 32);
-}
-
-// Maximum of 32 scores, masked (-1e30) past position p when `mask`.
-__device__ __forceinline__ float masked_max32(const uint32_t (&r)[32], bool mask, int key0, int p) {
-  float v[32];
-#pragma unroll
-  for (int c = 0; c < 32; ++c) {
-    const float x = __uint_as_float(r[c]);
-    v[c] = (mask && key0 + c > p) ? -1e30f : x;
-  }
-  float t[11];
-#pragma unroll
-  for (int i = 0; i < 10; ++i) t[i] = max3(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
-  t[10] = fmaxf(v[30], v[31]);
-  const float u0 = max3(t[0], t[1], t[2]), u1 = max3(t[3], t[4], t[5]);
-  const float u2 = max3(t[6], t[7], t[8]), u3 = fmaxf(t[9], t[10]);
-  return fmaxf(max3(u0, u1, u2), u3);
-}
-
-// 32 probabilities 2^(s * scale - m) (0 past position p when `mask`) packed as
-// bf16 pairs; returns their sum.
-__device__ __forceinline__ float probs32(const uint32_t (&r)[32], bool mask, int key0, int p,
-                                         float scale, float neg_m, uint32_t (&pk)[16]) {
-  float e[32];
-#pragma unroll
-  for (int c = 0; c < 32; ++c) {
-    const float x = (mask && key0 + c > p) ? -1e30f : __uint_as_float(r[c]);
-    e[c] = ex2(fmaf(x, scale, neg_m));
-  }
-#pragma unroll
-  for (int c = 0; c < 32; c += 2) pk[c / 2] = pack_bf16x2(e[c], e[c + 1]);
-#pragma unroll
-  for (int w = 16; w >= 1; w >>= 1)
-#pragma unroll
-    for (int i = 0; i < w; ++i) e[i] += e[i + w];
-  return e[0];
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -467,20 +459,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ms1 > mu1 + kRescaleThreshold) { mn1 = ms1; rs1 = true; }
         }
         const float al0 = rs0 ? ex2(mu0 - mn0) : 1.f, al1 = rs1 ? ex2(mu1 - mn1) : 1.f;
-        // probabilities: key pairs packed as bf16x2, in place over the scores
-        const float ng0 = -mn0, ng1 = -mn1;
-        float s0 = 0.f, s1 = 0.f;
+        // probabilities: key pairs packed as bf16x2, in place over the scores;
+        // the scaling and the row sums work on key pairs (f32x2)
+        const uint64_t sc2 = pack2(scale, scale);
+        const uint64_t ng0 = pack2(-mn0, -mn0), ng1 = pack2(-mn1, -mn1);
+        uint64_t acc0 = 0, acc1 = 0;                    // (even keys, odd keys) of each row
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
-          const float e0 = ex2(fmaf(__uint_as_float(r[4 * q]), scale, ng0));
-          const float e1 = ex2(fmaf(__uint_as_float(r[4 * q + 1]), scale, ng0));
-          const float e2 = ex2(fmaf(__uint_as_float(r[4 * q + 2]), scale, ng1));
-          const float e3 = ex2(fmaf(__uint_as_float(r[4 * q + 3]), scale, ng1));
-          s0 += e0 + e1;
-          s1 += e2 + e3;
+          const float2 x01 = unpack2(fma2(pack2(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1])), sc2, ng0));
+          const float2 x23 = unpack2(fma2(pack2(__uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3])), sc2, ng1));
+          const float e0 = ex2(x01.x), e1 = ex2(x01.y), e2 = ex2(x23.x), e3 = ex2(x23.y);
+          acc0 = add2(acc0, pack2(e0, e1));
+          acc1 = add2(acc1, pack2(e2, e3));
           r[2 * q] = pack_bf16x2(e0, e1);
           r[2 * q + 1] = pack_bf16x2(e2, e3);
         }
+        const float2 a0 = unpack2(acc0), a1 = unpack2(acc1);
+        const float s0 = a0.x + a0.y, s1 = a1.x + a1.y;
         tc::tmem_st_16x128b_x16(tS, *reinterpret_cast<uint32_t(*)[32]>(r));
         // tcgen05.ld/st are warp-collective (.sync.aligned): the whole warp
         // rescales its rows of O when any of them needs it (the factor is 1
@@ -497,9 +492,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t o[32];
             tc::tmem_ld_16x256b_x8(tO + c, o);
             tc::tmem_ld_wait();
+            const uint64_t f0 = pack2(al0, al0), f1 = pack2(al1, al1);
 #pragma unroll
-            for (int q = 0; q < 32; ++q)
-              o[q] = __float_as_uint(__uint_as_float(o[q]) * ((q & 2) ? al1 : al0));
+            for (int q = 0; q < 32; q += 2) {
+              const float2 v = unpack2(mul2(pack2(__uint_as_float(o[q]), __uint_as_float(o[q + 1])), (q & 2) ? f1 : f0));
+              o[q] = __float_as_uint(v.x);
+              o[q + 1] = __float_as_uint(v.y);
+            }
             tc::tmem_st_16x256b_x8(tO + c, o);
           }
         }
