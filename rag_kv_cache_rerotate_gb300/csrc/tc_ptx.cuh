@@ -58,7 +58,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Wait until the phase with the given parity has completed; false once
 // kWaitLimitNs have passed.  If abort_flag is given, also false soon after
-// it becomes non-zero.
+// it becomes non-zero.  try_wait itself suspends the thread for a while in
+// hardware, so the loop adds no sleep of its own: a sleep between polls
+// delays the hand-offs between the pipeline roles.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           const volatile int* abort_flag = nullptr) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -69,7 +71,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
       if (abort_flag && *abort_flag) return false;
       if (global_ns() - t0 > kWaitLimitNs) return false;
     }
-    if (i > 32) __nanosleep(64);
   }
   return false;
 }
@@ -124,7 +125,6 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
       if (abort_flag && *abort_flag) return false;
       if (global_ns() - t0 > kWaitLimitNs) return false;
     }
-    if (i > 32) __nanosleep(64);
   }
   return false;
 }
