@@ -277,7 +277,7 @@ fuse_status_t do_recompute(const fuse_layer_desc_t& d, const fuse_requests_t& r,
   cudaError_t e;
   if (tc_gemm) {
     e = traced("prepare_rows", s, [&] {
-      return launch_prepare_rows(r, max_rows, idx, f, d.head_dim, H, d.hidden, rows, rope,
+      return launch_prepare_rows(r, max_rows, idx, f, d.head_dim, H, d.hidden, rows, rope, R,
                                  at<void>(ws, L.hs), tc_attn ? attention_rtile(d) : 128,
                                  tc_attn ? at<void>(ws, L.tiles) : nullptr, err, s);
     });
@@ -288,7 +288,7 @@ fuse_status_t do_recompute(const fuse_layer_desc_t& d, const fuse_requests_t& r,
     });
   } else {
     e = traced("sel_rows", s, [&] {
-      return launch_build_sel_rows(r, max_rows, idx, f, d.head_dim, rows, rope, err, s);
+      return launch_build_sel_rows(r, max_rows, idx, f, d.head_dim, rows, rope, R, err, s);
     });
     if (e != cudaSuccess) return FUSE_ERR_CUDA;
     e = traced("qkv_gemm_simt", s, [&] {

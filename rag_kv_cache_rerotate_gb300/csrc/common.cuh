@@ -175,6 +175,14 @@ struct WorkRow {
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// RoPE table of the work rows: (cos, sin) of frequency pair j of work row m
+// sits at this float2 index.  Pairs of pairs are stored pair-major, so the
+// four floats of pairs 2i, 2i + 1 of row m are one float4 at i * n_rows + m
+// and threads holding consecutive rows read consecutive 16-byte entries.
+__host__ __device__ inline int64_t rope_index(int j, int64_t m, int64_t n_rows) {
+  return (((int64_t)(j >> 1) * n_rows + m) << 1) | (j & 1);
+}
+
 #ifdef __CUDACC__
 // Tile records of the tensor-core attention: the recomputed rows of each
 // request cut into tiles of rtile rows, in request order, each recorded as

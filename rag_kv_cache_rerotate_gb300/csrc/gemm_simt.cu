@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kThreads) gemm_simt_kernel(const GemmArgs a) {
         rot = false;
       }
       if (rot) {
-        const float2 cs = a.rope[m * H2 + j];
+        const float2 cs = a.rope[rope_index(j, m, a.M)];
         const float xr = fmaf(x, cs.x, -y * cs.y);
         const float yr = fmaf(y, cs.x, x * cs.y);
         x = xr;

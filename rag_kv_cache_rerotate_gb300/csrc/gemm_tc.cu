@@ -86,6 +86,7 @@ struct TcArgs {
   __nv_bfloat16* Kf;
   __nv_bfloat16* Vout;
   uint32_t* err;
+  int st32;              // Q, Kf and Vout 32-byte aligned: one 256-bit store per 16 values
 };
 
 struct SharedCtl {
@@ -204,6 +205,17 @@ __device__ __forceinline__ void store_bf16x16(__nv_bfloat16* dst, const float (&
   }
 }
 
+// The same as one 256-bit store (dst 32-byte aligned): the 32 bytes a thread
+// writes fill one sector in one instruction.
+__device__ __forceinline__ void store_bf16x16_v8(__nv_bfloat16* dst, const float (&x)[16]) {
+  uint32_t w[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) w[q] = pack_bf16x2(x[2 * q], x[2 * q + 1]);
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&x)[32]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -238,15 +250,16 @@ __device__ __forceinline__ void pre_recompute(const TcArgs& a, int m, int head, 
                             : a.Vout + (w.dst_row * Hkv + (head - Hq - Hkv)) * BN;
   }
   if (p.rot) {
-    const float4* cs = reinterpret_cast<const float4*>(a.rope + (int64_t)m * (BN / 2));
+    // (cos, sin) of pairs 2i, 2i + 1: one float4 at i * M + m (rope_index)
+    const float4* cs = reinterpret_cast<const float4*>(a.rope) + m;
 #pragma unroll
-    for (int i = 0; i < kRopeChunk / 2; ++i) p.cs[i] = __ldg(cs + i);
+    for (int i = 0; i < kRopeChunk / 2; ++i) p.cs[i] = __ldg(cs + (int64_t)i * a.M);
   }
 }
 
 __device__ __forceinline__ void epi_recompute(const TcArgs& a, uint32_t taddr, int m,
                                               const RecPre& p) {
-  const float4* csrow = reinterpret_cast<const float4*>(a.rope + (int64_t)m * (BN / 2));
+  const float4* csrow = reinterpret_cast<const float4*>(a.rope) + m;
   float4 cs[kRopeChunk / 2];
 #pragma unroll
   for (int i = 0; i < kRopeChunk / 2; ++i) cs[i] = p.cs[i];
@@ -256,7 +269,8 @@ __device__ __forceinline__ void epi_recompute(const TcArgs& a, uint32_t taddr, i
     float4 nx[kRopeChunk / 2];
     if (p.rot && p.dst && j0 + kRopeChunk < BN / 2) {
 #pragma unroll
-      for (int i = 0; i < kRopeChunk / 2; ++i) nx[i] = __ldg(csrow + (j0 + kRopeChunk) / 2 + i);
+      for (int i = 0; i < kRopeChunk / 2; ++i)
+        nx[i] = __ldg(csrow + (int64_t)((j0 + kRopeChunk) / 2 + i) * a.M);
     }
     uint32_t rx[kRopeChunk], ry[kRopeChunk];
     tc::tmem_ld_32x32b_x16(taddr + j0, rx);
@@ -282,8 +296,13 @@ __device__ __forceinline__ void epi_recompute(const TcArgs& a, uint32_t taddr, i
           y[i] = __uint_as_float(ry[i]);
         }
       }
-      store_bf16x16(p.dst + j0, x);
-      store_bf16x16(p.dst + j0 + BN / 2, y);
+      if (a.st32) {
+        store_bf16x16_v8(p.dst + j0, x);
+        store_bf16x16_v8(p.dst + j0 + BN / 2, y);
+      } else {
+        store_bf16x16(p.dst + j0, x);
+        store_bf16x16(p.dst + j0 + BN / 2, y);
+      }
     }
     if (j0 + kRopeChunk < BN / 2) {
 #pragma unroll
@@ -686,6 +705,8 @@ cudaError_t launch_project_recompute_tc(const fuse_layer_desc_t& d, int64_t n_ro
   a.Q = reinterpret_cast<__nv_bfloat16*>(Q);
   a.Kf = reinterpret_cast<__nv_bfloat16*>(Kf);
   a.Vout = reinterpret_cast<__nv_bfloat16*>(Vf);
+  a.st32 = ((reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(Kf) |
+             reinterpret_cast<uintptr_t>(Vf)) & 31u) == 0;
   a.err = err;
   return launch(mA, mQ, mK, mV, a, s);
 }

@@ -82,7 +82,7 @@ cudaError_t launch_build_score_map(const fuse_requests_t& reqs, int max_tok, int
 // Work rows (and their RoPE table) of S_r = idx_r U query rows, per request.
 cudaError_t launch_build_sel_rows(const fuse_requests_t& reqs, int max_rows, const int32_t* idx,
                                   const RopeFreqs& freqs, int head_dim, WorkRow* rows,
-                                  float2* rope, uint32_t* err, cudaStream_t s);
+                                  float2* rope, int64_t n_rows, uint32_t* err, cudaStream_t s);
 
 // Deviation: partial[slot, h] = cos(H_t W_V^T [h], Vf[t, h]) over all packed rows.
 cudaError_t launch_deviation_partials_simt(const fuse_layer_desc_t& desc, int64_t n_rows, const void* H,
@@ -97,8 +97,8 @@ cudaError_t launch_deviation_reduce(int64_t n_ctx, int n_parts, int n_kv_heads,
 // (tensor-core path), one launch.
 cudaError_t launch_prepare_rows(const fuse_requests_t& reqs, int max_rows, const int32_t* idx,
                                 const RopeFreqs& freqs, int head_dim, const void* H, int hidden,
-                                WorkRow* rows, float2* rope, void* Hs, int rtile, void* tiles,
-                                uint32_t* err, cudaStream_t s);
+                                WorkRow* rows, float2* rope, int64_t n_rows, void* Hs, int rtile,
+                                void* tiles, uint32_t* err, cudaStream_t s);
 
 // score = 1 - (sum_p partial[p]) / n_kv_heads, written to score[], then
 // top-k per request.

@@ -23,7 +23,8 @@ __global__ void score_map_kernel(const fuse_request_t* reqs, int32_t* map) {
 
 // One thread per (work row, frequency pair).
 __global__ void sel_rows_kernel(const fuse_request_t* reqs, const int32_t* idx, RopeFreqs f,
-                                int half_dim, WorkRow* rows, float2* rope, uint32_t* err) {
+                                int half_dim, WorkRow* rows, float2* rope, int64_t total_rows,
+                                uint32_t* err) {
   const int r = blockIdx.y;
   const fuse_request_t R = reqs[r];
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -56,7 +57,7 @@ __global__ void sel_rows_kernel(const fuse_request_t* reqs, const int32_t* idx, 
   }
   float c, sn;
   rope_cos_sin(s, f.hi[j], f.mid[j], f.lo[j], c, sn);
-  rope[out * half_dim + j] = make_float2(c, sn);
+  rope[rope_index(j, out, total_rows)] = make_float2(c, sn);
 }
 
 // One block per recomputed row (blockIdx.y = request): the work row, its RoPE
@@ -66,6 +67,7 @@ __global__ void __launch_bounds__(256) prepare_rows_kernel(const fuse_request_t*
                                                            const int32_t* idx, RopeFreqs f,
                                                            int half_dim, const __nv_bfloat16* H,
                                                            int hidden, WorkRow* rows, float2* rope,
+                                                           int64_t n_rows,
                                                            __nv_bfloat16* Hs, int rtile,
                                                            int4* tiles, uint32_t* err) {
   pdl_trigger();
@@ -101,7 +103,7 @@ __global__ void __launch_bounds__(256) prepare_rows_kernel(const fuse_request_t*
   if (t < half_dim) {
     float c, sn;
     rope_cos_sin(s, f.hi[t], f.mid[t], f.lo[t], c, sn);
-    rope[out * half_dim + t] = make_float2(c, sn);
+    rope[rope_index(t, out, n_rows)] = make_float2(c, sn);
   }
   const uint4* src = reinterpret_cast<const uint4*>(H + (R.row0 + s) * (int64_t)hidden);
   uint4* dst = reinterpret_cast<uint4*>(Hs + out * (int64_t)hidden);
@@ -112,12 +114,12 @@ __global__ void __launch_bounds__(256) prepare_rows_kernel(const fuse_request_t*
 
 cudaError_t launch_prepare_rows(const fuse_requests_t& reqs, int max_rows, const int32_t* idx,
                                 const RopeFreqs& freqs, int head_dim, const void* H, int hidden,
-                                WorkRow* rows, float2* rope, void* Hs, int rtile, void* tiles,
-                                uint32_t* err, cudaStream_t s) {
+                                WorkRow* rows, float2* rope, int64_t n_rows, void* Hs, int rtile,
+                                void* tiles, uint32_t* err, cudaStream_t s) {
   if (reqs.n_req == 0 || max_rows == 0) return cudaSuccess;
   dim3 grid(max_rows, reqs.n_req);
   return launch_pdl(prepare_rows_kernel, grid, dim3(256), 0, s, reqs.d_req, reqs.n_req, idx, freqs,
-                    head_dim / 2, reinterpret_cast<const __nv_bfloat16*>(H), hidden, rows, rope,
+                    head_dim / 2, reinterpret_cast<const __nv_bfloat16*>(H), hidden, rows, rope, n_rows,
                     reinterpret_cast<__nv_bfloat16*>(Hs), rtile, reinterpret_cast<int4*>(tiles),
                     err);
 }
@@ -132,12 +134,12 @@ cudaError_t launch_build_score_map(const fuse_requests_t& reqs, int max_tok, int
 
 cudaError_t launch_build_sel_rows(const fuse_requests_t& reqs, int max_rows, const int32_t* idx,
                                   const RopeFreqs& freqs, int head_dim, WorkRow* rows,
-                                  float2* rope, uint32_t* err, cudaStream_t s) {
+                                  float2* rope, int64_t n_rows, uint32_t* err, cudaStream_t s) {
   if (reqs.n_req == 0 || max_rows == 0) return cudaSuccess;
   const int h2 = head_dim / 2;
   const int64_t items = (int64_t)max_rows * h2;
   dim3 grid((unsigned)((items + 255) / 256), reqs.n_req);
-  sel_rows_kernel<<<grid, 256, 0, s>>>(reqs.d_req, idx, freqs, h2, rows, rope, err);
+  sel_rows_kernel<<<grid, 256, 0, s>>>(reqs.d_req, idx, freqs, h2, rows, rope, n_rows, err);
   return cudaGetLastError();
 }
 

@@ -25,33 +25,39 @@ __device__ __forceinline__ uint32_t float_key(float f, bool* is_nan) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-// Exclusive block-wide scan of one value per thread; also returns the total.
-__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_buf,
-                                                         uint32_t* total) {
+// Exclusive block-wide scan of a pair of values per thread (one pass of
+// barriers for both); the buffer is not reused after it.
+__device__ __forceinline__ uint2 block_exclusive_scan2(uint32_t a, uint32_t b, uint2* wbuf) {
   const int lane = threadIdx.x % 32;
   const int warp = threadIdx.x / 32;
-  uint32_t x = v;
+  uint32_t xa = a, xb = b;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
+    const uint32_t ya = __shfl_up_sync(0xffffffffu, xa, o);
+    const uint32_t yb = __shfl_up_sync(0xffffffffu, xb, o);
+    if (lane >= o) {
+      xa += ya;
+      xb += yb;
+    }
   }
-  if (lane == 31) warp_buf[warp] = x;
+  if (lane == 31) wbuf[warp] = make_uint2(xa, xb);
   __syncthreads();
   if (warp == 0) {
-    uint32_t w = lane < (int)(blockDim.x / 32) ? warp_buf[lane] : 0u;
+    uint2 w = lane < (int)(blockDim.x / 32) ? wbuf[lane] : make_uint2(0u, 0u);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
+      const uint32_t ya = __shfl_up_sync(0xffffffffu, w.x, o);
+      const uint32_t yb = __shfl_up_sync(0xffffffffu, w.y, o);
+      if (lane >= o) {
+        w.x += ya;
+        w.y += yb;
+      }
     }
-    warp_buf[lane] = w;   // inclusive prefix over warps
+    wbuf[lane] = w;   // inclusive prefix over warps
   }
   __syncthreads();
-  const uint32_t before = (warp > 0 ? warp_buf[warp - 1] : 0u) + x - v;
-  *total = warp_buf[blockDim.x / 32 - 1];
-  __syncthreads();
-  return before;
+  const uint2 pw = warp > 0 ? wbuf[warp - 1] : make_uint2(0u, 0u);
+  return make_uint2(pw.x + xa - a, pw.y + xb - b);
 }
 
 // With partial != null the scores are first formed from the cosine partials
@@ -68,6 +74,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const fuse_request_t
   __shared__ uint32_t hist[256];
   __shared__ uint32_t warp_buf[32];
   __shared__ uint32_t sel_digit, sel_remaining;
+  __shared__ uint2 pair_buf[32];
   pdl_trigger();
   pdl_wait();
   const int r = blockIdx.x;
@@ -88,20 +95,30 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const fuse_request_t
 
   bool nan_seen = false;
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-  for (int i = t; i < n; i += kTopkThreads) {
-    bool nn;
-    float v;
-    if (partial) {
-      v = head_mean_score(partial + (R.score0 + i) * n_parts, n_parts, n_kv_heads);
-      score_out[R.score0 + i] = v;
-    } else {
-      v = score[R.score0 + i];
+  // four tokens per thread at a time: their loads are all issued before the
+  // first store, so their latencies overlap
+  for (int i0 = t; i0 < n; i0 += 4 * kTopkThreads) {
+    float v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = i0 + q * kTopkThreads;
+      if (i < n)
+        v[q] = partial ? head_mean_score(partial + (R.score0 + i) * n_parts, n_parts, n_kv_heads)
+                       : score[R.score0 + i];
     }
-    const uint32_t key = float_key(v, &nn);
-    keys[i] = key;
-    kmin = min(kmin, key);
-    kmax = max(kmax, key);
-    nan_seen |= nn;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = i0 + q * kTopkThreads;
+      if (i < n) {
+        if (partial) score_out[R.score0 + i] = v[q];
+        bool nn;
+        const uint32_t key = float_key(v[q], &nn);
+        keys[i] = key;
+        kmin = min(kmin, key);
+        kmax = max(kmax, key);
+        nan_seen |= nn;
+      }
+    }
   }
   if (nan_seen) report_error(err, FUSE_ERR_DEVICE_BOUNDS, SITE_TOPK_NAN, r);
   // the keys' common leading bits decide nothing: start below them
@@ -196,10 +213,12 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const fuse_request_t
     n_gt += key > tau;
     n_eq += key == tau;
   }
-  uint32_t tot;
-  const uint32_t eq_before = block_exclusive_scan(n_eq, warp_buf, &tot);
+  // outputs before this thread's range: every key above tau there, and of
+  // the keys equal to it the first need_eq in index order
+  const uint2 before = block_exclusive_scan2(n_gt, n_eq, pair_buf);
+  const uint32_t eq_before = before.y;
   const uint32_t take_eq = eq_before >= need_eq ? 0u : min(n_eq, need_eq - eq_before);
-  const uint32_t out_before = block_exclusive_scan(n_gt + take_eq, warp_buf, &tot);
+  const uint32_t out_before = before.x + min(eq_before, need_eq);
   int32_t* out = idx + R.sel0;
   uint32_t o = out_before, eq_taken = 0;
   for (int i = i0; i < i1; ++i) {
