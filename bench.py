@@ -393,35 +393,78 @@ def native_run(args, ws, rank, local):
                 "frac": ach / peak, "traffic": _traffic(dom),
                 "peak_source": f"{peak_src} ({'sustained bf16' if bound == 'tensor' else 'HBM copy'})"}
 
-    # end to end through the C ABI with host buffers
+    # end to end through the C ABI with host buffers: every step uploads its
+    # inputs (chunk K/V caches and H) from pinned host memory and reads its
+    # result (O and idx) back.  Two input sets alternate so that, as in a
+    # serving loop, one step's upload runs on a copy stream while the previous
+    # step computes; every copy of every step lies inside the timed region.
     e2e = None
     if args.e2e_steps > 0:
-        b = sets[0]
-        host_in = []
-        for tsr in [b.H] + [v for k, v in b.storage.items() if k in ("K", "V")]:
-            h = torch.empty(tsr.shape, dtype=tsr.dtype, pin_memory=True)
-            h.copy_(tsr)
-            host_in.append((h, tsr))
-        O_h = torch.empty(b.O.shape, dtype=b.O.dtype, pin_memory=True)
-        idx_h = torch.empty(b.idx.shape, dtype=b.idx.dtype, pin_memory=True)
-        h2d = sum(h.numel() * h.element_size() for h, _ in host_in)
-        d2h = O_h.numel() * O_h.element_size() + idx_h.numel() * idx_h.element_size()
+        bufs = sets[:2]
+        host_in, host_out = [], []
+        for b in bufs:
+            pairs = []
+            for tsr in [b.H] + [v for k, v in b.storage.items() if k in ("K", "V")]:
+                h = torch.empty(tsr.shape, dtype=tsr.dtype, pin_memory=True)
+                h.copy_(tsr)
+                pairs.append((h, tsr))
+            host_in.append(pairs)
+            host_out.append((torch.empty(b.O.shape, dtype=b.O.dtype, pin_memory=True),
+                             torch.empty(b.idx.shape, dtype=b.idx.dtype, pin_memory=True)))
+        h2d = sum(h.numel() * h.element_size() for h, _ in host_in[0])
+        d2h = sum(t.numel() * t.element_size() for t in host_out[0])
+        # the upload spread over the copy streams (in pieces of at most 8 MiB
+        # when there are several; one stream already saturates the host link)
+        n_up = max(1, args.e2e_copy_streams)
+        ups = [torch.cuda.Stream() for _ in range(n_up)]
+        pieces = []
+        for pairs in host_in:
+            lst = []
+            for h, dv in pairs:
+                hf, df = h.view(-1), dv.view(-1)
+                step_el = max(1, (8 << 20) // h.element_size()) if n_up > 1 else hf.numel()
+                for o in range(0, hf.numel(), step_el):
+                    lst.append((hf[o:o + step_el], df[o:o + step_el]))
+            pieces.append(lst)
+        up = ups[0]
+        down = torch.cuda.Stream()
+        computed = [torch.cuda.Event() for _ in bufs]    # step on set s done
+        uploaded = [[torch.cuda.Event() for _ in ups] for _ in bufs]   # set s's inputs in place
+        read = [torch.cuda.Event() for _ in bufs]        # set s's results copied out
 
-        def e2e_step():
-            for h, dv in host_in:
-                dv.copy_(h, non_blocking=True)
+        def e2e_step(i):
+            s = i % 2
+            b = bufs[s]
+            for u in ups:
+                u.wait_event(computed[s])                 # the last step on set s read its inputs
+            for q, (h, dv) in enumerate(pieces[s]):
+                with torch.cuda.stream(ups[q % n_up]):
+                    dv.copy_(h, non_blocking=True)
+            for q, u in enumerate(ups):
+                uploaded[s][q].record(u)
+                stream.wait_event(uploaded[s][q])
+            stream.wait_event(read[s])                     # its previous results are out
             _step(fk, b)
-            O_h.copy_(b.O, non_blocking=True)
-            idx_h.copy_(b.idx, non_blocking=True)
+            computed[s].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(computed[s])
+                O_h, idx_h = host_out[s]
+                O_h.copy_(b.O, non_blocking=True)
+                idx_h.copy_(b.idx, non_blocking=True)
+                read[s].record(down)
 
-        for _ in range(3):
-            e2e_step()
+        for i in range(4):
+            e2e_step(i)
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
+        e0.record(up)                                      # before the first upload
+        for u in ups[1:] + [stream, down]:
+            u.wait_event(e0)
+        for i in range(args.e2e_steps):
+            e2e_step(i)
+        for s in range(2):
+            stream.wait_event(read[s])                     # after the last read-back
         e1.record(stream)
         torch.cuda.synchronize()
         ems = e0.elapsed_time(e1)
@@ -432,7 +475,11 @@ def native_run(args, ws, rank, local):
         e2e = {"value": ws * T * args.e2e_steps / (ems / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "steps": args.e2e_steps,
-               "what": "pinned-host chunk K/V caches and H copied in, fuse_layer_step, O and idx copied out"}
+               "what": "pinned-host chunk K/V caches and H copied in, fuse_layer_step, O and idx "
+                       "copied out; two input sets alternate, uploads overlap the previous step",
+               "copy_streams": n_up}
+        for b in bufs:
+            fk.check_errors(b.ws)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -483,6 +530,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--e2e-copy-streams", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=30.0)
     ap.add_argument("--ref-budget", type=float, default=150.0)
