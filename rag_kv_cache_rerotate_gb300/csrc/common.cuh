@@ -45,7 +45,8 @@ __device__ __forceinline__ void report_error(uint32_t* err, fuse_status_t code, 
 // that it may start while the previous one drains (launch_pdl).  A kernel lets
 // the next one start once all of its own CTAs are running (pdl_trigger) and
 // waits for the previous kernel to complete, with its writes visible, before
-// it touches global memory (pdl_wait); only on-chip set-up runs before that.
+// it touches global memory (pdl_wait); only on-chip set-up, and reads of the
+// caller's request table (which no kernel writes), run before that.
 // Both are no-ops for a kernel launched without the attribute.
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void pdl_trigger() {
@@ -142,6 +143,13 @@ __device__ __forceinline__ void rope_cos_sin(int p, float hi, float mid, float l
 // ----------------------------------------------------------------------------
 // The partials of a token are n_parts sums of its per-KV-head cosines (one
 // per head, or one per pair of heads); the score is
+// The same for n_parts == 4, from the four partials already loaded (the
+// same additions in the same order).
+__device__ __forceinline__ float head_mean_score4(float4 v, int n_heads) {
+  const float acc = (((0.f + v.x) + v.y) + v.z) + v.w;
+  return 1.0f - acc / (float)n_heads;
+}
+
 // 1 - (sum_p partial[p]) / n_heads, the sum taken in partial order; 16-byte
 // loads when n_parts % 4 == 0.
 __device__ __forceinline__ float head_mean_score(const float* pr, int n_parts, int n_heads) {

@@ -70,10 +70,10 @@ __global__ void __launch_bounds__(256) prepare_rows_kernel(const fuse_request_t*
                                                            int64_t n_rows,
                                                            __nv_bfloat16* Hs, int rtile,
                                                            int4* tiles, uint32_t* err) {
+  const int r = blockIdx.y;
+  const fuse_request_t R = reqs[r];     // the caller's table: no kernel writes it
   pdl_trigger();
   pdl_wait();
-  const int r = blockIdx.y;
-  const fuse_request_t R = reqs[r];
   const int o = blockIdx.x;
   const int t = threadIdx.x;
   if (tiles && o == 0 && r == 0) build_attn_tiles(reqs, n_req, idx, rtile, tiles);

@@ -75,10 +75,10 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const fuse_request_t
   __shared__ uint32_t warp_buf[32];
   __shared__ uint32_t sel_digit, sel_remaining;
   __shared__ uint2 pair_buf[32];
+  const int r = blockIdx.x;
+  const fuse_request_t R = reqs[r];     // the caller's table: no kernel writes it
   pdl_trigger();
   pdl_wait();
-  const int r = blockIdx.x;
-  const fuse_request_t R = reqs[r];
   const int n = R.n_ctx;
   const int k = R.k;
   if (n <= 0) return;
@@ -99,12 +99,24 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const fuse_request_t
   // first store, so their latencies overlap
   for (int i0 = t; i0 < n; i0 += 4 * kTopkThreads) {
     float v[4];
+    if (partial && n_parts == 4) {                 // one 16-byte load per token
+      float4 pv[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int i = i0 + q * kTopkThreads;
-      if (i < n)
-        v[q] = partial ? head_mean_score(partial + (R.score0 + i) * n_parts, n_parts, n_kv_heads)
-                       : score[R.score0 + i];
+      for (int q = 0; q < 4; ++q) {
+        const int i = i0 + q * kTopkThreads;
+        if (i < n) pv[q] = __ldg(reinterpret_cast<const float4*>(partial) + (R.score0 + i));
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (i0 + q * kTopkThreads < n) v[q] = head_mean_score4(pv[q], n_kv_heads);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int i = i0 + q * kTopkThreads;
+        if (i < n)
+          v[q] = partial ? head_mean_score(partial + (R.score0 + i) * n_parts, n_parts, n_kv_heads)
+                         : score[R.score0 + i];
+      }
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
