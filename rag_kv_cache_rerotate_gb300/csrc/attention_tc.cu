@@ -24,7 +24,7 @@
 //                        memory as an MN-major operand, O in TMEM columns
 //                        [384, 512)
 // The running maximum m is raised only when a block exceeds it by more than
-// 2^8 (then O and the running sum l are rescaled).  A separate warpgroup
+// 2^16 (then O and the running sum l are rescaled).  A separate warpgroup
 // writes O / l of a unit while the softmax starts on the next one (whose
 // first P.V waits until O has been read).
 // Roles, each behind its own mbarriers: warp 0 loads Q (two buffers, so the
@@ -61,7 +61,11 @@ constexpr int kThreads = 16 * 32;
 constexpr int kTmemCols = 512;                // S0 | S1 | S2 | O
 constexpr int kSBufs = 3;
 constexpr int kColO = 384;
-constexpr float kRescaleThreshold = 8.0f;     // log2 units
+// log2 units.  P is rounded to bf16 and summed in fp32 at the same relative
+// precision whatever its size, so a reference up to 2^16 below the true
+// maximum costs no accuracy (P, l and O stay far from overflow: at most
+// 2^16 x keys x |V|); a larger threshold means fewer O rescales.
+constexpr float kRescaleThreshold = 16.0f;
 // Reference maximum of a row none of whose keys so far was visible (log2
 // units): above every masked score (-1e30 * scale) and below every real one,
 // so masked probabilities are exactly 0 and the first visible block rescales
@@ -79,6 +83,7 @@ struct AttnArgs {
   int Hq, Hkv, g, rtile;
   float scale_log2;       // log2(e) / sqrt(d)
   uint32_t* err;
+  int st32;               // O 32-byte aligned: 256-bit stores
 };
 
 struct Ctl {
@@ -563,7 +568,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t r[32];
         tc::tmem_ld_32x32b_x32(tO + c, r);
         tc::tmem_ld_wait();
-        if (valid) {
+        if (valid && a.st32) {
+          // one 256-bit store per 16 values: the 32 bytes fill one sector
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(r[16 * q + 2 * e]) * inv,
+                                 __uint_as_float(r[16 * q + 2 * e + 1]) * inv);
+            asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + c + 16 * q),
+                         "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+                         "r"(w[7])
+                         : "memory");
+          }
+        } else if (valid) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint4 w;
@@ -659,6 +678,7 @@ cudaError_t launch_attention_tc(const fuse_layer_desc_t& d, const fuse_requests_
   a.rtile = rtile;
   a.scale_log2 = 1.4426950408889634f / sqrtf((float)kD);
   a.err = err;
+  a.st32 = (reinterpret_cast<uintptr_t>(O) & 31u) == 0;
   e = set_dyn_smem_once(reinterpret_cast<const void*>(attn_tc_kernel), kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = a.n_units < sm_count() ? a.n_units : sm_count();
