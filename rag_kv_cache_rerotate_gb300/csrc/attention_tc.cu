@@ -84,6 +84,7 @@ struct AttnArgs {
   float scale_log2;       // log2(e) / sqrt(d)
   uint32_t* err;
   int st32;               // O 32-byte aligned: 256-bit stores
+  int records_ready;      // tiles and rows complete before the previous kernel's release
 };
 
 struct Ctl {
@@ -227,7 +228,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   const int n_units = a.n_units;
+  // The first unit's tile record, and for the softmax threads the positions of
+  // their rows.  When the records come from a kernel that finished before the
+  // previous one could release its dependents, they are read before waiting.
+  const bool have0 = unit_at(0) < n_units;
+  int4 T0 = make_int4(0, 0, 1, 0);
+  int pos0[3] = {0, 0, 0};                          // softmax: rows R0, R1, the tile's first
+  auto first_records = [&]() {
+    if (!have0) return;
+    T0 = tile_of(a, unit_at(0));
+    if (warp >= kWarpSoft && warp < kWarpOut) {
+      const int R0 = (warp & 3) * 32 + ((warp - kWarpSoft) >> 2) * 16 + (lane >> 2);
+      pos0[0] = a.rows[T0.x + min(R0 / a.g, T0.z - 1)].pos;
+      pos0[1] = a.rows[T0.x + min((R0 + 8) / a.g, T0.z - 1)].pos;
+      pos0[2] = a.rows[T0.x].pos;
+    }
+  };
+  if (a.records_ready) first_records();
   pdl_wait();                 // inputs of the previous kernel complete and visible
+  if (!a.records_ready) first_records();
 
   if (warp == kWarpQK) {
     // --------------------------- Q and K loads ---------------------------
@@ -235,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t kc = 0;
       int i = 0;
       bool ok = true;
-      int4 T = unit_at(0) < n_units ? tile_of(a, unit_at(0)) : make_int4(0, 0, 0, 0);
+      int4 T = T0;
       for (; unit_at(i) < n_units && ok; ++i) {
         const int u = unit_at(i);
         const int4 cur = T;
@@ -274,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t vc = 0;
       bool ok = true;
-      int4 T = unit_at(0) < n_units ? tile_of(a, unit_at(0)) : make_int4(0, 0, 0, 0);
+      int4 T = T0;
       for (int i = 0; unit_at(i) < n_units && ok; ++i) {
         const int u = unit_at(i);
         const int4 cur = T;
@@ -303,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_s = tc::idesc_bf16_f32(128, kKB);
       uint32_t kc = 0, b = 0;
       bool ok = true;
-      int4 T = unit_at(0) < n_units ? tile_of(a, unit_at(0)) : make_int4(0, 0, 0, 0);
+      int4 T = T0;
       for (int i = 0; unit_at(i) < n_units && ok; ++i) {
         const int nkb = T.w;
         if (unit_at(i + 1) < n_units) T = tile_of(a, unit_at(i + 1));
@@ -346,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_o = tc::idesc_bf16_f32(128, kD, /*b_mn_major=*/true);
       uint32_t vc = 0, b = 0;
       bool ok = true;
-      int4 T = unit_at(0) < n_units ? tile_of(a, unit_at(0)) : make_int4(0, 0, 0, 0);
+      int4 T = T0;
       for (int i = 0; unit_at(i) < n_units && ok; ++i) {
         const int nkb = T.w;
         if (unit_at(i + 1) < n_units) T = tile_of(a, unit_at(i + 1));
@@ -394,13 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float scale = a.scale_log2;
     uint32_t b = 0;
     // this unit's record and positions, read one unit ahead
-    int4 T = unit_at(0) < n_units ? tile_of(a, unit_at(0)) : make_int4(0, 0, 1, 0);
-    int p0n = 0, p1n = 0, pfn = 0;
-    if (unit_at(0) < n_units) {
-      p0n = a.rows[T.x + min(rl0, T.z - 1)].pos;
-      p1n = a.rows[T.x + min(rl1, T.z - 1)].pos;
-      pfn = a.rows[T.x].pos;
-    }
+    int4 T = T0;
+    int p0n = pos0[0], p1n = pos0[1], pfn = pos0[2];
     for (int i = 0; unit_at(i) < n_units; ++i) {
       const int nkb = T.w;
       const int p0 = p0n, p1 = p1n;
@@ -544,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int rl = m / a.g;
     const int hh = m % a.g;
-    int4 T = unit_at(0) < n_units ? tile_of(a, unit_at(0)) : make_int4(0, 0, 0, 0);
+    int4 T = T0;
     for (int i = 0; unit_at(i) < n_units; ++i) {
       const int u = unit_at(i);
       const int4 cur = T;
@@ -679,6 +693,10 @@ cudaError_t launch_attention_tc(const fuse_layer_desc_t& d, const fuse_requests_
   a.scale_log2 = 1.4426950408889634f / sqrtf((float)kD);
   a.err = err;
   a.st32 = (reinterpret_cast<uintptr_t>(O) & 31u) == 0;
+  // the tile records and row tables come from the row preparation, which
+  // finished before the QKV projection (launched after it) let this kernel
+  // start; otherwise the tile kernel launched just above is still running
+  a.records_ready = tiles_ready ? 1 : 0;
   e = set_dyn_smem_once(reinterpret_cast<const void*>(attn_tc_kernel), kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = a.n_units < sm_count() ? a.n_units : sm_count();

@@ -283,6 +283,31 @@ def test_layer_step(name):
     _recompute_and_compare(case, b, idx)
 
 
+def _offset16(t):
+    """A copy of t whose storage starts 16 bytes past a 256-byte boundary:
+    aligned as the ABI requires (16 bytes) but not to 32 bytes."""
+    flat = torch.zeros(t.numel() * t.element_size() + 256, dtype=torch.uint8, device=t.device)
+    base = (-flat.data_ptr()) % 256 + 16
+    v = flat[base:base + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+    v.copy_(t)
+    assert v.data_ptr() % 32 == 16
+    return v
+
+
+# The Q/K/V scatter and the attention output use 256-bit stores when their
+# destinations are 32-byte aligned; fused caches and O that are only 16-byte
+# aligned take the 16-byte stores instead and must give the same results.
+@pytest.mark.parametrize("name", ["qwen3_8b_layer", "sparse_long_bf16"])
+def test_layer_step_16_byte_aligned_outputs(name):
+    case = case_of(name)
+    b = buffers(case)
+    b.Kf, b.Vf, b.O = _offset16(b.Kf), _offset16(b.Vf), _offset16(b.O)
+    fk.layer_step(b.desc, b.chunks, b.reqs, b.H, b.Wq, b.Wk, b.Wv, True, b.idx, b.Kf, b.Vf, b.O,
+                  b.score, b.ws)
+    fk.check_errors(b.ws)
+    _recompute_and_compare(case, b, b.idx.cpu().numpy())
+
+
 @pytest.mark.parametrize("ratio", [0.0, 1.0])
 def test_ratio_endpoints(ratio):
     cfg = synth.scaled(C["tiny_fp32"], ratio=ratio)
