@@ -197,26 +197,78 @@ __host__ __device__ inline int64_t rope_index(int j, int64_t m, int64_t n_rows) 
 // (first output row, the request's first fused row, rows, key blocks), the
 // key blocks being those up to the position of the tile's last row (selected
 // index, clamped to the request like the row tables, or n_ctx + query row).
-// Run by every thread of one block (the caller's branch must be block-uniform).
+// Run by every thread of one block of a multiple of 32 threads, at most 1024
+// (the caller's branch must be block-uniform); requests past kTileReqsSmem
+// are enumerated by one thread (slower, same result).
+constexpr int kTileReqsSmem = 1024;
 __device__ inline void build_attn_tiles(const fuse_request_t* reqs, int n_req, const int32_t* idx,
                                         int rtile, int4* tiles) {
-  __shared__ int s_nt;
-  if (threadIdx.x == 0) {
-    int nt = 0;
-    for (int q = 0; q < n_req; ++q) {
-      const int n = reqs[q].k + reqs[q].n_query;
-      for (int r0 = 0; r0 < n; r0 += rtile) tiles[nt++] = make_int4(q, r0, min(rtile, n - r0), 0);
+  __shared__ int s_first[kTileReqsSmem + 1];     // first tile of each request, then the total
+  __shared__ int s_warp[32];
+  const int tid = threadIdx.x, nth = blockDim.x;
+  if (n_req > kTileReqsSmem) {
+    if (tid == 0) {
+      int nt = 0;
+      for (int q = 0; q < n_req; ++q) {
+        const int n = reqs[q].k + reqs[q].n_query;
+        for (int r0 = 0; r0 < n; r0 += rtile) tiles[nt++] = make_int4(q, r0, min(rtile, n - r0), 0);
+      }
+      s_first[0] = nt;
     }
-    s_nt = nt;
+    __syncthreads();
+    const int nt = s_first[0];
+    for (int t = tid; t < nt; t += nth) {
+      const int4 x = tiles[t];
+      const fuse_request_t R = reqs[x.x];
+      const int o = x.y + x.z - 1;
+      const int pos = o < R.k ? min(max(idx[R.sel0 + o], 0), max(R.n_ctx - 1, 0)) : R.n_ctx + (o - R.k);
+      tiles[t] = make_int4((int)R.out0 + x.y, (int)R.row0, x.z, pos / 128 + 1);
+    }
+    return;
   }
+  // tiles per request, and their running sum, blockDim requests at a time
+  const int lane = tid % 32, warp = tid / 32, nw = nth / 32;
+  int carry = 0;                                 // block-uniform
+  for (int q0 = 0; q0 < n_req; q0 += nth) {
+    const int q = q0 + tid;
+    const int cnt = q < n_req ? (reqs[q].k + reqs[q].n_query + rtile - 1) / rtile : 0;
+    int x = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int w = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      s_warp[lane] = w;
+    }
+    __syncthreads();
+    if (q < n_req) s_first[q] = carry + (warp > 0 ? s_warp[warp - 1] : 0) + x - cnt;
+    carry += s_warp[nw - 1];
+    __syncthreads();                             // s_warp is rewritten by the next chunk
+  }
+  if (tid == 0) s_first[n_req] = carry;
   __syncthreads();
-  const int nt = s_nt;
-  for (int t = threadIdx.x; t < nt; t += blockDim.x) {
-    const int4 x = tiles[t];
-    const fuse_request_t R = reqs[x.x];
-    const int o = x.y + x.z - 1;
+  const int nt = s_first[n_req];
+  for (int t = tid; t < nt; t += nth) {
+    int lo = 0, hi = n_req - 1;                  // the request: last q with s_first[q] <= t
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_first[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    const fuse_request_t R = reqs[lo];
+    const int r0 = (t - s_first[lo]) * rtile;
+    const int rows = min(rtile, R.k + R.n_query - r0);
+    const int o = r0 + rows - 1;
     const int pos = o < R.k ? min(max(idx[R.sel0 + o], 0), max(R.n_ctx - 1, 0)) : R.n_ctx + (o - R.k);
-    tiles[t] = make_int4((int)R.out0 + x.y, (int)R.row0, x.z, pos / 128 + 1);
+    tiles[t] = make_int4((int)R.out0 + r0, (int)R.row0, rows, pos / 128 + 1);
   }
 }
 #endif
