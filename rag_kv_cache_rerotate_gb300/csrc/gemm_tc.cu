@@ -311,6 +311,22 @@ __device__ __forceinline__ void epi_recompute(const TcArgs& a, uint32_t taddr, i
   }
 }
 
+// B tensor map and first row of head `head` (the heads of map 0, then 1, then 2).
+__device__ __forceinline__ void b_map_of(const TcArgs& a, int head, const CUtensorMap* m0,
+                                         const CUtensorMap* m1, const CUtensorMap* m2,
+                                         const CUtensorMap*& mb, int& nrow) {
+  if (head < a.h0) {
+    mb = m0;
+    nrow = head * BN;
+  } else if (head < a.h0 + a.h1) {
+    mb = m1;
+    nrow = (head - a.h0) * BN;
+  } else {
+    mb = m2;
+    nrow = (head - a.h0 - a.h1) * BN;
+  }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB0,
@@ -349,10 +365,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::cluster_sync_all();      // both CTAs' barriers exist before any remote arrival
   tc::tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
-  pdl_wait();                 // inputs of the previous kernel complete and visible
-  // the next kernel may start once every CTA is here: the kernels before this
-  // one are complete by now (a stitch launched next may write the fused cache)
-  pdl_trigger();
+  // The TMA producer requests the weights (B) of its first stages before
+  // waiting on the previous kernel (they are the caller's inputs); every other
+  // thread waits first.  Each thread lets the next kernel start only after its
+  // own wait: the kernels before this one are then complete (a stitch launched
+  // next may write the fused cache; the attention reads the row tables).
+  const bool producer = warp == 0 && lane == 0;
+  if (!producer) {
+    pdl_wait();               // inputs of the previous kernel complete and visible
+    pdl_trigger();
+  }
 
   if (warp == 0) {
     // ---------------- TMA producer: this CTA's A rows and its head's B rows ----------------
@@ -364,22 +386,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t armed_ph[STAGES];
       for (int i = 0; i < STAGES; ++i) armed[i] = false;
       bool ok = true;
+      // B of the first tile's first stages, before the wait
+      int pre = 0;
+      if (pair < total) {
+        const int head = 2 * (pair / a.m_tiles) + (int)rank;
+        const CUtensorMap* mb;
+        int nrow;
+        b_map_of(a, head, &mapB0, &mapB1, &mapB2, mb, nrow);
+        pre = k_blocks < STAGES ? k_blocks : STAGES;
+        for (int kb = 0; kb < pre; ++kb) {          // stage kb, first use: no wait for it
+          uint8_t* sa = smem + kb * kStageBytes;
+          if (rank == 0) {
+            tc::mbar_arrive_expect_tx(&ctl->full[kb], 2 * kStageBytes);
+            tc::tma_load_2d(sa + kTileBytes, mb, &ctl->full[kb], kb * BK, nrow);
+          } else {
+            tc::tma_load_2d_pair(sa + kTileBytes, mb, leader_full + kb * (uint32_t)sizeof(uint64_t),
+                                 kb * BK, nrow);
+          }
+        }
+      }
+      pdl_wait();
+      pdl_trigger();
       for (int tile = pair; tile < total && ok; tile += n_pairs) {
         const int mt = tile % a.m_tiles;
         const int nt = tile / a.m_tiles;
         const int head = 2 * nt + (int)rank;
         const CUtensorMap* mb;
         int nrow;
-        if (head < a.h0) {
-          mb = &mapB0;
-          nrow = head * BN;
-        } else if (head < a.h0 + a.h1) {
-          mb = &mapB1;
-          nrow = (head - a.h0) * BN;
-        } else {
-          mb = &mapB2;
-          nrow = (head - a.h0 - a.h1) * BN;
-        }
+        b_map_of(a, head, &mapB0, &mapB1, &mapB2, mb, nrow);
         const int arow = mt * BMP + (int)rank * BM;
         for (int kb = 0; kb < k_blocks; ++kb) {
           if (!wait_or_abort(&ctl->empty[s], ph ^ 1, ctl)) {
@@ -388,15 +422,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           uint8_t* sa = smem + s * kStageBytes;
+          const bool b_done = tile == pair && kb < pre;   // armed and B requested above
           if (rank == 0) {
             // the stage is full once both CTAs' bytes have landed
-            tc::mbar_arrive_expect_tx(&ctl->full[s], 2 * kStageBytes);
+            if (!b_done) tc::mbar_arrive_expect_tx(&ctl->full[s], 2 * kStageBytes);
             tc::tma_load_2d(sa, &mapA, &ctl->full[s], kb * BK, arow);
-            tc::tma_load_2d(sa + kTileBytes, mb, &ctl->full[s], kb * BK, nrow);
+            if (!b_done) tc::tma_load_2d(sa + kTileBytes, mb, &ctl->full[s], kb * BK, nrow);
           } else {
             const uint32_t lf = leader_full + s * (uint32_t)sizeof(uint64_t);
             tc::tma_load_2d_pair(sa, &mapA, lf, kb * BK, arow);
-            tc::tma_load_2d_pair(sa + kTileBytes, mb, lf, kb * BK, nrow);
+            if (!b_done) tc::tma_load_2d_pair(sa + kTileBytes, mb, lf, kb * BK, nrow);
           }
           armed[s] = true;
           armed_ph[s] = ph;
