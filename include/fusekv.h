@@ -302,6 +302,37 @@ fuse_status_t fuse_check_errors(void* ws, fuse_stream_t stream, uint32_t* detail
 fuse_status_t fuse_select_topk_noalloc(const fuse_requests_t* reqs, const float* score,
                                        int32_t* idx, fuse_stream_t stream);
 
+/* Static selectors: indices generated from the chunk layout alone, no
+ * scores (the query-agnostic selectors of the "Token Selection" related-work
+ * section of the QCFuse page, and SelectiveRecompute, "Seam Repair" section
+ * of the KVBoost page).  A request's context is the concatenation of the
+ * chunks whose fused rows lie in [row0, row0 + N_r); a chunk starts at
+ * position s = dst_row - row0 of its request.
+ *   FUSE_SEL_CHUNK_HEAD: the first n tokens of every chunk, [s, s + min(n, len))
+ *     (EPIC's LegoLink rule: the first tokens of a stitched chunk act as
+ *     attention sinks; the page gives no count, so n is a parameter).
+ *   FUSE_SEL_SEAM_TAIL: the n tokens before every seam, [max(0, p - n), p)
+ *     for each p = s of a chunk that is not the request's first (a seam is
+ *     where two chunks join; the page's default is n = 16).
+ * The selection of a request is the union of its ranges, ascending.
+ * Requirements (else FUSE_ERR_INVALID_ARG): host mirrors of both tables;
+ * chunks sorted by dst_row and non-overlapping; every chunk with len > 0
+ * inside exactly one request's context rows; n >= 0. */
+typedef enum { FUSE_SEL_CHUNK_HEAD = 0, FUSE_SEL_SEAM_TAIL = 1 } fuse_static_sel_t;
+
+/* Host only, no launch: k_out[r] = size of request r's selection (host array
+ * of n_req entries), to be written into the request table's k before
+ * fuse_static_select. */
+fuse_status_t fuse_static_select_count(const fuse_requests_t* reqs, const fuse_chunks_t* chunks,
+                                       int32_t kind, int32_t n, int32_t* k_out);
+
+/* Enqueues one kernel that writes each request's selection, ascending, to
+ * idx[sel0 .. sel0 + k_r) (device array).  reqs->h_req[r].k must equal the
+ * count of fuse_static_select_count (else FUSE_ERR_INVALID_ARG).  The
+ * indices feed fuse_recompute_selected like those of fuse_select_topk. */
+fuse_status_t fuse_static_select(const fuse_requests_t* reqs, const fuse_chunks_t* chunks,
+                                 int32_t kind, int32_t n, int32_t* idx, fuse_stream_t stream);
+
 /* Kernel timing trace (no counterpart on the pages; a measurement aid).
  * fuse_trace_begin(n) creates n pairs of CUDA events and, until
  * fuse_trace_end, records one pair around each kernel the library launches,

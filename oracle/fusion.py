@@ -18,8 +18,8 @@ Sources (page title, then section / equation):
 * KVBoost: Chunk-Level KV Cache Reuse with Deviation-Guided Recomputation --
   section 3.1 (Eqs. 1-2, projections and causal attention), section 3.2
   (Eq. 3, RoPE and its relative-offset property), section 4.5 (Eq. 7, KIVI
-  asymmetric quantisation), section 4.6.2 (Alg. 2, deviation -> top-k ->
-  patch).
+  asymmetric quantisation), section 4.6.1 (Alg. 1, SelectiveRecompute seam
+  windows), section 4.6.2 (Alg. 2, deviation -> top-k -> patch).
 
 Readings taken where the pages leave a step open:
 
@@ -240,6 +240,30 @@ def select_topk(score: np.ndarray, k: int) -> np.ndarray:
         raise ValueError("k out of range")
     order = np.lexsort((np.arange(n), -s))   # primary: larger score; then lower index
     return np.sort(order[:k]).astype(np.int64)
+
+
+def static_select(chunk_starts: Sequence[int], chunk_lens: Sequence[int], n_ctx: int,
+                  kind: str, n: int) -> np.ndarray:
+    """Positions of one request chosen from its chunk layout alone, ascending.
+
+    kind "chunk_head" (QCFuse, related work on query-agnostic selection: EPIC
+    recomputes a fixed number of boundary tokens of every stitched chunk,
+    the first tokens of a chunk acting as attention sinks): the first n
+    positions of every chunk.  kind "seam_tail" (KVBoost section 4.6.1,
+    SelectiveRecompute): for every seam p -- the start of a chunk that follows
+    another chunk -- the positions max(0, p - n) .. p - 1.  Chunks are given
+    in position order; the selection is the union, read off a mask over the
+    request's positions."""
+    mask = np.zeros(n_ctx, dtype=bool)
+    for c, (s, ln) in enumerate(zip(chunk_starts, chunk_lens)):
+        if kind == "chunk_head":
+            mask[s:s + min(n, ln)] = True
+        elif kind == "seam_tail":
+            if c > 0:
+                mask[max(0, s - n):s] = True
+        else:
+            raise ValueError(kind)
+    return np.nonzero(mask)[0].astype(np.int64)
 
 
 def selected_rows(idx: np.ndarray, n_ctx: int, n_tok: int) -> np.ndarray:

@@ -104,6 +104,8 @@ _SIGS = {
     "fuse_pic_precompute": (_c.c_int, [_P, _P, _P, _P, _P, _P, _c.c_size_t, _P]),
     "fuse_stack_step": (_c.c_int, [_P, _P, _c.c_int32, _c.c_int32, _P, _P, _P, _P, _c.c_size_t, _P]),
     "fuse_check_errors": (_c.c_int, [_P, _P, _c.POINTER(_c.c_uint32)]),
+    "fuse_static_select_count": (_c.c_int, [_P, _P, _c.c_int32, _c.c_int32, _P]),
+    "fuse_static_select": (_c.c_int, [_P, _P, _c.c_int32, _c.c_int32, _P, _P]),
     "fuse_trace_begin": (_c.c_int, [_c.c_int32]),
     "fuse_trace_end": (_c.c_int, [_P, _c.c_int32, _c.POINTER(_c.c_int32)]),
     "fuse_status_string": (_c.c_char_p, [_c.c_int]),
@@ -254,6 +256,34 @@ def score_deviation(desc, reqs: RequestTable, H, Wv, Vf, score, ws, stream=None)
     _check(load().fuse_score_deviation(_c.byref(desc), _c.byref(reqs.c), _ptr(H), _ptr(Wv),
                                        _ptr(Vf), _ptr(score), _ptr(ws), ws.numel(),
                                        _stream(stream)), "fuse_score_deviation")
+
+
+SEL_CHUNK_HEAD, SEL_SEAM_TAIL = 0, 1
+
+
+def static_select_count(reqs: RequestTable, chunks: ChunkTable, kind: int, n: int) -> list:
+    """k_r of the static selector `kind` (SEL_CHUNK_HEAD / SEL_SEAM_TAIL) per request."""
+    k = (_c.c_int32 * max(1, reqs.n))()
+    _check(load().fuse_static_select_count(_c.byref(reqs.c), _c.byref(chunks.c), int(kind), int(n),
+                                           k), "fuse_static_select_count")
+    return [int(x) for x in k[:reqs.n]]
+
+
+def static_select(reqs: RequestTable, chunks: ChunkTable, kind: int, n: int, idx, stream=None):
+    _check(load().fuse_static_select(_c.byref(reqs.c), _c.byref(chunks.c), int(kind), int(n),
+                                     _ptr(idx), _stream(stream)), "fuse_static_select")
+
+
+def requests_with_k(reqs: RequestTable, k: Sequence[int], device="cuda") -> RequestTable:
+    """The same requests with k_r replaced, idx and O offsets packed again in
+    request order."""
+    out, sel, row = [], 0, 0
+    for r, kr in zip(reqs.host[: reqs.n], k):
+        q = Request(r.row0, r.score0, sel, row, r.n_ctx, r.n_query, int(kr), 0)
+        sel += int(kr)
+        row += int(kr) + r.n_query
+        out.append(q)
+    return RequestTable(out, device=device)
 
 
 def select_topk(reqs: RequestTable, score, idx, ws, stream=None):

@@ -135,3 +135,54 @@ def test_struct_layouts_match_header(fk):
     assert ctypes.sizeof(fk.Request) == 48
     assert ctypes.sizeof(fk.Requests) == 24
     assert ctypes.sizeof(fk.Totals) == 40
+
+
+def _static_layout(fk, seed):
+    """Five requests of 1-6 chunks (1-59 tokens each) and 0-8 query rows,
+    packed back to back, with host-only tables."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    reqs, chunks, layouts, row = [], [], [], 0
+    for _ in range(5):
+        lens = [int(x) for x in rng.integers(1, 60, size=int(rng.integers(1, 7)))]
+        starts = [sum(lens[:i]) for i in range(len(lens))]
+        n_ctx, nq = sum(lens), int(rng.integers(0, 9))
+        for s0, ln in zip(starts, lens):
+            e = fk.Chunk()
+            e.dst_row, e.pos, e.len = row + s0, s0, ln
+            chunks.append(e)
+        reqs.append(fk.Request(row, 0, 0, 0, n_ctx, nq, 0, 0))
+        layouts.append((starts, lens, n_ctx))
+        row += n_ctx + nq
+    return (fk.RequestTable(reqs, device=None), fk.ChunkTable(chunks, 0, 1, device=None), layouts)
+
+
+@pytest.mark.parametrize("kind,name", [(0, "chunk_head"), (1, "seam_tail")])
+def test_static_select_count_matches_oracle(fk, kind, name):
+    from oracle import fusion as orc
+    for seed in range(4):
+        rt, ct, layouts = _static_layout(fk, 11 * seed + kind)
+        for n in (0, 1, 3, 16, 100):
+            want = [len(orc.static_select(s, l, nc, name, n)) for s, l, nc in layouts]
+            assert fk.static_select_count(rt, ct, kind, n) == want
+
+
+def test_static_select_rejects_bad_tables(fk):
+    rt, ct, layouts = _static_layout(fk, 5)
+    with pytest.raises(fk.FuseError):
+        fk.static_select_count(rt, ct, 2, 16)                        # unknown kind
+    with pytest.raises(fk.FuseError):
+        fk.static_select_count(rt, ct, 0, -1)                        # negative n
+    entries = list(ct.entries)
+    entries[0], entries[1] = entries[1], entries[0]                  # not sorted by row
+    with pytest.raises(fk.FuseError):
+        fk.static_select_count(rt, fk.ChunkTable(entries, 0, 1, device=None), 0, 4)
+    orphan = fk.Chunk()
+    orphan.dst_row, orphan.len = 10 ** 9, 4                          # outside every request
+    with pytest.raises(fk.FuseError):
+        fk.static_select_count(rt, fk.ChunkTable(list(ct.entries) + [orphan], 0, 1, device=None), 0, 4)
+    # k of the request table must equal the count (checked before any launch)
+    k = fk.static_select_count(rt, ct, 1, 16)
+    wrong = fk.requests_with_k(rt, [x + 1 for x in k], device=None)
+    with pytest.raises(fk.FuseError):
+        fk.static_select(wrong, ct, 1, 16, None)

@@ -498,3 +498,31 @@ def test_layer_step_scores_and_selection_consistent():
     assert sc[idx].min() >= sc[unsel].max()
     # the most perturbed tokens deviate most
     assert np.corrcoef(np.argsort(np.argsort(e[:30])), np.argsort(np.argsort(sc)))[0, 1] > 0.5
+
+
+# Static selectors (QCFuse related work, EPIC boundary tokens; KVBoost 4.6.1,
+# SelectiveRecompute seam windows)
+def test_static_select_hand_worked():
+    # chunks of 5, 3 and 4 tokens at positions 0, 5 and 8
+    s, l = [0, 5, 8], [5, 3, 4]
+    assert orc.static_select(s, l, 12, "chunk_head", 2).tolist() == [0, 1, 5, 6, 8, 9]
+    assert orc.static_select(s, l, 12, "chunk_head", 4).tolist() == [0, 1, 2, 3, 5, 6, 7, 8, 9, 10, 11]
+    assert orc.static_select(s, l, 12, "seam_tail", 2).tolist() == [3, 4, 6, 7]
+    # windows overlap and reach back across a short chunk; the start clamps at 0
+    assert orc.static_select(s, l, 12, "seam_tail", 4).tolist() == [1, 2, 3, 4, 5, 6, 7]
+    assert orc.static_select(s, l, 12, "seam_tail", 9).tolist() == list(range(8))
+    assert orc.static_select(s, l, 12, "seam_tail", 0).tolist() == []
+    assert orc.static_select([0], [12], 12, "seam_tail", 16).tolist() == []   # one chunk: no seam
+
+
+def test_static_select_counts_from_the_pages():
+    # KVBoost 4.6.1: R = 16 and two seams in a 512-token prompt: 32 tokens
+    assert len(orc.static_select([0, 170, 340], [170, 170, 172], 512, "seam_tail", 16)) == 32
+    # chunk heads: every chunk contributes min(n, len) positions
+    rng = np.random.default_rng(3)
+    lens = rng.integers(0, 40, size=20)
+    starts = np.concatenate([[0], np.cumsum(lens)[:-1]])
+    for n in (0, 1, 7, 64):
+        got = orc.static_select(starts, lens, int(lens.sum()), "chunk_head", n)
+        assert len(got) == int(np.minimum(lens, n).sum())
+        assert np.all(np.diff(got) > 0)
