@@ -66,7 +66,7 @@ typedef enum {
                                  of range or out of order; the access was skipped  */
 } fuse_status_t;
 
-typedef enum { FUSE_F32 = 0, FUSE_BF16 = 1, FUSE_U8_ASYM = 2 } fuse_dtype_t;
+typedef enum { FUSE_F32 = 0, FUSE_BF16 = 1, FUSE_U8_ASYM = 2, FUSE_U4_ASYM = 3 } fuse_dtype_t;
 typedef enum { FUSE_KV_CONTIGUOUS = 0, FUSE_KV_PAGED = 1 } fuse_kv_layout_t;
 typedef enum { FUSE_ROPE_ROTATE_HALF = 0 } fuse_pos_encoding_t;
 
@@ -101,6 +101,10 @@ typedef struct {
  *               k_scale, k_zero  [Hkv, d]  per channel over the chunk's tokens;
  *               v_scale, v_zero  [len, Hkv] per token (CONTIGUOUS) or
  *                                [n_blocks, block_size, Hkv] (PAGED pool).
+ *   U4_ASYM     the same with 4-bit codes 0..15 (KIVI's b = 4), two per byte:
+ *               element 2m of a row in the low nibble of byte m, 2m + 1 in
+ *               the high nibble, so k and v arrays (and the pool) hold d / 2
+ *               bytes per (token, head); scale and zero as for U8_ASYM.
  *   For fuse_pic_precompute, k and v are outputs (CONTIGUOUS F32/BF16 only). */
 typedef struct {
   const void* k;
@@ -191,7 +195,8 @@ fuse_status_t fuse_workspace_reset(void* ws, size_t ws_bytes, fuse_stream_t stre
  * of [KVBoost] section 3.2: for every chunk i and local row r < len_i,
  *   Kf[dst_row_i + r] = R^{pos_i} K_i[r]     (keys re-rotated by the offset)
  *   Vf[dst_row_i + r] = V_i[r]               (values copied in token order)
- * after dequantisation when kv_storage is FUSE_U8_ASYM ([KVBoost] Eq. 7).
+ * after dequantisation when kv_storage is FUSE_U8_ASYM or FUSE_U4_ASYM
+ * ([KVBoost] Eq. 7).
  * A chunk with pos 0 whose storage type equals desc->dtype is copied bit for
  * bit.  Kf, Vf: [fused_rows, Hkv, d] in desc->dtype; every chunk must satisfy
  * dst_row + len <= fused_rows.  Query rows are not touched. */

@@ -116,10 +116,11 @@ fuse_status_t check_chunks(const fuse_layer_desc_t& d, const fuse_chunks_t* c, i
   *max_len = 0;
   if (c->kv_layout != FUSE_KV_CONTIGUOUS && c->kv_layout != FUSE_KV_PAGED)
     return FUSE_ERR_INVALID_ARG;
-  if (c->kv_storage != FUSE_F32 && c->kv_storage != FUSE_BF16 && c->kv_storage != FUSE_U8_ASYM)
+  if (c->kv_storage != FUSE_F32 && c->kv_storage != FUSE_BF16 && c->kv_storage != FUSE_U8_ASYM &&
+      c->kv_storage != FUSE_U4_ASYM)
     return FUSE_ERR_INVALID_ARG;
   const bool paged = c->kv_layout == FUSE_KV_PAGED;
-  const bool u8 = c->kv_storage == FUSE_U8_ASYM;
+  const bool u8 = c->kv_storage == FUSE_U8_ASYM || c->kv_storage == FUSE_U4_ASYM;   // quantised
   if (paged && (c->block_size <= 0 || c->n_pool_blocks <= 0)) return FUSE_ERR_INVALID_ARG;
   if (c->n_chunks == 0) return FUSE_OK;
   if (!c->h_chunks || !c->d_chunks) return FUSE_ERR_INVALID_ARG;

@@ -1,4 +1,4 @@
-// Stitch + RoPE re-rotation (+ KIVI int8 dequantisation, + paged gather).
+// Stitch + RoPE re-rotation (+ KIVI int8 / int4 dequantisation, + paged gather).
 //
 // QCFuse (section 2.1.2, Eq. 4): chunk caches built alone at local positions
 // are placed at their request positions; keys are remapped by the chunk's
@@ -18,6 +18,7 @@
 // loads before anything else.  Either way the chunk offset's (cos, sin) of the
 // d/2 frequencies are computed once per CTA (and chunk) into shared memory.
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
@@ -43,6 +44,17 @@ template <> struct Src8<__nv_bfloat16> {
     Vec8<__nv_bfloat16>::load(reinterpret_cast<const __nv_bfloat16*>(base) + e, x);
   }
 };
+// Four-bit codes packed two per byte (element 2m in the low nibble of byte
+// m): the tag type of the kernel's source argument.
+struct Nibbles {
+  uint8_t b;
+};
+// 8 four-bit codes from element e (a multiple of 8: 4 bytes at byte e / 2).
+__device__ __forceinline__ void load_u4(const void* base, int64_t e, float (&x)[8]) {
+  const uint32_t q = __ldg(reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(base) + e / 2));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) x[i] = (float)((q >> (4 * i)) & 0xFu);
+}
 // uint8 codes, dequantised with 8 per-element (scale, zero) pairs.
 __device__ __forceinline__ void load_u8(const void* base, int64_t e, float (&x)[8]) {
   uint2 q = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const uint8_t*>(base) + e));
@@ -103,7 +115,8 @@ __global__ void __launch_bounds__(kStitchThreads) stitch_kernel(const StitchArgs
   constexpr int H2 = D / 2;
   constexpr int PG = H2 / 8;           // 8-pair groups per head (K)
   constexpr int VG = D / 8;            // 8-element groups per head (V)
-  constexpr bool kU8 = sizeof(TS) == 1;
+  constexpr bool kU4 = std::is_same<TS, Nibbles>::value;
+  constexpr bool kU8 = std::is_same<TS, uint8_t>::value || kU4;   // quantised codes
   constexpr bool kSame = sizeof(TS) == sizeof(TO) && !kU8;
   pdl_trigger();
   pdl_wait();
@@ -137,7 +150,10 @@ __global__ void __launch_bounds__(kStitchThreads) stitch_kernel(const StitchArgs
         report_error(a.err, FUSE_ERR_DEVICE_BOUNDS, SITE_STITCH_BLOCK, chunk);
       } else {
         k_ok[q] = true;
-        if constexpr (kU8) {
+        if constexpr (kU4) {
+          load_u4(c.k, e, kx[q]);
+          load_u4(c.k, e + H2, ky[q]);
+        } else if constexpr (kU8) {
           load_u8(c.k, e, kx[q]);
           load_u8(c.k, e + H2, ky[q]);
         } else {
@@ -161,7 +177,9 @@ __global__ void __launch_bounds__(kStitchThreads) stitch_kernel(const StitchArgs
         report_error(a.err, FUSE_ERR_DEVICE_BOUNDS, SITE_STITCH_BLOCK, chunk);
       } else {
         v_ok[q] = true;
-        if constexpr (kU8)
+        if constexpr (kU4)
+          load_u4(c.v, e, vx[q]);
+        else if constexpr (kU8)
           load_u8(c.v, e, vx[q]);
         else
           Src8<TS>::load(c.v, e, vx[q]);
@@ -489,6 +507,9 @@ cudaError_t launch_stitch(const fuse_layer_desc_t& desc, const fuse_chunks_t& ch
     case FUSE_BF16:
       return out_bf16 ? launch_d<__nv_bfloat16, __nv_bfloat16>(a, chunks.n_chunks, D, paged, s)
                       : launch_d<__nv_bfloat16, float>(a, chunks.n_chunks, D, paged, s);
+    case FUSE_U4_ASYM:
+      return out_bf16 ? launch_d<Nibbles, __nv_bfloat16>(a, chunks.n_chunks, D, paged, s)
+                      : launch_d<Nibbles, float>(a, chunks.n_chunks, D, paged, s);
     default:
       return out_bf16 ? launch_d<uint8_t, __nv_bfloat16>(a, chunks.n_chunks, D, paged, s)
                       : launch_d<uint8_t, float>(a, chunks.n_chunks, D, paged, s);

@@ -29,7 +29,7 @@ FUSE_ERR_TIMEOUT = 6
 FUSE_ERR_DEVICE_BOUNDS = 7
 
 # fuse_dtype_t, fuse_kv_layout_t, fuse_pos_encoding_t
-FUSE_F32, FUSE_BF16, FUSE_U8_ASYM = 0, 1, 2
+FUSE_F32, FUSE_BF16, FUSE_U8_ASYM, FUSE_U4_ASYM = 0, 1, 2, 3
 FUSE_KV_CONTIGUOUS, FUSE_KV_PAGED = 0, 1
 FUSE_ROPE_ROTATE_HALF = 0
 

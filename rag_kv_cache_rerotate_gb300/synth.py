@@ -38,7 +38,7 @@ class FusionConfig:
     head_dim: int
     rope_base: float
     dtype: str                    # "f32" or "bf16": activations, weights, fused cache
-    kv_storage: str               # "f32", "bf16" or "u8" (KIVI asymmetric int8)
+    kv_storage: str               # "f32", "bf16", "u8" or "u4" (KIVI asymmetric int8 / int4)
     kv_layout: str                # "contiguous" or "paged"
     ratio: float                  # recompute ratio rho
     w_std: float                  # std of the projection weights

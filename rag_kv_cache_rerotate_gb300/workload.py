@@ -17,8 +17,8 @@ import torch
 from . import fusekv as fk
 from .synth import FusionConfig, RequestLayout, chunk_token_rows, draw_block_permutation
 
-_TORCH = {"f32": torch.float32, "bf16": torch.bfloat16, "u8": torch.uint8}
-_FUSE = {"f32": fk.FUSE_F32, "bf16": fk.FUSE_BF16, "u8": fk.FUSE_U8_ASYM}
+_TORCH = {"f32": torch.float32, "bf16": torch.bfloat16, "u8": torch.uint8, "u4": torch.uint8}
+_FUSE = {"f32": fk.FUSE_F32, "bf16": fk.FUSE_BF16, "u8": fk.FUSE_U8_ASYM, "u4": fk.FUSE_U4_ASYM}
 
 
 def desc_of(cfg: FusionConfig) -> fk.LayerDesc:
@@ -71,7 +71,7 @@ def _contiguous_storage(cfg, rows, caches: ChunkCaches, device):
     Kst = caches.K.to(device).contiguous()
     Vst = caches.V.to(device).contiguous()
     store = {"K": Kst, "V": Vst}
-    quant = cfg.kv_storage == "u8"
+    quant = cfg.kv_storage in ("u8", "u4")
     if quant:
         for name in ("k_scale", "k_zero", "v_scale", "v_zero"):
             store[name] = getattr(caches, name).to(device).contiguous()
@@ -105,9 +105,10 @@ def _paged_storage(cfg, rows, caches: ChunkCaches, device, layer=0):
     perm = draw_block_permutation(cfg, n_blocks, layer)
     Hkv, d = cfg.n_kv_heads, cfg.head_dim
     dt = caches.K.dtype
-    Kpool = torch.zeros(n_blocks, bs, Hkv, d, dtype=dt, device=device)
-    Vpool = torch.zeros(n_blocks, bs, Hkv, d, dtype=dt, device=device)
-    quant = cfg.kv_storage == "u8"
+    dk = caches.K.shape[-1]               # d, or d / 2 bytes of packed 4-bit codes
+    Kpool = torch.zeros(n_blocks, bs, Hkv, dk, dtype=dt, device=device)
+    Vpool = torch.zeros(n_blocks, bs, Hkv, dk, dtype=dt, device=device)
+    quant = cfg.kv_storage in ("u8", "u4")
     store = {"K": Kpool, "V": Vpool}
     if quant:
         store["k_scale"] = caches.k_scale.to(device).contiguous()
@@ -124,8 +125,8 @@ def _paged_storage(cfg, rows, caches: ChunkCaches, device, layer=0):
         slots.append(perm[b0 + r // bs].to(torch.int64) * bs + r % bs)
         b0 += nblk_per[ci]
     slots = torch.cat(slots).to(device) if slots else torch.zeros(0, dtype=torch.int64, device=device)
-    Kpool.view(-1, Hkv, d)[slots] = K
-    Vpool.view(-1, Hkv, d)[slots] = V
+    Kpool.view(-1, Hkv, dk)[slots] = K
+    Vpool.view(-1, Hkv, dk)[slots] = V
     if quant:
         store["v_scale"].view(-1, Hkv)[slots] = caches.v_scale.to(device)
         store["v_zero"].view(-1, Hkv)[slots] = caches.v_zero.to(device)

@@ -30,6 +30,15 @@ class Case:
     V_cached: List[np.ndarray]
 
 
+def _pack(q: np.ndarray, bits: int) -> np.ndarray:
+    """Codes as the library stores them: uint8, or for 4 bits two per byte
+    along the last axis (element 2m in the low nibble of byte m)."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    if bits == 8:
+        return q
+    return np.ascontiguousarray(q[..., 0::2] | (q[..., 1::2] << 4))
+
+
 def make_case(cfg: synth.FusionConfig, layouts=None, layer: int = 0, e_scale: float = 1.0) -> Case:
     layouts = layouts if layouts is not None else synth.draw_layouts(cfg)
     draws = synth.draw_layer(cfg, layouts, layer=layer, e_scale=e_scale)
@@ -40,13 +49,14 @@ def make_case(cfg: synth.FusionConfig, layouts=None, layer: int = 0, e_scale: fl
     kq_s, kq_z, vq_s, vq_z = [], [], [], []
     for (_, _, row, _pos, n) in synth.chunk_token_rows(layouts):
         K, V = orc.pic_precompute(Hc[row:row + n], Wk, Wv, Hkv, d, cfg.rope_base)
-        if cfg.kv_storage == "u8":
-            qk, sk, zk = orc.kivi_quantize_key(K)
-            qv, sv, zv = orc.kivi_quantize_value(V)
+        if cfg.kv_storage in ("u8", "u4"):
+            bits = 8 if cfg.kv_storage == "u8" else 4
+            qk, sk, zk = orc.kivi_quantize_key(K, bits)
+            qv, sv, zv = orc.kivi_quantize_value(V, bits)
             sk16, zk16 = sk.astype(np.float16), zk.astype(np.float16)
             sv16, zv16 = sv.astype(np.float16), zv.astype(np.float16)
-            Ks.append(torch.from_numpy(qk))
-            Vs.append(torch.from_numpy(qv))
+            Ks.append(torch.from_numpy(_pack(qk, bits)))
+            Vs.append(torch.from_numpy(_pack(qv, bits)))
             kq_s.append(torch.from_numpy(sk16))
             kq_z.append(torch.from_numpy(zk16))
             vq_s.append(torch.from_numpy(sv16))
@@ -63,7 +73,7 @@ def make_case(cfg: synth.FusionConfig, layouts=None, layer: int = 0, e_scale: fl
             Kc.append(f64(Kt))
             Vc.append(f64(Vt))
     caches = workload.ChunkCaches(torch.cat(Ks), torch.cat(Vs))
-    if cfg.kv_storage == "u8":
+    if cfg.kv_storage in ("u8", "u4"):
         caches.k_scale = torch.stack(kq_s)
         caches.k_zero = torch.stack(kq_z)
         caches.v_scale = torch.cat(vq_s)

@@ -47,12 +47,23 @@ SMALL = {
                                           seed=12),
 }
 
+# Cases whose storage type only the stitch sees (it dequantises into the fused
+# cache; everything after reads that cache): the stitch and score/top-k tests
+# take them, the recompute tests (which share the oracle's stitched cache)
+# gain nothing from them.
+STORAGE = {
+    # four 1024-token chunks of the int8 long-context workload with KIVI's
+    # 4-bit codes (two per byte)
+    "int4_4x1024": synth.scaled(C["llama3_70b_int8_long"], chunks_per_request=4, query_len=64,
+                                kv_storage="u4", seed=8),
+}
+
 _CASES = {}
 
 
 def case_of(name):
     if name not in _CASES:
-        _CASES[name] = make_case(SMALL[name])
+        _CASES[name] = make_case(SMALL[name] if name in SMALL else STORAGE[name])
     return _CASES[name]
 
 
@@ -89,7 +100,7 @@ def _oracle_stitched(case, store=None):
     return out
 
 
-@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("name", list(SMALL) + list(STORAGE))
 def test_stitch_rerotate(name):
     case = case_of(name)
     b = buffers(case)
@@ -102,7 +113,7 @@ def test_stitch_rerotate(name):
         if n == 0:
             continue
         assert max_row_rel(Kf[row0:row0 + n], K) <= tol
-        if case.cfg.kv_storage == "u8":
+        if case.cfg.kv_storage in ("u8", "u4"):
             assert max_row_rel(Vf[row0:row0 + n], V) <= tol
         else:
             assert np.array_equal(Vf[row0:row0 + n], V)
@@ -141,7 +152,7 @@ def test_stitch_large_positions_fp32():
     assert np.array_equal(f64(Vf), f64(caches.V))
 
 
-@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("name", list(SMALL) + list(STORAGE))
 def test_score_and_topk(name):
     case = case_of(name)
     b = buffers(case)
