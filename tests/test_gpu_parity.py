@@ -56,6 +56,9 @@ STORAGE = {
     # 4-bit codes (two per byte)
     "int4_4x1024": synth.scaled(C["llama3_70b_int8_long"], chunks_per_request=4, query_len=64,
                                 kv_storage="u4", seed=8),
+    # two requests of the batched paged workload with 4-bit codes in the
+    # block pool (d / 2 bytes per token and head, partial tail blocks)
+    "int4_paged2": synth.scaled(C["llama3_8b_paged_batch16"], n_requests=2, kv_storage="u4"),
 }
 
 _CASES = {}
