@@ -216,18 +216,6 @@ __device__ __forceinline__ void store_bf16x16_v8(__nv_bfloat16* dst, const float
                : "memory");
 }
 
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&x)[32]) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 w;
-    w.x = pack_bf16x2(x[8 * q + 0], x[8 * q + 1]);
-    w.y = pack_bf16x2(x[8 * q + 2], x[8 * q + 3]);
-    w.z = pack_bf16x2(x[8 * q + 4], x[8 * q + 5]);
-    w.w = pack_bf16x2(x[8 * q + 6], x[8 * q + 7]);
-    reinterpret_cast<uint4*>(dst)[q] = w;
-  }
-}
-
 // Operands of the recompute epilogue of one row and head loaded before the
 // accumulator is ready: the destination row and the first RoPE factors.
 constexpr int kRopeChunk = 16;                     // rotation pairs per step
@@ -623,13 +611,6 @@ int resident_pairs(const void* kernel) {
     cudaGetLastError();
   cache[{dev, kernel}] = n;
   return n;
-}
-
-int sm_count() {
-  int dev = 0, n = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 1;
 }
 
 cudaError_t launch(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtensorMap& mB1,
