@@ -422,8 +422,11 @@ cudaError_t launch_bulk_t(const BulkArgs& a, int free_sms, cudaStream_t s) {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  // alongside a kernel that holds the other SMs, two CTAs on each free SM
-  const int ctas = free_sms >= 8 ? 2 * free_sms : 2 * std::max(sms, 1);
+  // two CTAs per SM of the device, each through a short contiguous range of
+  // tiles: beside a kernel that holds most SMs (free_sms >= 0), the CTAs past
+  // the free SMs start as that kernel's CTAs finish and end soon after
+  (void)free_sms;
+  const int ctas = 2 * std::max(sms, 1);
   const int grid = std::min(a.total_tiles, ctas);
   return launch_pdl(k, dim3(grid), dim3(kBulkThreads), kBulkSmem, s, a);
 }
