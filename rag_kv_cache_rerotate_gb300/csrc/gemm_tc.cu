@@ -53,7 +53,6 @@ constexpr int kAccCols = BN2;
 constexpr int kTmemCols = 2 * kAccCols;             // two accumulators: all 512 columns
 constexpr int kEpiThreads = 256;                    // two warpgroups, one per head
 constexpr int kThreads = 64 + kEpiThreads;
-constexpr int kSmemBytes = STAGES * kStageBytes + 1024 + 512;
 
 enum Mode : int { MODE_DEVIATION = 0, MODE_RECOMPUTE = 1 };
 
@@ -100,6 +99,11 @@ struct SharedCtl {
   uint32_t tmem_base;
   volatile int abort_flag;
 };
+
+// The stages, then the control block, after aligning the base to 1024 bytes
+// (up to 1023 bytes of slack).
+constexpr int kSmemBytes = STAGES * kStageBytes + 1024 + (int)sizeof(SharedCtl);
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, SharedCtl* ctl) {
   return tc::mbar_wait(bar, parity, &ctl->abort_flag);
