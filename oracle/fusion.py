@@ -20,6 +20,9 @@ Sources (page title, then section / equation):
   (Eq. 3, RoPE and its relative-offset property), section 4.5 (Eq. 7, KIVI
   asymmetric quantisation), section 4.6.1 (Alg. 1, SelectiveRecompute seam
   windows), section 4.6.2 (Alg. 2, deviation -> top-k -> patch).
+* QCFuse section 3.2.1 (Eqs. 9-10) and section 3.4.2 (Eq. 20): the
+  query-aware importance of a context token, the attention mass the user
+  query's tokens and heads put on it, summed over the critical layers.
 
 Readings taken where the pages leave a step open:
 
@@ -34,6 +37,10 @@ Readings taken where the pages leave a step open:
 * Refreshed K/V of all selected rows are written before any attention row
   is evaluated, so a selected row sees the refreshed entries of earlier
   selected rows (QCFuse Eq. 6 text: "already refreshed prefix positions").
+* The attention mass of Eq. 10 is taken with the softmax over the context
+  keys only (the arguments the equation names: the query states and the
+  context keys), not over the context plus the query's own keys; the
+  query's inputs at the layer are the query rows of ``H``.
 * Top-k breaks ties toward the lower token index; ``-0`` counts as ``+0``;
   a NaN score is an error.
 * KIVI codes are unsigned ``0 .. 2^b - 1`` with ``zero = min``; a channel
@@ -59,7 +66,8 @@ F64 = np.float64
 __all__ = [
     "round_bf16", "rope_inv_freq", "rope_rotate", "pic_precompute", "kivi_quantize_key",
     "kivi_quantize_value", "kivi_dequantize", "stitch_rerotate",
-    "deviation_scores", "k_from_ratio", "select_topk", "selected_rows",
+    "deviation_scores", "k_from_ratio", "select_topk", "static_select",
+    "attention_mass_scores", "selected_rows",
     "project_rows", "recompute_selected", "layer_step",
 ]
 
@@ -264,6 +272,50 @@ def static_select(chunk_starts: Sequence[int], chunk_lens: Sequence[int], n_ctx:
         else:
             raise ValueError(kind)
     return np.nonzero(mask)[0].astype(np.int64)
+
+
+# --------------------------------------------------------------------------
+# Query-aware attention mass (QCFuse section 3.2.1, Eqs. 9-10; Eq. 20)
+# --------------------------------------------------------------------------
+
+def attention_mass_scores(H_query: np.ndarray, Wq, K_ctx: np.ndarray,
+                          n_q_heads: int, n_kv_heads: int, head_dim: int, base: float,
+                          store=None) -> np.ndarray:
+    """Importance ``I(t)`` of every context token of one request at one layer:
+    the attention the user query pays to it (QCFuse Eq. 10 for one layer;
+    Eq. 20 adds this quantity over the critical layers L*).
+
+    ``H_query`` ``[Qn, D]`` holds the query tokens' inputs to the layer; query
+    token u sits at request position ``N + u`` with ``N = K_ctx.shape[0]``,
+    so its state is ``q_{u,h} = R^{N+u} W_Q x_u`` (head h of the projection,
+    the same projection the recomputation uses).  ``K_ctx`` ``[N, Hkv, d]``
+    holds the stitched PIC keys of the N context tokens (QCFuse Eq. 4).
+    For every (u, h) the weights over the context keys are
+    ``softmax_t(q_{u,h} . K[t, h // g] / sqrt(d))``, ``g = Hq / Hkv``, and
+    ``I(t)`` is the sum of the weight of t over all (u, h): each (u, h)
+    contributes a total of exactly 1.  ``store`` (the layer's storage
+    rounding) is applied to q where it is materialised.
+    """
+    X = np.asarray(H_query, F64)
+    K = np.asarray(K_ctx, F64)
+    n_query = X.shape[0]
+    n = K.shape[0]
+    out = np.zeros(n, dtype=F64)
+    if n == 0 or n_query == 0:
+        return out
+    g = n_q_heads // n_kv_heads
+    q = (X @ np.asarray(Wq, F64).T).reshape(n_query, n_q_heads, head_dim)
+    q = rope_rotate(q, (n + np.arange(n_query))[:, None], base)
+    if store is not None:
+        q = store(q)
+    scale = 1.0 / math.sqrt(head_dim)
+    for h in range(n_q_heads):
+        logits = np.matmul(q[:, h, :], K[:, h // g, :].T) * scale       # [Qn, N]
+        m = logits.max(axis=1, keepdims=True)
+        w = np.exp(logits - m)
+        w /= w.sum(axis=1, keepdims=True)
+        out += w.sum(axis=0)
+    return out
 
 
 def selected_rows(idx: np.ndarray, n_ctx: int, n_tok: int) -> np.ndarray:

@@ -526,3 +526,83 @@ def test_static_select_counts_from_the_pages():
         got = orc.static_select(starts, lens, int(lens.sum()), "chunk_head", n)
         assert len(got) == int(np.minimum(lens, n).sum())
         assert np.all(np.diff(got) > 0)
+
+
+# Query-aware attention mass (QCFuse section 3.2.1, Eqs. 9-10; Eq. 20)
+def _mass_hand_setup(n_q_heads, n_kv_heads, q_head, key_head, hot):
+    """d = 2 (one RoPE pair, theta_0 = 1 radian per position), N = 2 context
+    keys, one query token at position 2.  W_Q maps x = (1, 0) to q = (1, 0)
+    for query head `q_head` only; after R^2 that q is (cos 2, sin 2).  Key
+    `hot` of KV head `key_head` is sqrt(2) ln 3 (cos 2, sin 2), every other
+    key is 0: that head's logits are ln 3 at `hot` and 0 elsewhere, so its
+    weights are 3/4 and 1/4; every other query head (q = 0) spreads 1/2, 1/2."""
+    Wq = np.zeros((n_q_heads * 2, 2))
+    Wq[2 * q_head:2 * q_head + 2] = np.eye(2)
+    K = np.zeros((2, n_kv_heads, 2))
+    K[hot, key_head] = math.sqrt(2.0) * math.log(3.0) * np.array([math.cos(2.0), math.sin(2.0)])
+    return np.array([[1.0, 0.0]]), Wq, K
+
+
+def test_attention_mass_hand_worked_d2():
+    H, Wq, K = _mass_hand_setup(2, 1, 0, 0, 1)
+    got = orc.attention_mass_scores(H, Wq, K, 2, 1, 2, 1e4)
+    assert np.allclose(got, [0.25 + 0.5, 0.75 + 0.5], atol=1e-12)
+
+
+def test_attention_mass_gqa_query_head_reads_kv_head_h_div_g():
+    # Hq = 4, Hkv = 2: query head 2 reads KV head 1 (not 2 % 2 = 0)
+    H, Wq, K = _mass_hand_setup(4, 2, 2, 1, 0)
+    K[1, 0] = K[0, 1]              # KV head 0 would favour the other key
+    got = orc.attention_mass_scores(H, Wq, K, 4, 2, 2, 1e4)
+    assert np.allclose(got, [0.75 + 1.5, 0.25 + 1.5], atol=1e-12)
+
+
+def test_attention_mass_matches_complex_form_and_library_softmax():
+    # d = 4: pairs (0, 2) and (1, 3) as complex numbers turned by e^{i p theta_j};
+    # q . k = Re(sum_j z_q,j conj(z_k,j)); the softmax is scipy's.
+    from scipy.special import softmax
+    rng = _rng(31)
+    n, n_query, hq, hkv, d, base = 7, 3, 4, 2, 4, 100.0
+    H = rng.standard_normal((n_query, 5))
+    Wq = rng.standard_normal((hq * d, 5))
+    K = rng.standard_normal((n, hkv, d))
+    want = np.zeros(n)
+    for u in range(n_query):
+        qraw = (Wq @ H[u]).reshape(hq, d)
+        for h in range(hq):
+            logits = []
+            for t in range(n):
+                acc = 0.0
+                for j in range(2):
+                    theta = base ** (-2.0 * j / d)
+                    zq = complex(qraw[h, j], qraw[h, j + 2]) * complex(
+                        math.cos((n + u) * theta), math.sin((n + u) * theta))
+                    zk = complex(K[t, h // 2, j], K[t, h // 2, j + 2])
+                    acc += (zq * zk.conjugate()).real
+                logits.append(acc / 2.0)                       # 1 / sqrt(4)
+            want += softmax(np.array(logits))
+    got = orc.attention_mass_scores(H, Wq, K, hq, hkv, d, base)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+def test_attention_mass_invariants():
+    rng = _rng(32)
+    n, n_query, hq, hkv, d, D = 40, 6, 8, 2, 16, 24
+    H = rng.standard_normal((n_query, D))
+    Wq = rng.standard_normal((hq * d, D)) * 0.5
+    K = rng.standard_normal((n, hkv, d))
+    I = orc.attention_mass_scores(H, Wq, K, hq, hkv, d, 1e4)
+    # every (query token, head) spreads a total weight of 1 over the context
+    assert abs(I.sum() - n_query * hq) < 1e-9
+    assert np.all(I > 0)
+    # the same vector added to every key of a head moves each logit row by a
+    # constant: the softmax, hence the mass, does not change
+    shift = rng.standard_normal((1, hkv, d)) * 3.0
+    assert np.allclose(orc.attention_mass_scores(H, Wq, K + shift, hq, hkv, d, 1e4), I,
+                       rtol=1e-10, atol=1e-12)
+    # zero keys: uniform weights
+    assert np.allclose(orc.attention_mass_scores(H, Wq, 0 * K, hq, hkv, d, 1e4),
+                       n_query * hq / n, atol=1e-12)
+    # no query token: nothing spread; no context: nothing to score
+    assert np.array_equal(orc.attention_mass_scores(H[:0], Wq, K, hq, hkv, d, 1e4), np.zeros(n))
+    assert orc.attention_mass_scores(H, Wq, K[:0], hq, hkv, d, 1e4).shape == (0,)
