@@ -4,7 +4,8 @@
  * One layer-step of RAG KV-cache fusion with selective recomputation, as
  * stated on two pages:
  *   [QCFuse]  "QCFuse: Query-Aware Cache Fusion via Compressed View for
- *             Efficient RAG Serving", section 2.1 (Eqs. 1-7), Eq. 11.
+ *             Efficient RAG Serving", section 2.1 (Eqs. 1-7), Eq. 11,
+ *             section 3.2.1 (Eqs. 9-10), section 3.4.2 (Eq. 20).
  *   [KVBoost] "KVBoost: Chunk-Level KV Cache Reuse with Deviation-Guided
  *             Recomputation", sections 3.1-3.2 (Eqs. 1-3), 4.5 (Eq. 7),
  *             4.6.2 (Alg. 2, CacheBlendRecompute).
@@ -213,6 +214,27 @@ fuse_status_t fuse_stitch_rerotate(const fuse_layer_desc_t* desc, const fuse_chu
 fuse_status_t fuse_score_deviation(const fuse_layer_desc_t* desc, const fuse_requests_t* reqs,
                                    const void* H, const void* Wv, const void* Vf, float* score,
                                    void* ws, size_t ws_bytes, fuse_stream_t stream);
+
+/* Query-aware importance of every context token ([QCFuse] section 3.2.1,
+ * Eqs. 9-10, the full-view attention mass; section 3.4.2, Eq. 20, its sum
+ * over the critical layers).  For request r with N = N_r context and
+ * Qn = Qn_r query tokens, query token u (row row0 + N + u of H) has the state
+ *   q_{u,h} = R^{N+u} W_Q x_u        (head h, the recomputation's projection)
+ * and the score of context token t is the attention weight it receives,
+ *   I(t) = sum_{u < Qn} sum_h softmax_{t' < N}(q_{u,h} . Kf[row0 + t', h/g] / sqrt(d))[t],
+ * the softmax over the N context keys of the layer's fused cache (Kf after
+ * fuse_stitch_rerotate: the PIC keys of [QCFuse] Eq. 4).  Every (u, h)
+ * spreads a total of 1, so the scores of a request sum to Qn * Hq.
+ * accumulate == 0 writes I to score[score0 + t]; accumulate != 0 adds it
+ * (call once per critical layer for Eq. 20's sum).  Kf and H are only read.
+ * Query states are materialised in desc->dtype (bf16 layers round q to
+ * bf16); logits, weights and sums are fp32.  Deterministic: no
+ * floating-point atomics.  Needs the workspace of fuse_workspace_size.
+ * FUSE_ERR_UNSUPPORTED for more than 65535 requests. */
+fuse_status_t fuse_score_attention_mass(const fuse_layer_desc_t* desc, const fuse_requests_t* reqs,
+                                        const void* H, const void* Wq, const void* Kf,
+                                        int32_t accumulate, float* score, void* ws,
+                                        size_t ws_bytes, fuse_stream_t stream);
 
 /* TopK(score, k_r) per request ([QCFuse] Eq. 11; [KVBoost] Alg. 2 step 3):
  * the k_r largest scores, ties broken toward the lower token index, -0 equal

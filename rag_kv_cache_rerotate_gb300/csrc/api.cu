@@ -25,6 +25,9 @@ cudaError_t launch_project_recompute_tc(const fuse_layer_desc_t& desc, int64_t n
                                         const WorkRow* rows, const float2* rope, const void* H,
                                         const void* Wq, const void* Wk, const void* Wv, void* Q,
                                         void* Kf, void* Vf, void* Hs, uint32_t* err, cudaStream_t s);
+cudaError_t launch_project_query_tc(const fuse_layer_desc_t& d, int64_t n_rows, const float2* rope,
+                                    const void* Wq, void* Q, const void* Hs, uint32_t* err,
+                                    cudaStream_t s);
 bool tc_attention_supported(const fuse_layer_desc_t& desc);
 int attention_rtile(const fuse_layer_desc_t& d);
 size_t attention_tiles_bytes(int64_t n_out, int n_req);
@@ -80,6 +83,8 @@ struct ReqInfo {
   fuse_totals_t tot;   // extents implied by the offsets (max over requests)
   int n_req;
   bool sorted;         // row0 ascending, request row ranges disjoint
+  int64_t n_qrows;     // sum of n_query: the packed query rows of the scorer
+  int32_t max_query;   // max n_query
 };
 
 fuse_status_t check_reqs(const fuse_requests_t* r, ReqInfo* info, bool need_device = true) {
@@ -105,6 +110,8 @@ fuse_status_t check_reqs(const fuse_requests_t* r, ReqInfo* info, bool need_devi
     t.n_out = std::max<int64_t>(t.n_out, q.out0 + q.k + q.n_query);
     t.max_ctx = std::max<int32_t>(t.max_ctx, q.n_ctx);
     t.max_tok = std::max<int32_t>(t.max_tok, (int32_t)T);
+    info->n_qrows += q.n_query;
+    info->max_query = std::max(info->max_query, q.n_query);
   }
   if (t.n_tok > INT32_MAX) return FUSE_ERR_UNSUPPORTED;
   return FUSE_OK;
@@ -147,10 +154,15 @@ fuse_status_t check_chunks(const fuse_layer_desc_t& d, const fuse_chunks_t* c, i
 
 // Workspace regions (each 256-byte aligned).
 struct WsLayout {
-  size_t partial, keys, map, rows, rope, q, hs, tiles, total;
+  size_t partial, keys, map, rows, rope, q, hs, tiles;
+  size_t mrows, mrope, mq, mhs, mstats, mnorm, qoff;   // query-aware scorer
+  size_t total;
 };
 
-WsLayout ws_layout(const fuse_layer_desc_t& d, const fuse_totals_t& t, int n_req) {
+WsLayout ws_layout(const fuse_layer_desc_t& d, const ReqInfo& info) {
+  const fuse_totals_t& t = info.tot;
+  const int n_req = info.n_req;
+  const size_t nq = (size_t)info.n_qrows;
   WsLayout L;
   size_t off = sizeof(WsHeader);
   auto take = [&](size_t bytes) {
@@ -167,6 +179,13 @@ WsLayout ws_layout(const fuse_layer_desc_t& d, const fuse_totals_t& t, int n_req
   L.q = take((size_t)t.n_out * d.n_q_heads * d.head_dim * es);
   L.hs = take((size_t)t.n_out * d.hidden * es);
   L.tiles = take(attention_tiles_bytes(t.n_out, n_req));
+  L.mrows = take(nq * sizeof(WorkRow));
+  L.mrope = take(nq * (d.head_dim / 2) * sizeof(float2));
+  L.mq = take(nq * d.n_q_heads * d.head_dim * es);
+  L.mhs = take(nq * d.hidden * es);
+  L.mstats = take(nq * d.n_q_heads * (size_t)mass_key_tiles(t.max_ctx) * sizeof(float2));
+  L.mnorm = take(nq * d.n_q_heads * sizeof(float2));
+  L.qoff = take((size_t)n_req * sizeof(int32_t));
   L.total = off;
   return L;
 }
@@ -212,7 +231,7 @@ bool chunks_sorted(const fuse_chunks_t& c) {
 fuse_status_t do_score(const fuse_layer_desc_t& d, const fuse_requests_t& r, const ReqInfo& info,
                        const void* H, const void* Wv, const void* Vf, float* score, void* ws,
                        cudaStream_t s, bool reduce = true, const fuse_chunks_t* v_chunks = nullptr) {
-  const WsLayout L = ws_layout(d, info.tot, info.n_req);
+  const WsLayout L = ws_layout(d, info);
   if (info.tot.n_ctx == 0) return FUSE_OK;
   int32_t* map = at<int32_t>(ws, L.map);
   float* partial = at<float>(ws, L.partial);
@@ -249,7 +268,7 @@ fuse_status_t do_score(const fuse_layer_desc_t& d, const fuse_requests_t& r, con
 fuse_status_t do_reduce_topk(const fuse_layer_desc_t& d, const fuse_requests_t& r,
                              const ReqInfo& info, float* score, int32_t* idx, void* ws,
                              cudaStream_t s) {
-  const WsLayout L = ws_layout(d, info.tot, info.n_req);
+  const WsLayout L = ws_layout(d, info);
   if (info.tot.n_ctx == 0) return FUSE_OK;
   return cuda_status(traced("reduce_topk", s, [&] {
     return launch_reduce_topk(r, info.tot.max_ctx, at<float>(ws, L.partial), score_parts(d),
@@ -262,7 +281,7 @@ fuse_status_t do_recompute(const fuse_layer_desc_t& d, const fuse_requests_t& r,
                            const ReqInfo& info, const void* H, const void* Wq, const void* Wk,
                            const void* Wv, const int32_t* idx, void* Kf, void* Vf, void* O,
                            void* ws, cudaStream_t s) {
-  const WsLayout L = ws_layout(d, info.tot, info.n_req);
+  const WsLayout L = ws_layout(d, info);
   const int64_t R = info.tot.n_out;
   if (R == 0) return FUSE_OK;
   int max_rows = 0;
@@ -307,6 +326,44 @@ fuse_status_t do_recompute(const fuse_layer_desc_t& d, const fuse_requests_t& r,
   return cuda_status(e);
 }
 
+// Query-aware attention mass (QCFuse Eqs. 9-10, 20): the query rows packed,
+// their Q projected (Q heads only), then the scoring launches.
+fuse_status_t do_mass(const fuse_layer_desc_t& d, const fuse_requests_t& r, const ReqInfo& info,
+                      const void* H, const void* Wq, const void* Kf, float* score, int accumulate,
+                      void* ws, cudaStream_t s) {
+  const WsLayout L = ws_layout(d, info);
+  if (info.tot.n_ctx == 0 || info.tot.max_ctx == 0) return FUSE_OK;
+  const int64_t nq = info.n_qrows;
+  WorkRow* rows = at<WorkRow>(ws, L.mrows);
+  float2* rope = at<float2>(ws, L.mrope);
+  void* Q = at<void>(ws, L.mq);
+  int32_t* qoff = at<int32_t>(ws, L.qoff);
+  uint32_t* err = at<uint32_t>(ws, 0);
+  const bool tc = tc_gemm_supported(d);
+  const RopeFreqs f = make_freqs(d);
+  cudaError_t e = traced("query_rows", s, [&] {
+    return launch_query_rows(r, info.max_query, f, d.head_dim, H, d.hidden, rows, rope, nq,
+                             tc ? at<void>(ws, L.mhs) : nullptr, qoff, err, s);
+  });
+  if (e == cudaSuccess && nq > 0) {
+    if (tc)
+      e = traced("query_gemm_tc", s, [&] {
+        return launch_project_query_tc(d, nq, rope, Wq, Q, at<void>(ws, L.mhs), err, s);
+      });
+    else
+      e = traced("query_gemm_simt", s, [&] {
+        return launch_project_query_simt(d, nq, rows, rope, H, Wq, Q, err, s);
+      });
+  }
+  if (e == cudaSuccess)
+    e = traced("attention_mass", s, [&] {
+      return launch_attention_mass(d, r, info.tot.max_ctx, nq, rows, qoff, Q, Kf,
+                                   at<float2>(ws, L.mstats), at<float2>(ws, L.mnorm),
+                                   at<float>(ws, L.partial), score, accumulate, s);
+    });
+  return cuda_status(e);
+}
+
 struct LayerArgs {
   const fuse_chunks_t* chunks;
   const void* H;
@@ -331,7 +388,7 @@ fuse_status_t check_layer(const fuse_layer_desc_t& d, const ReqInfo& info, const
   if (!aligned16(a.H) || !aligned16(a.Wq) || !aligned16(a.Wk) || !aligned16(a.Wv) ||
       !aligned16(a.Kf) || !aligned16(a.Vf) || !aligned16(a.O) || !aligned16(score))
     return FUSE_ERR_MISALIGNED;
-  return check_ws(ws, ws_bytes, ws_layout(d, info.tot, info.n_req).total);
+  return check_ws(ws, ws_bytes, ws_layout(d, info).total);
 }
 
 // Deviation scores and the top-k selection of one (scoring) layer.
@@ -420,7 +477,7 @@ fuse_status_t fuse_workspace_size(const fuse_layer_desc_t* desc, const fuse_requ
   ReqInfo info;
   st = check_reqs(reqs, &info, /*need_device=*/false);
   if (st != FUSE_OK) return st;
-  *bytes = ws_layout(*desc, info.tot, info.n_req).total;
+  *bytes = ws_layout(*desc, info).total;
   return FUSE_OK;
 }
 
@@ -456,9 +513,27 @@ fuse_status_t fuse_score_deviation(const fuse_layer_desc_t* desc, const fuse_req
   if (info.tot.n_ctx > 0 && (!H || !Wv || !Vf || !score)) return FUSE_ERR_INVALID_ARG;
   if (!aligned16(H) || !aligned16(Wv) || !aligned16(Vf) || !aligned16(score))
     return FUSE_ERR_MISALIGNED;
-  st = check_ws(ws, ws_bytes, ws_layout(*desc, info.tot, info.n_req).total);
+  st = check_ws(ws, ws_bytes, ws_layout(*desc, info).total);
   if (st != FUSE_OK) return st;
   return do_score(*desc, *reqs, info, H, Wv, Vf, score, ws, (cudaStream_t)stream);
+}
+
+fuse_status_t fuse_score_attention_mass(const fuse_layer_desc_t* desc, const fuse_requests_t* reqs,
+                                        const void* H, const void* Wq, const void* Kf,
+                                        int32_t accumulate, float* score, void* ws,
+                                        size_t ws_bytes, fuse_stream_t stream) {
+  fuse_status_t st = check_desc(desc);
+  if (st != FUSE_OK) return st;
+  ReqInfo info;
+  st = check_reqs(reqs, &info);
+  if (st != FUSE_OK) return st;
+  if (info.n_req > 65535 || info.n_qrows > INT32_MAX) return FUSE_ERR_UNSUPPORTED;
+  if (info.tot.n_ctx > 0 && (!H || !Wq || !Kf || !score)) return FUSE_ERR_INVALID_ARG;
+  if (!aligned16(H) || !aligned16(Wq) || !aligned16(Kf) || !aligned16(score))
+    return FUSE_ERR_MISALIGNED;
+  st = check_ws(ws, ws_bytes, ws_layout(*desc, info).total);
+  if (st != FUSE_OK) return st;
+  return do_mass(*desc, *reqs, info, H, Wq, Kf, score, accumulate, ws, (cudaStream_t)stream);
 }
 
 fuse_status_t fuse_select_topk(const fuse_requests_t* reqs, const float* score, int32_t* idx,
@@ -495,7 +570,7 @@ fuse_status_t fuse_recompute_selected(const fuse_layer_desc_t* desc, const fuse_
   if (!aligned16(H) || !aligned16(Wq) || !aligned16(Wk) || !aligned16(Wv) || !aligned16(Kf) ||
       !aligned16(Vf) || !aligned16(O))
     return FUSE_ERR_MISALIGNED;
-  st = check_ws(ws, ws_bytes, ws_layout(*desc, info.tot, info.n_req).total);
+  st = check_ws(ws, ws_bytes, ws_layout(*desc, info).total);
   if (st != FUSE_OK) return st;
   return do_recompute(*desc, *reqs, info, H, Wq, Wk, Wv, idx, Kf, Vf, O, ws, (cudaStream_t)stream);
 }

@@ -31,6 +31,7 @@ enum ErrSite : uint32_t {
   SITE_GEMM_TIMEOUT = 6,     // tensor-core pipeline wait gave up
   SITE_ATTN_TIMEOUT = 7,     // attention pipeline wait gave up
   SITE_STITCH_TIMEOUT = 8,   // stitch bulk-copy wait gave up
+  SITE_MASS_ROWS = 9,        // query rows past the host's count (device table differs)
 };
 
 __device__ __forceinline__ void report_error(uint32_t* err, fuse_status_t code, uint32_t site,

@@ -331,6 +331,28 @@ cudaError_t launch_project_recompute_simt(const fuse_layer_desc_t& desc, int64_t
   return dispatch(desc, a, a.n0 + 2 * a.n1, s);
 }
 
+cudaError_t launch_project_query_simt(const fuse_layer_desc_t& desc, int64_t n_rows,
+                                      const WorkRow* rows, const float2* rope, const void* H,
+                                      const void* Wq, void* Q, uint32_t* err, cudaStream_t s) {
+  GemmArgs a = {};
+  a.M = n_rows;
+  a.K = desc.hidden;
+  a.A = H;
+  a.rows = rows;
+  a.W0 = Wq;
+  a.W1 = Wq;
+  a.W2 = Wq;
+  a.n0 = desc.n_q_heads * desc.head_dim;
+  a.n1 = 0;
+  a.n_q_heads = desc.n_q_heads;
+  a.n_kv_heads = desc.n_kv_heads;
+  a.mode = EPI_RECOMPUTE;
+  a.rope = rope;
+  a.Q = Q;
+  a.err = err;
+  return dispatch(desc, a, a.n0, s);     // Q heads only: no K/V columns, no scatter
+}
+
 cudaError_t launch_project_pic(const fuse_layer_desc_t& desc, int n_chunks, int max_len,
                                const RopeFreqs& freqs, const void* H, const void* Wk, const void* Wv,
                                const fuse_chunk_t* d_chunks, uint32_t* err, cudaStream_t s) {

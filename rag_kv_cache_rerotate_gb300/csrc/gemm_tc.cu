@@ -731,4 +731,30 @@ cudaError_t launch_project_recompute_tc(const fuse_layer_desc_t& d, int64_t n_ro
   return launch(mA, mQ, mK, mV, a, s);
 }
 
+// Q heads only (query-aware scoring): Q[m] = R^{pos} W_Q Hs[m]; no K/V scatter.
+cudaError_t launch_project_query_tc(const fuse_layer_desc_t& d, int64_t n_rows, const float2* rope,
+                                    const void* Wq, void* Q, const void* Hs, uint32_t* err,
+                                    cudaStream_t s) {
+  if (n_rows == 0) return cudaSuccess;
+  CUtensorMap mA, mQ;
+  if (!make_map(&mA, Hs, n_rows, d.hidden) ||
+      !make_map(&mQ, Wq, (int64_t)d.n_q_heads * d.head_dim, d.hidden))
+    return cudaErrorInvalidValue;
+  TcArgs a = {};
+  a.M = (int)n_rows;
+  a.K = d.hidden;
+  a.m_tiles = (int)((n_rows + BMP - 1) / BMP);
+  a.n_tiles = d.n_q_heads / 2;
+  a.h0 = d.n_q_heads;
+  a.h1 = 0;
+  a.mode = MODE_RECOMPUTE;
+  a.n_q_heads = d.n_q_heads;
+  a.n_kv_heads = d.n_kv_heads;
+  a.rope = rope;
+  a.Q = reinterpret_cast<__nv_bfloat16*>(Q);
+  a.st32 = (reinterpret_cast<uintptr_t>(Q) & 31u) == 0;
+  a.err = err;
+  return launch(mA, mQ, mQ, mQ, a, s);
+}
+
 }  // namespace fusekv

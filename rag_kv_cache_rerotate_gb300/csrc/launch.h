@@ -122,6 +122,24 @@ cudaError_t launch_project_pic(const fuse_layer_desc_t& desc, int n_chunks, int 
                                const RopeFreqs& freqs, const void* H, const void* Wk, const void* Wv,
                                const fuse_chunk_t* d_chunks, uint32_t* err, cudaStream_t s);
 
+// Query projection of packed work rows (Q heads only, RoPE at each row's position).
+cudaError_t launch_project_query_simt(const fuse_layer_desc_t& desc, int64_t n_rows,
+                                      const WorkRow* rows, const float2* rope, const void* H,
+                                      const void* Wq, void* Q, uint32_t* err, cudaStream_t s);
+
+// Query-aware attention mass: key tiles per request, the packed query rows
+// (offsets, work rows, RoPE table, gathered inputs), and the scoring launches.
+int mass_key_tiles(int max_ctx);
+cudaError_t launch_query_rows(const fuse_requests_t& reqs, int max_query, const RopeFreqs& freqs,
+                              int head_dim, const void* H, int hidden, WorkRow* rows, float2* rope,
+                              int64_t n_rows, void* Hs, int32_t* qoff, uint32_t* err,
+                              cudaStream_t s);
+cudaError_t launch_attention_mass(const fuse_layer_desc_t& d, const fuse_requests_t& reqs,
+                                  int max_ctx, int64_t n_qrows, const WorkRow* rows,
+                                  const int32_t* qoff, const void* Q, const void* Kf,
+                                  float2* stats, float2* norm, float* partial, float* score,
+                                  int accumulate, cudaStream_t s);
+
 // Causal GQA attention of the work rows over the fused cache.
 cudaError_t launch_attention_simt(const fuse_layer_desc_t& desc, int64_t n_rows, const WorkRow* rows,
                                   const void* Q, const void* Kf, const void* Vf, void* O,

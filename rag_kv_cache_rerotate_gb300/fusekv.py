@@ -96,6 +96,8 @@ _SIGS = {
     "fuse_workspace_reset": (_c.c_int, [_P, _c.c_size_t, _P]),
     "fuse_stitch_rerotate": (_c.c_int, [_P, _P, _P, _P, _c.c_int64, _P, _c.c_size_t, _P]),
     "fuse_score_deviation": (_c.c_int, [_P, _P, _P, _P, _P, _P, _P, _c.c_size_t, _P]),
+    "fuse_score_attention_mass": (_c.c_int, [_P, _P, _P, _P, _P, _c.c_int32, _P, _P,
+                                             _c.c_size_t, _P]),
     "fuse_select_topk": (_c.c_int, [_P, _P, _P, _P, _c.c_size_t, _P]),
     "fuse_recompute_selected": (_c.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                            _c.c_size_t, _P]),
@@ -256,6 +258,16 @@ def score_deviation(desc, reqs: RequestTable, H, Wv, Vf, score, ws, stream=None)
     _check(load().fuse_score_deviation(_c.byref(desc), _c.byref(reqs.c), _ptr(H), _ptr(Wv),
                                        _ptr(Vf), _ptr(score), _ptr(ws), ws.numel(),
                                        _stream(stream)), "fuse_score_deviation")
+
+
+def score_attention_mass(desc, reqs: RequestTable, H, Wq, Kf, score, ws, accumulate=False,
+                         stream=None):
+    """Query-aware attention mass of every context token (QCFuse Eqs. 9-10;
+    ``accumulate=True`` adds this layer's term, Eq. 20)."""
+    _check(load().fuse_score_attention_mass(_c.byref(desc), _c.byref(reqs.c), _ptr(H), _ptr(Wq),
+                                            _ptr(Kf), int(bool(accumulate)), _ptr(score),
+                                            _ptr(ws), ws.numel(), _stream(stream)),
+           "fuse_score_attention_mass")
 
 
 SEL_CHUNK_HEAD, SEL_SEAM_TAIL = 0, 1

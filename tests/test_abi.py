@@ -186,3 +186,28 @@ def test_static_select_rejects_bad_tables(fk):
     wrong = fk.requests_with_k(rt, [x + 1 for x in k], device=None)
     with pytest.raises(fk.FuseError):
         fk.static_select(wrong, ct, 1, 16, None)
+
+
+def test_attention_mass_argument_errors(fk):
+    # every call below carries one error, found on the host before any launch
+    lib = fk.load()
+    desc = _desc(fk)
+    t = fk.plan_requests([256], [16], 0.3, device=None)
+    t.c.d_req = 16                                      # a non-null stand-in, never dereferenced
+    need = fk.workspace_size(desc, t)
+
+    def call(H, Wq, Kf, score, ws, nbytes):
+        return lib.fuse_score_attention_mass(ctypes.byref(desc), ctypes.byref(t.c), H, Wq, Kf, 0,
+                                             score, ws, nbytes, None)
+
+    A = 1 << 20                                         # aligned stand-ins, never dereferenced
+    assert call(None, A, A, A, A, need) == fk.FUSE_ERR_INVALID_ARG
+    assert call(A, A, None, A, A, need) == fk.FUSE_ERR_INVALID_ARG
+    assert call(A + 8, A, A, A, A, need) == fk.FUSE_ERR_MISALIGNED
+    assert call(A, A, A, A + 4, A, need) == fk.FUSE_ERR_MISALIGNED
+    assert call(A, A, A, A, A, need - 1) == fk.FUSE_ERR_WORKSPACE
+    assert call(A, A, A, A, A + 16, need) == fk.FUSE_ERR_MISALIGNED     # workspace: 256 bytes
+    assert call(A, A, A, A, None, need) == fk.FUSE_ERR_WORKSPACE
+    # the packed query rows (Q, RoPE table, tile statistics) need workspace
+    t0 = fk.plan_requests([256], [0], 0.3, device=None)
+    assert need > fk.workspace_size(desc, t0)
