@@ -393,6 +393,46 @@ def native_run(args, ws, rank, local):
                 "frac": ach / peak, "traffic": _traffic(dom),
                 "peak_source": f"{peak_src} ({'sustained bf16' if bound == 'tensor' else 'HBM copy'})"}
 
+    # the query-aware attention-mass scorer (QCFuse Eqs. 9-10), timed apart
+    # from the step on the same input sets: CUDA events around the calls on
+    # the launching stream, then its kernels with the library's trace on
+    scorer = None
+    if args.scorer_calls > 0:
+        def mass(b):
+            fk.score_attention_mass(b.desc, b.reqs, b.H, b.Wq, b.Kf, b.score, b.ws)
+        for i in range(3):
+            mass(sets[i % n_sets])
+        torch.cuda.synchronize()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for i in range(args.scorer_calls):
+            mass(sets[i % n_sets])
+        s1.record(stream)
+        torch.cuda.synchronize()
+        us = 1e3 * s0.elapsed_time(s1) / args.scorer_calls
+        fk.trace_begin(args.scorer_calls * 8 + 8)
+        for i in range(args.scorer_calls):
+            mass(sets[i % n_sets])
+        torch.cuda.synchronize()
+        sper = {}
+        for name, kms in fk.trace_end():
+            c, tot = sper.get(name, (0, 0.0))
+            sper[name] = (c + 1, tot + kms)
+        for b in sets:
+            fk.check_errors(b.ws)
+        Qn = q.n_query
+        s_work = {"query_gemm_tc": 2.0 * Qn * D * Hq * d, "query_gemm_simt": 2.0 * Qn * D * Hq * d,
+                  "attention_mass": 2.0 * Qn * Hq * N * d}
+        sk = {}
+        for n, (c, tot) in sper.items():
+            sk[n] = {"launches": c, "avg_us": 1e3 * tot / c}
+            if n in s_work:
+                sk[n]["TFLOP/s"] = s_work[n] / (tot / c / 1e3) / 1e12
+        scorer = {"us_per_call": us, "calls": args.scorer_calls, "kernels": sk,
+                  "work": "query GEMM 2*Qn*D*Hq*d flop; attention mass one Q.K pass "
+                          "2*Qn*Hq*N*d flop (computed twice: statistics and mass)"}
+
     # end to end through the C ABI with host buffers: every step uploads its
     # inputs (chunk K/V caches and H) from pinned host memory and reads its
     # result (O and idx) back.  Two input sets alternate so that, as in a
@@ -498,6 +538,8 @@ def native_run(args, ws, rank, local):
         "config": cfg_json, "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches, "clocks": clocks, "impl": "native",
     }
+    if scorer is not None:
+        out["attention_mass_scorer"] = scorer
     if rank == 0:
         print(json.dumps(out), flush=True)
     if ws > 1:
@@ -532,6 +574,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--e2e-copy-streams", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--scorer-calls", type=int, default=50)
     ap.add_argument("--cpu-budget", type=float, default=30.0)
     ap.add_argument("--ref-budget", type=float, default=150.0)
     args = ap.parse_args()
