@@ -30,7 +30,9 @@ Readings taken where the pages leave a step open:
   ``theta_j = base^(-2j/d)``; KVBoost targets HuggingFace RoPE models.
 * The deviation is computed on V at one layer (1 - cosine between the
   freshly projected V and the cached V, averaged over KV heads); KVBoost's
-  Alg. 2 writes it on K averaged over all layers and heads.
+  Alg. 2 writes it on K averaged over all layers and heads.  ``key_deviation_scores`` states that printed form: the fresh key is
+  ``R^t W_K x_t`` at the token's request position, the stale key the
+  stitched cache's, and H is the number of key (KV) heads.
 * Query rows are always recomputed, never scored, and are not counted in
   ``N`` or ``k``.  ``k = floor(rho * N + 1e-9)``; the epsilon keeps binary
   fractions such as ``0.29 * 100`` from dropping a token.
@@ -66,7 +68,7 @@ F64 = np.float64
 __all__ = [
     "round_bf16", "rope_inv_freq", "rope_rotate", "pic_precompute", "kivi_quantize_key",
     "kivi_quantize_value", "kivi_dequantize", "stitch_rerotate",
-    "deviation_scores", "k_from_ratio", "select_topk", "static_select",
+    "deviation_scores", "key_deviation_scores", "k_from_ratio", "select_topk", "static_select",
     "attention_mass_scores", "selected_rows",
     "project_rows", "recompute_selected", "layer_step",
 ]
@@ -222,6 +224,36 @@ def deviation_scores(H_ctx: np.ndarray, Wv: np.ndarray, V_cached: np.ndarray,
     den = np.sqrt(np.sum(Vn * Vn, axis=-1)) * np.sqrt(np.sum(Vc * Vc, axis=-1))
     cos = dot / np.maximum(den, 1e-30)
     return 1.0 - cos.mean(axis=1)
+
+
+def key_deviation_scores(H_ctx_layers: Sequence[np.ndarray], Wk_layers: Sequence[np.ndarray],
+                         K_stale_layers: Sequence[np.ndarray], n_kv_heads: int, head_dim: int,
+                         base: float) -> np.ndarray:
+    """KVBoost Alg. 2 step 2 as the page writes it, on the keys of L layers:
+    ``delta_t = 1 - (1/(L Hkv)) sum_{l,h} cos(K~_t^(l,h), K_t^(l,h))``.
+
+    Per layer l: ``H_ctx_layers[l]`` ``[N, D]`` holds the layer's inputs at
+    the N context tokens (the probe pass), ``Wk_layers[l]`` its key
+    projection, ``K_stale_layers[l]`` ``[N, Hkv, d]`` the assembled keys (the
+    stitched cache).  The fresh key of token t is ``K~_t = R^t W_K x_t``, at
+    the token's request position t, as the probe pass places it.  H in the
+    formula is the number of key heads, Hkv.  The cosine denominator is
+    clamped at 1e-30 (a zero vector gives cosine 0).
+    """
+    n_layers = len(H_ctx_layers)
+    if n_layers == 0 or len(Wk_layers) != n_layers or len(K_stale_layers) != n_layers:
+        raise ValueError("one H, W_K and stale K per layer")
+    n = np.asarray(H_ctx_layers[0]).shape[0]
+    acc = np.zeros(n, dtype=F64)
+    for X, Wk, Ks in zip(H_ctx_layers, Wk_layers, K_stale_layers):
+        X = np.asarray(X, F64)
+        Kn = (X @ np.asarray(Wk, F64).T).reshape(n, n_kv_heads, head_dim)
+        Kn = rope_rotate(Kn, np.arange(n)[:, None], base)
+        Ko = np.asarray(Ks, F64).reshape(n, n_kv_heads, head_dim)
+        dot = np.sum(Kn * Ko, axis=-1)
+        den = np.sqrt(np.sum(Kn * Kn, axis=-1)) * np.sqrt(np.sum(Ko * Ko, axis=-1))
+        acc += np.sum(dot / np.maximum(den, 1e-30), axis=1)
+    return 1.0 - acc / (n_layers * n_kv_heads)
 
 
 # --------------------------------------------------------------------------

@@ -606,3 +606,61 @@ def test_attention_mass_invariants():
     # no query token: nothing spread; no context: nothing to score
     assert np.array_equal(orc.attention_mass_scores(H[:0], Wq, K, hq, hkv, d, 1e4), np.zeros(n))
     assert orc.attention_mass_scores(H, Wq, K[:0], hq, hkv, d, 1e4).shape == (0,)
+
+
+# Key deviation over layers (KVBoost section 4.6.2, Alg. 2 step 2 as printed)
+def _rot2(angle, scale=1.0):
+    return scale * np.array([math.cos(angle), math.sin(angle)])
+
+
+def test_key_deviation_hand_worked_d2():
+    # d = 2 (theta_0 = 1 radian per position), W_K = I, x_t = (1, 0): the fresh
+    # key of token t is (cos t, sin t).  Stale keys turned further by phi_t
+    # (and scaled, which a cosine ignores) give delta_t = 1 - cos(phi_t).
+    phi, scale = [0.0, math.pi / 3, math.pi], [1.0, 2.0, 0.5]
+    H = np.array([[1.0, 0.0]] * 3)
+    K = np.stack([_rot2(t + p, s) for t, (p, s) in enumerate(zip(phi, scale))])[:, None, :]
+    got = orc.key_deviation_scores([H], [np.eye(2)], [K], 1, 2, 1e4)
+    assert np.allclose(got, [0.0, 0.5, 2.0], atol=1e-12)
+    # a second layer whose stale keys are all a quarter turn off (delta 1):
+    # the two layers' deviations are averaged
+    K2 = np.stack([_rot2(t + math.pi / 2) for t in range(3)])[:, None, :]
+    got2 = orc.key_deviation_scores([H, H], [np.eye(2), np.eye(2)], [K, K2], 1, 2, 1e4)
+    assert np.allclose(got2, [0.5, 0.75, 1.5], atol=1e-12)
+    # a zero stale key has cosine 0
+    got3 = orc.key_deviation_scores([H], [np.eye(2)], [0 * K], 1, 2, 1e4)
+    assert np.allclose(got3, [1.0, 1.0, 1.0], atol=1e-12)
+
+
+def test_key_deviation_averages_over_key_heads():
+    # Hkv = 2 heads of d = 2 reading the same x: head 0 matches, head 1 is a
+    # quarter turn off -> 1 - (1 + 0) / 2
+    H = np.array([[1.0, 0.0]] * 2)
+    Wk = np.vstack([np.eye(2), np.eye(2)])
+    K = np.stack([np.stack([_rot2(t), _rot2(t + math.pi / 2)]) for t in range(2)])
+    got = orc.key_deviation_scores([H], [Wk], [K], 2, 2, 1e4)
+    assert np.allclose(got, [0.5, 0.5], atol=1e-12)
+
+
+def test_key_deviation_zero_on_unperturbed_stitched_cache():
+    # QCFuse Eqs. 3-4 with KVBoost Eq. 3: a stitched PIC key of an unperturbed
+    # token equals its fresh key at the request position, in every layer;
+    # perturbing the probe's input of some tokens raises exactly those
+    rng = _rng(41)
+    lens = [5, 9, 4]
+    n = sum(lens)
+    layers = []
+    for l in range(3):
+        Wq, Wk, Wv = _tiny_model(50 + l)
+        H = rng.standard_normal((n, 32))
+        starts = np.cumsum([0] + lens[:-1])
+        Kc, Vc = zip(*[orc.pic_precompute(H[s:s + ln], Wk, Wv, 2, 8, 1e4)
+                       for s, ln in zip(starts, lens)])
+        K, _ = orc.stitch_rerotate(list(Kc), list(Vc), 1e4)
+        layers.append((H, Wk, K))
+    Hs, Ws, Ks = zip(*layers)
+    assert np.max(np.abs(orc.key_deviation_scores(Hs, Ws, Ks, 2, 8, 1e4))) < 1e-12
+    bumped = [h.copy() for h in Hs]
+    bumped[1][[3, 11]] += 0.5 * rng.standard_normal((2, 32))
+    d = orc.key_deviation_scores(bumped, Ws, Ks, 2, 8, 1e4)
+    assert np.all(d[[3, 11]] > 1e-6) and np.max(np.abs(np.delete(d, [3, 11]))) < 1e-12
