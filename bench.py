@@ -90,6 +90,22 @@ def _traffic(kernel):
     return float(v) if v is not None else None
 
 
+def max_over_ranks(ms: float, ws: int, device) -> float:
+    """The slowest rank's time: every rank contributes its own and all get the
+    maximum (one all-reduce of a single number; nothing on the data path)."""
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(ws: int, units_per_step: float, steps: int, ms: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest
+    rank's time (each rank runs its own copy of the workload)."""
+    return ws * units_per_step * steps / (ms / 1e3)
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -327,11 +343,7 @@ def native_run(args, ws, rank, local):
     if ws > 1:
         dist.barrier()
     clocks = sampler.stop()
-    ms = ev0.elapsed_time(ev1)
-    t = torch.tensor([ms], device="cuda", dtype=torch.float64)
-    if ws > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), ws, "cuda")
     for b in sets:
         fk.check_errors(b.ws)
 
@@ -507,12 +519,8 @@ def native_run(args, ws, rank, local):
             stream.wait_event(read[s])                     # after the last read-back
         e1.record(stream)
         torch.cuda.synchronize()
-        ems = e0.elapsed_time(e1)
-        te = torch.tensor([ems], device="cuda", dtype=torch.float64)
-        if ws > 1:
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        ems = float(te.item())
-        e2e = {"value": ws * T * args.e2e_steps / (ems / 1e3), "unit": UNIT,
+        ems = max_over_ranks(e0.elapsed_time(e1), ws, "cuda")
+        e2e = {"value": job_rate(ws, T, args.e2e_steps, ems), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "steps": args.e2e_steps,
                "what": "pinned-host chunk K/V caches and H copied in, fuse_layer_step, O and idx "
@@ -531,7 +539,7 @@ def native_run(args, ws, rank, local):
     cfg_json["recomputed_rows"] = int(R)
     cfg_json["parallelism"] = f"replicas x{ws}" if ws > 1 else "single GPU"
     out = {
-        "metric": METRIC, "value": ws * T * args.steps / (ms / 1e3), "unit": UNIT, "n_gpus": ws,
+        "metric": METRIC, "value": job_rate(ws, T, args.steps, ms), "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded Gaussian draws; chunk caches from fuse_pic_precompute)",
