@@ -9,6 +9,8 @@
  *   [KVBoost] "KVBoost: Chunk-Level KV Cache Reuse with Deviation-Guided
  *             Recomputation", sections 3.1-3.2 (Eqs. 1-3), 4.5 (Eq. 7),
  *             4.6.2 (Alg. 2, CacheBlendRecompute).
+ *   [PCR]     "PCR: A Prefetch-Enhanced Cache Reuse System for Low-Latency
+ *             RAG Serving", layer-wise overlapping (Figure 8).
  *
  * Conventions shared by every call
  * --------------------------------
@@ -293,6 +295,74 @@ fuse_status_t fuse_stack_step(const fuse_layer_desc_t* desc, const fuse_requests
                               int32_t n_layers, int32_t score_layer, const fuse_layer_io_t* layers,
                               int32_t* idx, float* score, void* ws, size_t ws_bytes,
                               fuse_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Layer-wise loading overlapped with the layers' fusion ([QCFuse] Figure 9,
+ * pipeline cache fusion: each layer starts from its loaded PIC entries while
+ * later layers' caches are still loading; [PCR] layer-wise overlapping,
+ * Figure 8: computation starts once the first layer's cache is loaded).     */
+
+/* One host-to-device copy: `bytes` from host memory `src` to device memory
+ * `dst`.  The copy overlaps kernels only when `src` is page-locked. */
+typedef struct {
+  void* dst;
+  const void* src;
+  size_t bytes;
+} fuse_copy_t;
+
+/* The uploads of one layer of a streamed stack: the copies that fill its
+ * staging slot (the device buffers its chunk table points into, and any
+ * other input the caller streams through the slot). */
+typedef struct {
+  int32_t slot;                /* 0 .. n_slots - 1 */
+  int32_t n_copies;
+  const fuse_copy_t* copies;   /* host [n_copies] */
+} fuse_layer_upload_t;
+
+/* fuse_stack_step with every layer's inputs uploaded into a ring of n_slots
+ * staging slots on copy_stream while earlier layers compute on stream.
+ * Layers run in the order: score_layer (stitch, score, select, recompute),
+ * then every other layer in index order (stitch, recompute).  The layers
+ * share only the selection, so every output equals fuse_stack_step's on the
+ * uploaded data.  Layer l's copies start after every earlier layer that
+ * used the same slot has finished on stream; layer l's kernels start after
+ * its copies.  With n_slots >= 2 one layer's upload overlaps the previous
+ * layer's kernels.  The schedule is the one fuse_stack_pipeline_plan
+ * returns.  The call creates and destroys its own CUDA events (2 * n_slots,
+ * n_slots <= 64); everything else is as for fuse_stack_step.  copy_stream
+ * and stream must differ for any overlap (the same stream runs everything
+ * in order).  Argument errors are returned before any copy or launch. */
+fuse_status_t fuse_stack_step_streamed(const fuse_layer_desc_t* desc, const fuse_requests_t* reqs,
+                                       int32_t n_layers, int32_t score_layer,
+                                       const fuse_layer_io_t* layers,
+                                       const fuse_layer_upload_t* uploads, int32_t n_slots,
+                                       fuse_stream_t copy_stream, int32_t* idx, float* score,
+                                       void* ws, size_t ws_bytes, fuse_stream_t stream);
+
+/* The operations of a streamed stack, in issue order. */
+typedef enum {
+  FUSE_OP_WAIT_FREE = 0,    /* copy stream waits until the slot's last user finished  */
+  FUSE_OP_COPY = 1,         /* copy stream: the layer's uploads                        */
+  FUSE_OP_MARK_READY = 2,   /* copy stream: the slot's data is in place               */
+  FUSE_OP_WAIT_READY = 3,   /* compute stream waits for the slot's data               */
+  FUSE_OP_COMPUTE = 4,      /* compute stream: the layer's kernels                      */
+  FUSE_OP_MARK_FREE = 5     /* compute stream: the layer is done with the slot          */
+} fuse_pipeline_op_kind_t;
+
+typedef struct {
+  int32_t kind;    /* fuse_pipeline_op_kind_t */
+  int32_t layer;
+  int32_t slot;
+} fuse_pipeline_op_t;
+
+/* The schedule of fuse_stack_step_streamed (host only, no CUDA call):
+ * slot_of_layer[l] in 0 .. n_slots-1 for every layer.  Writes at most
+ * max_ops operations to ops and their count to *n_ops (5 per layer, plus a
+ * FUSE_OP_WAIT_FREE before every reuse of a slot); FUSE_ERR_WORKSPACE when
+ * max_ops is too small (*n_ops then holds the count needed). */
+fuse_status_t fuse_stack_pipeline_plan(int32_t n_layers, int32_t score_layer,
+                                       const int32_t* slot_of_layer, int32_t n_slots,
+                                       fuse_pipeline_op_t* ops, int32_t max_ops, int32_t* n_ops);
 
 /* Position-independent chunk caches, [QCFuse] Eq. 3 with one projection layer
  * standing in for the model: for every chunk i and local row r,

@@ -426,6 +426,56 @@ fuse_status_t do_stitch_score_select(const fuse_layer_desc_t& d, const fuse_chun
   return do_reduce_topk(d, r, info, score, idx, ws, s);
 }
 
+// Schedule of a streamed stack (QCFuse Figure 9; PCR layer-wise overlapping).
+// Layers run in the order score layer, then the others by index.  The
+// copies are issued as early as the slots allow: a layer's copies follow the
+// previous user of its slot (in that order) once that user's release has
+// been issued, and copies stay in layer order.  Because a slot's next copy is
+// issued only after its current user's release, every wait binds to the
+// record it is meant for (a CUDA wait takes the event's latest record).
+constexpr int kMaxSlots = 64;
+
+fuse_status_t stack_plan(int n_layers, int score_layer, const int32_t* slot_of_layer, int n_slots,
+                         std::vector<fuse_pipeline_op_t>& ops) {
+  if (n_layers <= 0 || score_layer < 0 || score_layer >= n_layers || n_slots <= 0 ||
+      n_slots > kMaxSlots || !slot_of_layer)
+    return FUSE_ERR_INVALID_ARG;
+  for (int l = 0; l < n_layers; ++l)
+    if (slot_of_layer[l] < 0 || slot_of_layer[l] >= n_slots) return FUSE_ERR_INVALID_ARG;
+  std::vector<int> order;
+  order.push_back(score_layer);
+  for (int l = 0; l < n_layers; ++l)
+    if (l != score_layer) order.push_back(l);
+  std::vector<int> last_user(n_slots, -1);     // order index of the slot's latest copy
+  std::vector<char> released(n_layers, 0);     // order index -> release issued
+  ops.clear();
+  auto op = [&](int kind, int l) { ops.push_back(fuse_pipeline_op_t{kind, l, slot_of_layer[l]}); };
+  int next_copy = 0;
+  auto issue_copies = [&] {
+    while (next_copy < n_layers) {
+      const int l = order[next_copy];
+      const int sl = slot_of_layer[l];
+      const int prev = last_user[sl];
+      if (prev >= 0 && !released[prev]) break;
+      if (prev >= 0) op(FUSE_OP_WAIT_FREE, l);
+      op(FUSE_OP_COPY, l);
+      op(FUSE_OP_MARK_READY, l);
+      last_user[sl] = next_copy;
+      ++next_copy;
+    }
+  };
+  issue_copies();
+  for (int i = 0; i < n_layers; ++i) {
+    const int l = order[i];
+    op(FUSE_OP_WAIT_READY, l);
+    op(FUSE_OP_COMPUTE, l);
+    op(FUSE_OP_MARK_FREE, l);
+    released[i] = 1;
+    issue_copies();
+  }
+  return FUSE_OK;
+}
+
 }  // namespace
 }  // namespace fusekv
 
@@ -631,6 +681,104 @@ fuse_status_t fuse_stack_step(const fuse_layer_desc_t* desc, const fuse_requests
     if (st != FUSE_OK) return st;
   }
   return FUSE_OK;
+}
+
+fuse_status_t fuse_stack_pipeline_plan(int32_t n_layers, int32_t score_layer,
+                                       const int32_t* slot_of_layer, int32_t n_slots,
+                                       fuse_pipeline_op_t* ops, int32_t max_ops, int32_t* n_ops) {
+  if (!n_ops || max_ops < 0 || (max_ops > 0 && !ops)) return FUSE_ERR_INVALID_ARG;
+  std::vector<fuse_pipeline_op_t> plan;
+  const fuse_status_t st = stack_plan(n_layers, score_layer, slot_of_layer, n_slots, plan);
+  if (st != FUSE_OK) return st;
+  *n_ops = (int32_t)plan.size();
+  if ((int64_t)plan.size() > max_ops) return FUSE_ERR_WORKSPACE;
+  std::copy(plan.begin(), plan.end(), ops);
+  return FUSE_OK;
+}
+
+fuse_status_t fuse_stack_step_streamed(const fuse_layer_desc_t* desc, const fuse_requests_t* reqs,
+                                       int32_t n_layers, int32_t score_layer,
+                                       const fuse_layer_io_t* layers,
+                                       const fuse_layer_upload_t* uploads, int32_t n_slots,
+                                       fuse_stream_t copy_stream, int32_t* idx, float* score,
+                                       void* ws, size_t ws_bytes, fuse_stream_t stream) {
+  fuse_status_t st = check_desc(desc);
+  if (st != FUSE_OK) return st;
+  ReqInfo info;
+  st = check_reqs(reqs, &info);
+  if (st != FUSE_OK) return st;
+  if (n_layers <= 0 || !layers || !uploads || score_layer < 0 || score_layer >= n_layers)
+    return FUSE_ERR_INVALID_ARG;
+  std::vector<int> max_len(n_layers);
+  std::vector<int32_t> slot_of(n_layers);
+  for (int l = 0; l < n_layers; ++l) {
+    const fuse_layer_io_t& L = layers[l];
+    LayerArgs la{L.chunks, L.H, L.Wq, L.Wk, L.Wv, L.Kf, L.Vf, L.O};
+    st = check_layer(*desc, info, la, l == score_layer, idx, score, ws, ws_bytes, &max_len[l]);
+    if (st != FUSE_OK) return st;
+    const fuse_layer_upload_t& U = uploads[l];
+    if (U.n_copies < 0 || (U.n_copies > 0 && !U.copies)) return FUSE_ERR_INVALID_ARG;
+    for (int c = 0; c < U.n_copies; ++c)
+      if (U.copies[c].bytes > 0 && (!U.copies[c].dst || !U.copies[c].src))
+        return FUSE_ERR_INVALID_ARG;
+    slot_of[l] = U.slot;
+  }
+  std::vector<fuse_pipeline_op_t> plan;
+  st = stack_plan(n_layers, score_layer, slot_of.data(), n_slots, plan);
+  if (st != FUSE_OK) return st;
+
+  cudaStream_t s = (cudaStream_t)stream, cs = (cudaStream_t)copy_stream;
+  std::vector<cudaEvent_t> ready(n_slots, nullptr), freed(n_slots, nullptr);
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i < n_slots && e == cudaSuccess; ++i) {
+    e = cudaEventCreateWithFlags(&ready[i], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&freed[i], cudaEventDisableTiming);
+  }
+  st = cuda_status(e);
+  for (size_t i = 0; i < plan.size() && st == FUSE_OK; ++i) {
+    const fuse_pipeline_op_t& o = plan[i];
+    const fuse_layer_io_t& L = layers[o.layer];
+    switch (o.kind) {
+      case FUSE_OP_WAIT_FREE:
+        st = cuda_status(cudaStreamWaitEvent(cs, freed[o.slot], 0));
+        break;
+      case FUSE_OP_COPY: {
+        const fuse_layer_upload_t& U = uploads[o.layer];
+        for (int c = 0; c < U.n_copies && st == FUSE_OK; ++c)
+          if (U.copies[c].bytes > 0)
+            st = cuda_status(cudaMemcpyAsync(U.copies[c].dst, U.copies[c].src, U.copies[c].bytes,
+                                             cudaMemcpyDefault, cs));
+        break;
+      }
+      case FUSE_OP_MARK_READY:
+        st = cuda_status(cudaEventRecord(ready[o.slot], cs));
+        break;
+      case FUSE_OP_WAIT_READY:
+        st = cuda_status(cudaStreamWaitEvent(s, ready[o.slot], 0));
+        break;
+      case FUSE_OP_COMPUTE:
+        if (o.layer == score_layer)
+          st = do_stitch_score_select(*desc, *L.chunks, max_len[o.layer], *reqs, info, L.H, L.Wv,
+                                      L.Kf, L.Vf, score, idx, ws, s);
+        else
+          st = do_stitch(*desc, *L.chunks, max_len[o.layer], L.Kf, L.Vf, ws, s);
+        if (st == FUSE_OK)
+          st = do_recompute(*desc, *reqs, info, L.H, L.Wq, L.Wk, L.Wv, idx, L.Kf, L.Vf, L.O, ws, s);
+        break;
+      case FUSE_OP_MARK_FREE:
+        st = cuda_status(cudaEventRecord(freed[o.slot], s));
+        break;
+      default:
+        st = FUSE_ERR_INVALID_ARG;
+    }
+  }
+  // destroying an event with work still pending is allowed: it is released
+  // once that work completes
+  for (int i = 0; i < n_slots; ++i) {
+    if (ready[i]) cudaEventDestroy(ready[i]);
+    if (freed[i]) cudaEventDestroy(freed[i]);
+  }
+  return st;
 }
 
 fuse_status_t fuse_pic_precompute(const fuse_layer_desc_t* desc, const fuse_chunks_t* chunks,

@@ -71,6 +71,21 @@ class LayerIO(_c.Structure):
                 ("O", _c.c_void_p)]
 
 
+class Copy(_c.Structure):
+    _fields_ = [("dst", _c.c_void_p), ("src", _c.c_void_p), ("bytes", _c.c_size_t)]
+
+
+class LayerUpload(_c.Structure):
+    _fields_ = [("slot", _c.c_int32), ("n_copies", _c.c_int32), ("copies", _c.c_void_p)]
+
+
+class PipelineOp(_c.Structure):
+    _fields_ = [("kind", _c.c_int32), ("layer", _c.c_int32), ("slot", _c.c_int32)]
+
+
+OP_WAIT_FREE, OP_COPY, OP_MARK_READY, OP_WAIT_READY, OP_COMPUTE, OP_MARK_FREE = range(6)
+
+
 class Totals(_c.Structure):
     _fields_ = [("n_tok", _c.c_int64), ("n_ctx", _c.c_int64), ("n_sel", _c.c_int64),
                 ("n_out", _c.c_int64), ("max_ctx", _c.c_int32), ("max_tok", _c.c_int32)]
@@ -104,6 +119,10 @@ _SIGS = {
     "fuse_layer_step": (_c.c_int, [_P, _P, _P, _P, _P, _P, _P, _c.c_int32, _P, _P, _P, _P, _P,
                                    _P, _c.c_size_t, _P]),
     "fuse_pic_precompute": (_c.c_int, [_P, _P, _P, _P, _P, _P, _c.c_size_t, _P]),
+    "fuse_stack_step_streamed": (_c.c_int, [_P, _P, _c.c_int32, _c.c_int32, _P, _P, _c.c_int32,
+                                            _P, _P, _P, _P, _c.c_size_t, _P]),
+    "fuse_stack_pipeline_plan": (_c.c_int, [_c.c_int32, _c.c_int32, _P, _c.c_int32, _P,
+                                            _c.c_int32, _c.POINTER(_c.c_int32)]),
     "fuse_stack_step": (_c.c_int, [_P, _P, _c.c_int32, _c.c_int32, _P, _P, _P, _P, _c.c_size_t, _P]),
     "fuse_check_errors": (_c.c_int, [_P, _P, _c.POINTER(_c.c_uint32)]),
     "fuse_static_select_count": (_c.c_int, [_P, _P, _c.c_int32, _c.c_int32, _P]),
@@ -328,6 +347,48 @@ def stack_step(desc, reqs: RequestTable, layers, score_layer: int, idx, score, w
     _check(load().fuse_stack_step(_c.byref(desc), _c.byref(reqs.c), len(layers), int(score_layer),
                                   arr, _ptr(idx), _ptr(score), _ptr(ws), ws.numel(),
                                   _stream(stream)), "fuse_stack_step")
+
+
+def stack_pipeline_plan(n_layers: int, score_layer: int, slot_of_layer: Sequence[int],
+                        n_slots: int) -> list:
+    """The issue order of ``stack_step_streamed``: (kind, layer, slot) tuples."""
+    slots = (_c.c_int32 * max(1, n_layers))(*[int(x) for x in slot_of_layer])
+    n = _c.c_int32(0)
+    st = load().fuse_stack_pipeline_plan(int(n_layers), int(score_layer), slots, int(n_slots),
+                                         None, 0, _c.byref(n))
+    if st not in (FUSE_OK, FUSE_ERR_WORKSPACE):
+        _check(st, "fuse_stack_pipeline_plan")
+    ops = (PipelineOp * max(1, n.value))()
+    _check(load().fuse_stack_pipeline_plan(int(n_layers), int(score_layer), slots, int(n_slots),
+                                           ops, n.value, _c.byref(n)), "fuse_stack_pipeline_plan")
+    return [(o.kind, o.layer, o.slot) for o in ops[:n.value]]
+
+
+def stack_step_streamed(desc, reqs: RequestTable, layers, score_layer: int, uploads, n_slots: int,
+                        idx, score, ws, copy_stream, stream=None):
+    """``uploads[l]``: (slot, [(dst tensor, src tensor), ...]) -- whole-tensor
+    copies that fill layer l's staging slot.  ``copy_stream``: a
+    ``torch.cuda.Stream`` other than ``stream``."""
+    arr = (LayerIO * len(layers))()
+    for i, b in enumerate(layers):
+        arr[i] = LayerIO(_c.addressof(b.chunks.c), _ptr(b.H), _ptr(b.Wq), _ptr(b.Wk), _ptr(b.Wv),
+                         _ptr(b.Kf), _ptr(b.Vf), _ptr(b.O))
+    keep = []
+    ups = (LayerUpload * len(layers))()
+    for i, (slot, pairs) in enumerate(uploads):
+        cs = (Copy * max(1, len(pairs)))()
+        for j, (dst, src) in enumerate(pairs):
+            nb = src.numel() * src.element_size()
+            if dst.numel() * dst.element_size() != nb:
+                raise ValueError("a copy's source and destination differ in size")
+            cs[j] = Copy(_ptr(dst), _ptr(src), nb)
+        keep.append(cs)
+        ups[i] = LayerUpload(int(slot), len(pairs), _c.addressof(cs))
+    _check(load().fuse_stack_step_streamed(_c.byref(desc), _c.byref(reqs.c), len(layers),
+                                           int(score_layer), arr, ups, int(n_slots),
+                                           _stream(copy_stream), _ptr(idx), _ptr(score),
+                                           _ptr(ws), ws.numel(), _stream(stream)),
+           "fuse_stack_step_streamed")
 
 
 def pic_precompute(desc, chunks: ChunkTable, H_clean, Wk, Wv, ws, stream=None):

@@ -211,3 +211,35 @@ def test_attention_mass_argument_errors(fk):
     # the packed query rows (Q, RoPE table, tile statistics) need workspace
     t0 = fk.plan_requests([256], [0], 0.3, device=None)
     assert need > fk.workspace_size(desc, t0)
+
+
+def test_stack_step_streamed_argument_errors(fk):
+    # one valid layer built from aligned stand-in pointers; each call below
+    # carries one error in its uploads, found before any copy or launch
+    lib = fk.load()
+    desc = _desc(fk)
+    t = fk.plan_requests([64], [8], 0.25, device=None)
+    t.c.d_req = 16
+    e = fk.Chunk()
+    e.k, e.v, e.dst_row, e.pos, e.len = 4096, 4096, 0, 0, 64
+    tab = fk.ChunkTable([e], fk.FUSE_KV_CONTIGUOUS, fk.FUSE_F32, device=None)
+    tab.c.d_chunks = 4096
+    A = 1 << 20
+    layers = (fk.LayerIO * 1)(fk.LayerIO(ctypes.addressof(tab.c), A, A, A, A, A, A, A))
+    need = fk.workspace_size(desc, t)
+
+    def call(uploads, n_slots):
+        return lib.fuse_stack_step_streamed(ctypes.byref(desc), ctypes.byref(t.c), 1, 0, layers,
+                                            uploads, n_slots, None, A, A, A, need, None)
+
+    assert call(None, 1) == fk.FUSE_ERR_INVALID_ARG
+    bad = (fk.Copy * 1)(fk.Copy(A, None, 256))                      # no source
+    ups = (fk.LayerUpload * 1)(fk.LayerUpload(0, 1, ctypes.addressof(bad)))
+    assert call(ups, 1) == fk.FUSE_ERR_INVALID_ARG
+    ups2 = (fk.LayerUpload * 1)(fk.LayerUpload(0, 2, None))           # copies missing
+    assert call(ups2, 1) == fk.FUSE_ERR_INVALID_ARG
+    ok = (fk.Copy * 1)(fk.Copy(A, A, 256))
+    ups3 = (fk.LayerUpload * 1)(fk.LayerUpload(1, 1, ctypes.addressof(ok)))   # slot 1 of 1
+    assert call(ups3, 1) == fk.FUSE_ERR_INVALID_ARG
+    ups4 = (fk.LayerUpload * 1)(fk.LayerUpload(0, 1, ctypes.addressof(ok)))
+    assert call(ups4, 0) == fk.FUSE_ERR_INVALID_ARG                   # no slot at all
