@@ -61,7 +61,7 @@ typedef enum {
   FUSE_OK = 0,
   FUSE_ERR_INVALID_ARG = 1,   /* null pointer, bad size, inconsistent tables      */
   FUSE_ERR_MISALIGNED = 2,    /* a pointer or row stride not aligned to 16 bytes   */
-  FUSE_ERR_UNSUPPORTED = 3,   /* a valid request this build does not handle        */
+  FUSE_ERR_UNSUPPORTED = 3,   /* a valid request the library does not handle       */
   FUSE_ERR_WORKSPACE = 4,     /* workspace null or smaller than fuse_workspace_size */
   FUSE_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed              */
   FUSE_ERR_TIMEOUT = 6,       /* (device) a bounded wait gave up                   */
