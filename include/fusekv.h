@@ -217,6 +217,26 @@ fuse_status_t fuse_score_deviation(const fuse_layer_desc_t* desc, const fuse_req
                                    const void* H, const void* Wv, const void* Vf, float* score,
                                    void* ws, size_t ws_bytes, fuse_stream_t stream);
 
+/* Key deviation, one layer's term of [KVBoost] Alg. 2 step 2 as printed,
+ *   delta_t = 1 - (1/(L Hkv)) sum_{l,h} cos(K~_t^(l,h), K_t^(l,h)),
+ * which is the mean over the L layers of 1 - (1/Hkv) sum_h cos.  For every
+ * context token t of every request, with the fresh key at the token's
+ * request position (where the probe pass puts it),
+ *   K~_t = R^t W_K x_t  (x_t = H[row0 + t]),   K_t = Kf[row0 + t] (stitched),
+ *   v_t  = weight * (1 - (1/Hkv) sum_h cos(K~_t[h], K_t[h])),
+ * each cosine's denominator clamped at 1e-30; accumulate == 0 writes v_t to
+ * score[score0 + t], accumulate != 0 adds it.  One call per layer with
+ * weight = 1/L (the first with accumulate == 0) leaves delta_t in score.
+ * The fresh keys are materialised in desc->dtype (a bf16 layer rounds them
+ * to bf16); cosines and sums are fp32, heads summed in order, no atomics.
+ * Kf and H are only read.  Needs the workspace of fuse_workspace_size.
+ * FUSE_ERR_INVALID_ARG for a weight that is not finite;
+ * FUSE_ERR_UNSUPPORTED for more than 65535 requests. */
+fuse_status_t fuse_score_key_deviation(const fuse_layer_desc_t* desc, const fuse_requests_t* reqs,
+                                       const void* H, const void* Wk, const void* Kf, float weight,
+                                       int32_t accumulate, float* score, void* ws,
+                                       size_t ws_bytes, fuse_stream_t stream);
+
 /* Query-aware importance of every context token ([QCFuse] section 3.2.1,
  * Eqs. 9-10, the full-view attention mass; section 3.4.2, Eq. 20, its sum
  * over the critical layers).  For request r with N = N_r context and

@@ -29,6 +29,13 @@ cudaError_t launch_project_query_tc(const fuse_layer_desc_t& d, int64_t n_rows, 
                                     const void* Wq, void* Q, const void* Hs, uint32_t* err,
                                     cudaStream_t s);
 bool tc_attention_supported(const fuse_layer_desc_t& desc);
+// Key deviation (csrc/key_deviation.cu).
+cudaError_t launch_key_rows(const fuse_requests_t& reqs, int max_tok, const RopeFreqs& freqs,
+                            int head_dim, int64_t n_rows, WorkRow* rows, float2* rope,
+                            cudaStream_t s);
+cudaError_t launch_key_cosine(const fuse_layer_desc_t& d, const fuse_requests_t& reqs, int max_ctx,
+                              const void* Kn, const void* Kf, float weight, int accumulate,
+                              float* score, cudaStream_t s);
 int attention_rtile(const fuse_layer_desc_t& d);
 size_t attention_tiles_bytes(int64_t n_out, int n_req);
 cudaError_t launch_attention_tc(const fuse_layer_desc_t& d, const fuse_requests_t& reqs,
@@ -156,6 +163,7 @@ fuse_status_t check_chunks(const fuse_layer_desc_t& d, const fuse_chunks_t* c, i
 struct WsLayout {
   size_t partial, keys, map, rows, rope, q, hs, tiles;
   size_t mrows, mrope, mq, mhs, mstats, mnorm, qoff;   // query-aware scorer
+  size_t krows, krope, kn;                             // key deviation
   size_t total;
 };
 
@@ -186,6 +194,9 @@ WsLayout ws_layout(const fuse_layer_desc_t& d, const ReqInfo& info) {
   L.mstats = take(nq * d.n_q_heads * (size_t)mass_key_tiles(t.max_ctx) * sizeof(float2));
   L.mnorm = take(nq * d.n_q_heads * sizeof(float2));
   L.qoff = take((size_t)n_req * sizeof(int32_t));
+  L.krows = take((size_t)t.n_tok * sizeof(WorkRow));
+  L.krope = take((size_t)t.n_tok * (d.head_dim / 2) * sizeof(float2));
+  L.kn = take((size_t)t.n_tok * d.n_kv_heads * d.head_dim * es);
   L.total = off;
   return L;
 }
@@ -360,6 +371,44 @@ fuse_status_t do_mass(const fuse_layer_desc_t& d, const fuse_requests_t& r, cons
       return launch_attention_mass(d, r, info.tot.max_ctx, nq, rows, qoff, Q, Kf,
                                    at<float2>(ws, L.mstats), at<float2>(ws, L.mnorm),
                                    at<float>(ws, L.partial), score, accumulate, s);
+    });
+  return cuda_status(e);
+}
+
+// Key deviation, one layer's term (KVBoost Alg. 2 step 2): fresh keys of
+// every packed row at its request position through the query-state
+// projection with the key heads in place of the query heads, then the
+// per-token cosines against the stitched keys.
+fuse_status_t do_key_deviation(const fuse_layer_desc_t& d, const fuse_requests_t& r,
+                               const ReqInfo& info, const void* H, const void* Wk, const void* Kf,
+                               float weight, int accumulate, float* score, void* ws,
+                               cudaStream_t s) {
+  const WsLayout L = ws_layout(d, info);
+  if (info.tot.n_ctx == 0 || info.tot.max_ctx == 0) return FUSE_OK;
+  const int64_t n = info.tot.n_tok;
+  WorkRow* rows = at<WorkRow>(ws, L.krows);
+  float2* rope = at<float2>(ws, L.krope);
+  void* Kn = at<void>(ws, L.kn);
+  uint32_t* err = at<uint32_t>(ws, 0);
+  fuse_layer_desc_t dk = d;
+  dk.n_q_heads = d.n_kv_heads;
+  const RopeFreqs f = make_freqs(d);
+  cudaError_t e = traced("key_rows", s, [&] {
+    return launch_key_rows(r, info.tot.max_tok, f, d.head_dim, n, rows, rope, s);
+  });
+  if (e == cudaSuccess) {
+    if (tc_gemm_supported(dk))
+      e = traced("key_gemm_tc", s, [&] {
+        return launch_project_query_tc(dk, n, rope, Wk, Kn, H, err, s);
+      });
+    else
+      e = traced("key_gemm_simt", s, [&] {
+        return launch_project_query_simt(dk, n, rows, rope, H, Wk, Kn, err, s);
+      });
+  }
+  if (e == cudaSuccess)
+    e = traced("key_cosine", s, [&] {
+      return launch_key_cosine(d, r, info.tot.max_ctx, Kn, Kf, weight, accumulate, score, s);
     });
   return cuda_status(e);
 }
@@ -584,6 +633,26 @@ fuse_status_t fuse_score_attention_mass(const fuse_layer_desc_t* desc, const fus
   st = check_ws(ws, ws_bytes, ws_layout(*desc, info).total);
   if (st != FUSE_OK) return st;
   return do_mass(*desc, *reqs, info, H, Wq, Kf, score, accumulate, ws, (cudaStream_t)stream);
+}
+
+fuse_status_t fuse_score_key_deviation(const fuse_layer_desc_t* desc, const fuse_requests_t* reqs,
+                                      const void* H, const void* Wk, const void* Kf, float weight,
+                                      int32_t accumulate, float* score, void* ws, size_t ws_bytes,
+                                      fuse_stream_t stream) {
+  fuse_status_t st = check_desc(desc);
+  if (st != FUSE_OK) return st;
+  ReqInfo info;
+  st = check_reqs(reqs, &info);
+  if (st != FUSE_OK) return st;
+  if (info.n_req > 65535) return FUSE_ERR_UNSUPPORTED;
+  if (!std::isfinite(weight)) return FUSE_ERR_INVALID_ARG;
+  if (info.tot.n_ctx > 0 && (!H || !Wk || !Kf || !score)) return FUSE_ERR_INVALID_ARG;
+  if (!aligned16(H) || !aligned16(Wk) || !aligned16(Kf) || !aligned16(score))
+    return FUSE_ERR_MISALIGNED;
+  st = check_ws(ws, ws_bytes, ws_layout(*desc, info).total);
+  if (st != FUSE_OK) return st;
+  return do_key_deviation(*desc, *reqs, info, H, Wk, Kf, weight, accumulate, score, ws,
+                          (cudaStream_t)stream);
 }
 
 fuse_status_t fuse_select_topk(const fuse_requests_t* reqs, const float* score, int32_t* idx,

@@ -113,6 +113,8 @@ _SIGS = {
     "fuse_score_deviation": (_c.c_int, [_P, _P, _P, _P, _P, _P, _P, _c.c_size_t, _P]),
     "fuse_score_attention_mass": (_c.c_int, [_P, _P, _P, _P, _P, _c.c_int32, _P, _P,
                                              _c.c_size_t, _P]),
+    "fuse_score_key_deviation": (_c.c_int, [_P, _P, _P, _P, _P, _c.c_float, _c.c_int32, _P,
+                                            _P, _c.c_size_t, _P]),
     "fuse_select_topk": (_c.c_int, [_P, _P, _P, _P, _c.c_size_t, _P]),
     "fuse_recompute_selected": (_c.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                            _c.c_size_t, _P]),
@@ -287,6 +289,17 @@ def score_attention_mass(desc, reqs: RequestTable, H, Wq, Kf, score, ws, accumul
                                             _ptr(Kf), int(bool(accumulate)), _ptr(score),
                                             _ptr(ws), ws.numel(), _stream(stream)),
            "fuse_score_attention_mass")
+
+
+def score_key_deviation(desc, reqs: RequestTable, H, Wk, Kf, score, ws, weight=1.0,
+                        accumulate=False, stream=None):
+    """KVBoost Alg. 2 step 2 on the keys, one layer's term:
+    ``score (+)= weight * (1 - mean_h cos(R^t W_K x_t, Kf[t]))``; ``weight=1/L``
+    over L layers (accumulating after the first) gives the printed delta."""
+    _check(load().fuse_score_key_deviation(_c.byref(desc), _c.byref(reqs.c), _ptr(H), _ptr(Wk),
+                                           _ptr(Kf), float(weight), int(bool(accumulate)),
+                                           _ptr(score), _ptr(ws), ws.numel(), _stream(stream)),
+           "fuse_score_key_deviation")
 
 
 SEL_CHUNK_HEAD, SEL_SEAM_TAIL = 0, 1

@@ -243,3 +243,26 @@ def test_stack_step_streamed_argument_errors(fk):
     assert call(ups3, 1) == fk.FUSE_ERR_INVALID_ARG
     ups4 = (fk.LayerUpload * 1)(fk.LayerUpload(0, 1, ctypes.addressof(ok)))
     assert call(ups4, 0) == fk.FUSE_ERR_INVALID_ARG                   # no slot at all
+
+
+def test_key_deviation_argument_errors(fk):
+    # every call below carries one error, found on the host before any launch
+    lib = fk.load()
+    desc = _desc(fk)
+    t = fk.plan_requests([128], [8], 0.3, device=None)
+    t.c.d_req = 16
+    need = fk.workspace_size(desc, t)
+    A = 1 << 20
+
+    def call(H, Wk, Kf, weight, score, ws, nbytes):
+        return lib.fuse_score_key_deviation(ctypes.byref(desc), ctypes.byref(t.c), H, Wk, Kf,
+                                            weight, 0, score, ws, nbytes, None)
+
+    assert call(None, A, A, 1.0, A, A, need) == fk.FUSE_ERR_INVALID_ARG
+    assert call(A, A, A, float("nan"), A, A, need) == fk.FUSE_ERR_INVALID_ARG
+    assert call(A, A, A, float("inf"), A, A, need) == fk.FUSE_ERR_INVALID_ARG
+    assert call(A, A + 2, A, 1.0, A, A, need) == fk.FUSE_ERR_MISALIGNED
+    assert call(A, A, A, 1.0, A, A, need - 1) == fk.FUSE_ERR_WORKSPACE
+    # the fresh keys of every packed row need workspace
+    t2 = fk.plan_requests([256], [8], 0.3, device=None)
+    assert fk.workspace_size(desc, t2) > need
