@@ -529,6 +529,48 @@ def native_run(args, ws, rank, local):
         for b in bufs:
             fk.check_errors(b.ws)
 
+    # the key deviation over layers (KVBoost Alg. 2 step 2 as printed), one
+    # layer's term per call, timed like the scorer after everything above;
+    # a failure here is reported in the line instead of ending the run
+    key_dev = None
+    if args.key_deviation_calls > 0:
+        try:
+            def kdev(b):
+                fk.score_key_deviation(b.desc, b.reqs, b.H, b.Wk, b.Kf, b.score, b.ws)
+            for i in range(3):
+                kdev(sets[i % n_sets])
+            torch.cuda.synchronize()
+            k0 = torch.cuda.Event(enable_timing=True)
+            k1 = torch.cuda.Event(enable_timing=True)
+            k0.record(stream)
+            for i in range(args.key_deviation_calls):
+                kdev(sets[i % n_sets])
+            k1.record(stream)
+            torch.cuda.synchronize()
+            kus = 1e3 * k0.elapsed_time(k1) / args.key_deviation_calls
+            fk.trace_begin(args.key_deviation_calls * 8 + 8)
+            for i in range(args.key_deviation_calls):
+                kdev(sets[i % n_sets])
+            torch.cuda.synchronize()
+            kper = {}
+            for name, kms in fk.trace_end():
+                c, tot = kper.get(name, (0, 0.0))
+                kper[name] = (c + 1, tot + kms)
+            for b in sets:
+                fk.check_errors(b.ws)
+            kk = {}
+            for n_, (c, tot) in kper.items():
+                kk[n_] = {"launches": c, "avg_us": 1e3 * tot / c}
+                avg_s = tot / c / 1e3
+                if n_ in ("key_gemm_tc", "key_gemm_simt"):
+                    kk[n_]["TFLOP/s"] = 2.0 * T * D * Hkv * d / avg_s / 1e12
+                if n_ == "key_cosine":
+                    kk[n_]["GB/s"] = 2.0 * N * Hkv * d * 2 / avg_s / 1e9
+            key_dev = {"us_per_call": kus, "calls": args.key_deviation_calls, "kernels": kk,
+                       "work": "fresh keys 2*T*D*Hkv*d flop; cosines read 2*N*Hkv*d bf16"}
+        except Exception as ex:                      # reported, not fatal
+            key_dev = {"error": f"{type(ex).__name__}: {ex}"}
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_oracle_run(cfg, 1, 0, budget_s=args.cpu_budget)
@@ -548,6 +590,8 @@ def native_run(args, ws, rank, local):
     }
     if scorer is not None:
         out["attention_mass_scorer"] = scorer
+    if key_dev is not None:
+        out["key_deviation"] = key_dev
     if rank == 0:
         print(json.dumps(out), flush=True)
     if ws > 1:
@@ -583,6 +627,7 @@ def main():
     ap.add_argument("--e2e-copy-streams", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--scorer-calls", type=int, default=50)
+    ap.add_argument("--key-deviation-calls", type=int, default=50)
     ap.add_argument("--cpu-budget", type=float, default=30.0)
     ap.add_argument("--ref-budget", type=float, default=150.0)
     args = ap.parse_args()
