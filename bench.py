@@ -571,6 +571,76 @@ def native_run(args, ws, rank, local):
         except Exception as ex:                      # reported, not fatal
             key_dev = {"error": f"{type(ex).__name__}: {ex}"}
 
+    # layer-wise loading overlapped with fusion (QCFuse Figure 9; PCR
+    # layer-wise overlapping): the input sets as the layers of a stack scored
+    # at layer 0.  Timed three ways -- the resident stack, the uploads of every
+    # layer's chunk caches from pinned host memory alone, and the streamed
+    # stack through two staging slots -- after everything above (the slots
+    # are the first two sets' cache storage, overwritten here).
+    streamed = None
+    if args.streamed_layers > 1 and n_sets >= 2:
+        try:
+            import types
+            nl = min(args.streamed_layers, n_sets)
+            lay = sets[:nl]
+            names = [k for k in lay[0].storage if k in ("K", "V")]
+            host = []
+            for b in lay:
+                hb = {}
+                for k in names:
+                    h = torch.empty(b.storage[k].shape, dtype=b.storage[k].dtype, pin_memory=True)
+                    h.copy_(b.storage[k])
+                    hb[k] = h
+                host.append(hb)
+            up_bytes = sum(h.numel() * h.element_size() for hb in host for h in hb.values())
+            b0 = lay[0]
+            cstream = torch.cuda.Stream()
+
+            def timed(fn):
+                a0 = torch.cuda.Event(enable_timing=True)
+                a1 = torch.cuda.Event(enable_timing=True)
+                a0.record(stream)
+                cstream.wait_event(a0)
+                fn()
+                stream.wait_stream(cstream)
+                a1.record(stream)
+                torch.cuda.synchronize()
+                return a0.elapsed_time(a1)
+
+            def resident():
+                fk.stack_step(b0.desc, b0.reqs, lay, 0, b0.idx, b0.score, b0.ws)
+
+            slots = lay[:2]
+
+            def uploads_only():
+                with torch.cuda.stream(cstream):
+                    for l in range(nl):
+                        for k in names:
+                            slots[l % 2].storage[k].copy_(host[l][k], non_blocking=True)
+
+            layers = [types.SimpleNamespace(chunks=slots[l % 2].chunks, H=b.H, Wq=b.Wq, Wk=b.Wk,
+                                            Wv=b.Wv, Kf=b.Kf, Vf=b.Vf, O=b.O)
+                      for l, b in enumerate(lay)]
+            ups = [(l % 2, [(slots[l % 2].storage[k], host[l][k]) for k in names])
+                   for l in range(nl)]
+
+            def streamed_stack():
+                fk.stack_step_streamed(b0.desc, b0.reqs, layers, 0, ups, 2, b0.idx, b0.score,
+                                       b0.ws, cstream)
+
+            res = {}
+            for name_, fn in (("resident_ms", resident), ("uploads_ms", uploads_only),
+                              ("streamed_ms", streamed_stack)):
+                timed(fn)
+                res[name_] = statistics.median(timed(fn) for _ in range(args.streamed_reps))
+            fk.check_errors(b0.ws)
+            hidden = res["resident_ms"] + res["uploads_ms"] - res["streamed_ms"]
+            streamed = dict(res, layers=nl, slots=2, upload_bytes=int(up_bytes),
+                            upload_GBps=up_bytes / (res["uploads_ms"] / 1e3) / 1e9,
+                            hidden_fraction=hidden / min(res["resident_ms"], res["uploads_ms"]))
+        except Exception as ex:                      # reported, not fatal
+            streamed = {"error": f"{type(ex).__name__}: {ex}"}
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_oracle_run(cfg, 1, 0, budget_s=args.cpu_budget)
@@ -592,6 +662,8 @@ def native_run(args, ws, rank, local):
         out["attention_mass_scorer"] = scorer
     if key_dev is not None:
         out["key_deviation"] = key_dev
+    if streamed is not None:
+        out["streamed_stack"] = streamed
     if rank == 0:
         print(json.dumps(out), flush=True)
     if ws > 1:
@@ -628,6 +700,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--scorer-calls", type=int, default=50)
     ap.add_argument("--key-deviation-calls", type=int, default=50)
+    ap.add_argument("--streamed-layers", type=int, default=4)
+    ap.add_argument("--streamed-reps", type=int, default=5)
     ap.add_argument("--cpu-budget", type=float, default=30.0)
     ap.add_argument("--ref-budget", type=float, default=150.0)
     args = ap.parse_args()
