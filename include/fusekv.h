@@ -21,9 +21,11 @@
  * Pointers.  Every tensor pointer is a device pointer aligned to 16 bytes,
  *   unless the field says "host".
  * Errors.  Argument errors are detected on the host and returned before any
- *   launch.  Launch failures return FUSE_ERR_CUDA.  Errors that only the GPU
- *   can see (an out-of-range block id or selected index, an unsorted index
- *   list, a wait that timed out) are recorded in the workspace's error word
+ *   launch; every call that takes a request table rejects one of more
+ *   than 65535 requests with FUSE_ERR_UNSUPPORTED.  Launch failures return
+ *   FUSE_ERR_CUDA.  Errors that only the GPU can see (an out-of-range block
+ *   id or selected index, an unsorted index list, a wait that timed out)
+ *   are recorded in the workspace's error word
  *   and reported by fuse_check_errors().  Nothing aborts or exits.
  * Layouts (row-major, innermost last).
  *   H        [T_total, hidden]            current hidden states; request r owns
@@ -230,8 +232,7 @@ fuse_status_t fuse_score_deviation(const fuse_layer_desc_t* desc, const fuse_req
  * The fresh keys are materialised in desc->dtype (a bf16 layer rounds them
  * to bf16); cosines and sums are fp32, heads summed in order, no atomics.
  * Kf and H are only read.  Needs the workspace of fuse_workspace_size.
- * FUSE_ERR_INVALID_ARG for a weight that is not finite;
- * FUSE_ERR_UNSUPPORTED for more than 65535 requests. */
+ * FUSE_ERR_INVALID_ARG for a weight that is not finite. */
 fuse_status_t fuse_score_key_deviation(const fuse_layer_desc_t* desc, const fuse_requests_t* reqs,
                                        const void* H, const void* Wk, const void* Kf, float weight,
                                        int32_t accumulate, float* score, void* ws,
@@ -251,8 +252,7 @@ fuse_status_t fuse_score_key_deviation(const fuse_layer_desc_t* desc, const fuse
  * (call once per critical layer for Eq. 20's sum).  Kf and H are only read.
  * Query states are materialised in desc->dtype (bf16 layers round q to
  * bf16); logits, weights and sums are fp32.  Deterministic: no
- * floating-point atomics.  Needs the workspace of fuse_workspace_size.
- * FUSE_ERR_UNSUPPORTED for more than 65535 requests. */
+ * floating-point atomics.  Needs the workspace of fuse_workspace_size. */
 fuse_status_t fuse_score_attention_mass(const fuse_layer_desc_t* desc, const fuse_requests_t* reqs,
                                         const void* H, const void* Wq, const void* Kf,
                                         int32_t accumulate, float* score, void* ws,

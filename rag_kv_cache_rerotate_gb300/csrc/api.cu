@@ -47,6 +47,7 @@ cudaError_t launch_attention_tc(const fuse_layer_desc_t& d, const fuse_requests_
 namespace {
 
 constexpr int kMaxPosition = 1 << 24;   // positions stay exact in fp32
+constexpr int kMaxRequests = 65535;      // launch grids give each request one y index
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -96,6 +97,7 @@ struct ReqInfo {
 
 fuse_status_t check_reqs(const fuse_requests_t* r, ReqInfo* info, bool need_device = true) {
   if (!r || r->n_req < 0) return FUSE_ERR_INVALID_ARG;
+  if (r->n_req > kMaxRequests) return FUSE_ERR_UNSUPPORTED;   // one grid row per request
   std::memset(info, 0, sizeof(*info));
   info->n_req = r->n_req;
   if (r->n_req == 0) return FUSE_OK;
@@ -626,7 +628,7 @@ fuse_status_t fuse_score_attention_mass(const fuse_layer_desc_t* desc, const fus
   ReqInfo info;
   st = check_reqs(reqs, &info);
   if (st != FUSE_OK) return st;
-  if (info.n_req > 65535 || info.n_qrows > INT32_MAX) return FUSE_ERR_UNSUPPORTED;
+  if (info.n_qrows > INT32_MAX) return FUSE_ERR_UNSUPPORTED;
   if (info.tot.n_ctx > 0 && (!H || !Wq || !Kf || !score)) return FUSE_ERR_INVALID_ARG;
   if (!aligned16(H) || !aligned16(Wq) || !aligned16(Kf) || !aligned16(score))
     return FUSE_ERR_MISALIGNED;
@@ -644,7 +646,6 @@ fuse_status_t fuse_score_key_deviation(const fuse_layer_desc_t* desc, const fuse
   ReqInfo info;
   st = check_reqs(reqs, &info);
   if (st != FUSE_OK) return st;
-  if (info.n_req > 65535) return FUSE_ERR_UNSUPPORTED;
   if (!std::isfinite(weight)) return FUSE_ERR_INVALID_ARG;
   if (info.tot.n_ctx > 0 && (!H || !Wk || !Kf || !score)) return FUSE_ERR_INVALID_ARG;
   if (!aligned16(H) || !aligned16(Wk) || !aligned16(Kf) || !aligned16(score))

@@ -105,6 +105,7 @@ fuse_status_t static_counts(const fuse_requests_t& reqs, const fuse_chunks_t& ch
                             int n, std::vector<int32_t>& k) {
   if (kind != FUSE_SEL_CHUNK_HEAD && kind != FUSE_SEL_SEAM_TAIL) return FUSE_ERR_INVALID_ARG;
   if (n < 0 || reqs.n_req < 0 || chunks.n_chunks < 0) return FUSE_ERR_INVALID_ARG;
+  if (reqs.n_req > 65535) return FUSE_ERR_UNSUPPORTED;
   if ((reqs.n_req > 0 && !reqs.h_req) || (chunks.n_chunks > 0 && !chunks.h_chunks))
     return FUSE_ERR_INVALID_ARG;
   const fuse_chunk_t* ch = chunks.h_chunks;

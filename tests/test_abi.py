@@ -266,3 +266,12 @@ def test_key_deviation_argument_errors(fk):
     # the fresh keys of every packed row need workspace
     t2 = fk.plan_requests([256], [8], 0.3, device=None)
     assert fk.workspace_size(desc, t2) > need
+
+
+def test_more_than_65535_requests_are_unsupported(fk):
+    ok = fk.plan_requests([1] * 65535, [0] * 65535, 0.5, device=None)
+    assert fk.workspace_size(_desc(fk), ok) > 0
+    big = fk.plan_requests([1] * 65536, [0] * 65536, 0.5, device=None)
+    with pytest.raises(fk.FuseError) as e:
+        fk.workspace_size(_desc(fk), big)
+    assert e.value.status == fk.FUSE_ERR_UNSUPPORTED
