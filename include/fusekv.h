@@ -346,10 +346,14 @@ typedef struct {
  * share only the selection, so every output equals fuse_stack_step's on the
  * uploaded data.  Layer l's copies start after every earlier layer that
  * used the same slot has finished on stream; layer l's kernels start after
- * its copies.  With n_slots >= 2 one layer's upload overlaps the previous
- * layer's kernels.  The schedule is the one fuse_stack_pipeline_plan
- * returns.  The call creates and destroys its own CUDA events (2 * n_slots,
- * n_slots <= 64); everything else is as for fuse_stack_step.  copy_stream
+ * its copies.  Every copy also follows all work enqueued on stream before
+ * the call (an earlier call's kernels may still read the slots), and the
+ * call's last kernel on stream follows every copy, so back-to-back calls on
+ * one stream need no ordering by the caller.  With n_slots >= 2 one layer's
+ * upload overlaps the previous layer's kernels.  The schedule is the one
+ * fuse_stack_pipeline_plan returns.  The call creates and destroys its own
+ * CUDA events (2 * n_slots + 1, n_slots <= 64); everything else is as for
+ * fuse_stack_step.  copy_stream
  * and stream must differ for any overlap (the same stream runs everything
  * in order).  Argument errors are returned before any copy or launch. */
 fuse_status_t fuse_stack_step_streamed(const fuse_layer_desc_t* desc, const fuse_requests_t* reqs,

@@ -799,11 +799,16 @@ fuse_status_t fuse_stack_step_streamed(const fuse_layer_desc_t* desc, const fuse
 
   cudaStream_t s = (cudaStream_t)stream, cs = (cudaStream_t)copy_stream;
   std::vector<cudaEvent_t> ready(n_slots, nullptr), freed(n_slots, nullptr);
-  cudaError_t e = cudaSuccess;
+  cudaEvent_t entry = nullptr;
+  cudaError_t e = cudaEventCreateWithFlags(&entry, cudaEventDisableTiming);
   for (int i = 0; i < n_slots && e == cudaSuccess; ++i) {
     e = cudaEventCreateWithFlags(&ready[i], cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&freed[i], cudaEventDisableTiming);
   }
+  // every upload follows the work enqueued on `stream` before this call: a
+  // slot's buffers may still be read by an earlier call's kernels
+  if (e == cudaSuccess) e = cudaEventRecord(entry, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, entry, 0);
   st = cuda_status(e);
   for (size_t i = 0; i < plan.size() && st == FUSE_OK; ++i) {
     const fuse_pipeline_op_t& o = plan[i];
@@ -844,6 +849,7 @@ fuse_status_t fuse_stack_step_streamed(const fuse_layer_desc_t* desc, const fuse
   }
   // destroying an event with work still pending is allowed: it is released
   // once that work completes
+  if (entry) cudaEventDestroy(entry);
   for (int i = 0; i < n_slots; ++i) {
     if (ready[i]) cudaEventDestroy(ready[i]);
     if (freed[i]) cudaEventDestroy(freed[i]);

@@ -293,7 +293,7 @@ cudaError_t launch_topk(const fuse_requests_t& reqs, int max_ctx, const float* s
 namespace fusekv {
 namespace {
 
-constexpr int kNoallocHeaderWords = 64;          // word 0: device error code (cleared per call)
+constexpr int kNoallocHeaderWords = 64;          // word 0: device error code (written, never read)
 constexpr int kNoallocMaxDevices = 64;
 
 static __device__ __align__(256) uint32_t g_topk_scratch[kNoallocHeaderWords + FUSE_TOPK_NOALLOC_MAX_KEYS];
@@ -326,6 +326,7 @@ extern "C" fuse_status_t fuse_select_topk_noalloc(const fuse_requests_t* reqs, c
                                                   int32_t* idx, fuse_stream_t stream) {
   using namespace fusekv;
   if (!reqs || reqs->n_req < 0) return FUSE_ERR_INVALID_ARG;
+  if (reqs->n_req > 65535) return FUSE_ERR_UNSUPPORTED;   // the request-table limit of every call
   if (reqs->n_req == 0) return FUSE_OK;
   if (!reqs->h_req || !reqs->d_req) return FUSE_ERR_INVALID_ARG;
   int64_t n_ctx = 0, n_sel = 0;
@@ -346,12 +347,18 @@ extern "C" fuse_status_t fuse_select_topk_noalloc(const fuse_requests_t* reqs, c
     return FUSE_ERR_MISALIGNED;
   uint32_t* scratch = nullptr;
   if (noalloc_scratch(&scratch) != cudaSuccess) return FUSE_ERR_CUDA;
-  cudaStream_t s = (cudaStream_t)stream;
-  // the error word must start at zero for the kernel's first-error report
-  if (cudaMemsetAsync(scratch, 0, sizeof(uint32_t) * 2, s) != cudaSuccess) return FUSE_ERR_CUDA;
-  topk_kernel<<<reqs->n_req, kTopkThreads, 0, s>>>(reqs->d_req, score, idx,
-                                                   scratch + kNoallocHeaderWords, scratch,
-                                                   /*keys_in_smem=*/0);
+  // The kernel records a NaN score in the scratch's error word, which nothing
+  // reads (this variant does not report NaN), so the word is never cleared.
+  // cudaLaunchKernelEx returns this launch's own error, not one left pending
+  // by earlier work.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(reqs->n_req);
+  cfg.blockDim = dim3(kTopkThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = (cudaStream_t)stream;
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, topk_kernel, reqs->d_req, score, idx, scratch + kNoallocHeaderWords,
+                         scratch, /*keys_in_smem=*/0, (const float*)nullptr, 0, 0, (float*)nullptr);
   (void)max_ctx;
-  return cudaGetLastError() == cudaSuccess ? FUSE_OK : FUSE_ERR_CUDA;
+  return e == cudaSuccess ? FUSE_OK : FUSE_ERR_CUDA;
 }

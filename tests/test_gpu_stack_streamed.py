@@ -79,10 +79,10 @@ def test_streamed_stack_equals_the_resident_stack(n_slots):
             h.copy_(t)
             pinned[name] = h
         host.append(pinned)
+    torch.cuda.synchronize()             # the pinned copies above are host work
     for b in slots:                      # nothing of the slots' own data may survive
         for t in b.storage.values():
-            t.zero_()
-    torch.cuda.synchronize()             # the uploads do not wait for the compute stream
+            t.zero_()                    # on the compute stream: the uploads follow it
     layers = [_Layer(own[l], slots[slot_of[l]]) for l in range(cfg.n_layers)]
     uploads = [(slot_of[l], [(slots[slot_of[l]].storage[name], host[l][name])
                              for name in host[l]]) for l in range(cfg.n_layers)]
@@ -99,3 +99,49 @@ def test_streamed_stack_equals_the_resident_stack(n_slots):
         assert torch.equal(own[l].Kf, ref[l].Kf), l
         assert torch.equal(own[l].Vf, ref[l].Vf), l
         assert torch.equal(own[l].O, ref[l].O), l
+
+
+def test_streamed_stack_back_to_back_calls():
+    # Two calls in a row on one stream, sharing two staging slots, with no
+    # ordering added by the caller: the second call uploads other layers'
+    # caches into the slots the first call's last layers still read.  The
+    # first call's outputs must still equal the resident stack's.
+    cfg, cases = _cases()
+    ref = _reference()
+    n_slots = 2
+    first = [buffers(c) for c in cases]
+    second = [buffers(c) for c in cases]
+    slots = first[:n_slots]
+    order = [cfg.score_layer] + [l for l in range(cfg.n_layers) if l != cfg.score_layer]
+    slot_of = {l: i % n_slots for i, l in enumerate(order)}
+    host = []
+    for b in first:
+        pinned = {}
+        for name, t in b.storage.items():
+            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            h.copy_(t)
+            pinned[name] = h
+        host.append(pinned)
+    torch.cuda.synchronize()
+    L = cfg.n_layers
+
+    def run(outs, src_of):
+        layers = [_Layer(outs[l], slots[slot_of[l]]) for l in range(L)]
+        uploads = [(slot_of[l], [(slots[slot_of[l]].storage[name], host[src_of(l)][name])
+                                 for name in host[l]]) for l in range(L)]
+        s = outs[cfg.score_layer]
+        fk.stack_step_streamed(s.desc, s.reqs, layers, cfg.score_layer, uploads, n_slots, s.idx,
+                               s.score, s.ws, torch.cuda.Stream())
+
+    run(first, lambda l: l)                  # the layers' own caches
+    run(second, lambda l: (l + 1) % L)       # another layer's caches, at once
+    fk.check_errors(first[cfg.score_layer].ws)
+    fk.check_errors(second[cfg.score_layer].ws)
+    torch.cuda.synchronize()
+    r = ref[cfg.score_layer]
+    assert torch.equal(first[cfg.score_layer].idx, r.idx)
+    assert torch.equal(first[cfg.score_layer].score, r.score)
+    for l in range(L):
+        assert torch.equal(first[l].Kf, ref[l].Kf), l
+        assert torch.equal(first[l].Vf, ref[l].Vf), l
+        assert torch.equal(first[l].O, ref[l].O), l

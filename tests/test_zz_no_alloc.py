@@ -2,7 +2,8 @@
 device memory (all HBM already handed to a KV-cache pool, or running where
 the allocator must not be touched).  Its key scratch is a fixed array inside
 the library; this test checks, through the C ABI, that two calls in a row
-select exactly what fuse_select_topk (with a caller workspace) selects.
+select exactly what fuse_select_topk (with a caller workspace) selects, and
+what the oracle's top-k selects from the same scores.
 
 Kept in a file of its own that pytest collects last; it passes alone in a
 fresh process and after the other tests."""
@@ -13,6 +14,7 @@ import numpy as np
 import pytest
 import torch
 
+from oracle import fusion as orc
 from rag_kv_cache_rerotate_gb300 import _build
 from rag_kv_cache_rerotate_gb300 import fusekv as fk
 
@@ -56,6 +58,12 @@ def test_noalloc_topk_matches_workspace_topk_twice(lib):
         assert st == fk.FUSE_OK, fk.status_string(st)
         torch.cuda.synchronize()
         assert torch.equal(got, want), f"call {call}"
+        # and each request's selection is the oracle's top-k of its scores
+        got_h, score_h = got.cpu().numpy(), score.cpu().numpy()
+        for i in range(len(sizes)):
+            q = reqs[i]
+            ref = orc.select_topk(score_h[q.score0:q.score0 + q.n_ctx], q.k)
+            assert got_h[q.sel0:q.sel0 + q.k].tolist() == ref.tolist(), (call, i)
 
 
 def test_noalloc_topk_rejects_oversize(lib):
