@@ -397,6 +397,22 @@ fuse_status_t fuse_pic_precompute(const fuse_layer_desc_t* desc, const fuse_chun
                                   const void* H_clean, const void* Wk, const void* Wv,
                                   void* ws, size_t ws_bytes, fuse_stream_t stream);
 
+/* KIVI asymmetric quantisation of chunk caches ([KVBoost] section 4.5,
+ * Eq. 7, b = 8 for FUSE_U8_ASYM, b = 4 for FUSE_U4_ASYM), the inverse of the
+ * stitch's dequantisation; it prepares int8 / int4 inputs (it is not part of
+ * a layer-step).  src: CONTIGUOUS caches in desc->dtype; dst: CONTIGUOUS
+ * with the same n_chunks and lengths, kv_storage FUSE_U8_ASYM or
+ * FUSE_U4_ASYM, its k, v, k_scale, k_zero, v_scale, v_zero are outputs
+ * (layouts as in fuse_chunk_t).  With L = 2^b - 1, a group with minimum mn
+ * and maximum mx is stored as q = rint((x - mn) / (mx - mn) * L) (round half
+ * to even, in fp64), scale = fp16((mx - mn) / L), zero = fp16(mn); a constant
+ * group gets q = 0 and scale 0.  Key groups: (chunk, head, channel) over the
+ * chunk's tokens; value groups: (token, head) over d.  Argument errors
+ * (mismatched tables, other layouts or storage) are returned before any
+ * launch. */
+fuse_status_t fuse_kivi_quantize(const fuse_layer_desc_t* desc, const fuse_chunks_t* src,
+                                 const fuse_chunks_t* dst, fuse_stream_t stream);
+
 /* Synchronise the stream, read the workspace's error word, clear it, and
  * return it (FUSE_OK if no device-side error was recorded).  If detail is
  * not NULL it receives a code locating the failed check. */

@@ -393,7 +393,6 @@ def recompute_selected(H: np.ndarray, Wq, Wk, Wv, idx: np.ndarray, n_ctx: int,
     """
     T = H.shape[0]
     d = head_dim
-    g = n_q_heads // n_kv_heads
     S = selected_rows(idx, n_ctx, T)
     q, k, v = project_rows(np.asarray(H, F64)[S], Wq, Wk, Wv, S,
                            n_q_heads, n_kv_heads, d, base)
@@ -403,9 +402,26 @@ def recompute_selected(H: np.ndarray, Wq, Wk, Wv, idx: np.ndarray, n_ctx: int,
     Vf = np.array(V_fused, dtype=F64, copy=True)
     Kf[S] = k
     Vf[S] = v
-    Kt = np.ascontiguousarray(Kf.transpose(1, 0, 2))     # [Hkv, T, d]
-    Vt = np.ascontiguousarray(Vf.transpose(1, 0, 2))
     rows = np.arange(S.shape[0]) if out_rows is None else np.asarray(out_rows)
+    O = causal_attention(q, Kf, Vf, S, rows, n_q_heads, n_kv_heads, d)
+    return Kf, Vf, O, S
+
+
+def causal_attention(q: np.ndarray, K_fused: np.ndarray, V_fused: np.ndarray, S: np.ndarray,
+                     rows: np.ndarray, n_q_heads: int, n_kv_heads: int, head_dim: int):
+    """Causal GQA attention rows over a fused cache (KVBoost Eq. 2).
+
+    For each ``r`` in ``rows`` (indices into S), the row at position
+    ``p = S[r]`` with query ``q[r]`` (``[Hq, d]``) attends over ``j <= p`` of
+    ``K_fused``/``V_fused`` (``[T, Hkv, d]``) with scale ``1/sqrt(d)``; query
+    head h reads KV head ``h // (Hq/Hkv)``; two-pass softmax with the maximum
+    subtracted.  Returns ``O [len(rows), Hq, d]``.
+    """
+    d = head_dim
+    g = n_q_heads // n_kv_heads
+    Kt = np.ascontiguousarray(np.asarray(K_fused, F64).transpose(1, 0, 2))     # [Hkv, T, d]
+    Vt = np.ascontiguousarray(np.asarray(V_fused, F64).transpose(1, 0, 2))
+    rows = np.asarray(rows)
     O = np.zeros((rows.shape[0], n_q_heads, d), dtype=F64)
     scale = 1.0 / math.sqrt(d)
     for o, r in enumerate(rows):
@@ -416,7 +432,7 @@ def recompute_selected(H: np.ndarray, Wq, Wk, Wv, idx: np.ndarray, n_ctx: int,
         w = np.exp(logits - m)
         w /= w.sum(axis=-1, keepdims=True)
         O[o] = np.matmul(w, Vt[:, :p + 1, :]).reshape(n_q_heads, d)
-    return Kf, Vf, O, S
+    return O
 
 
 def layer_step(H: np.ndarray, Wq, Wk, Wv, K_chunks, V_chunks, ratio: float,

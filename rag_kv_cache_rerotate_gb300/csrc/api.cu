@@ -881,6 +881,30 @@ fuse_status_t fuse_pic_precompute(const fuse_layer_desc_t* desc, const fuse_chun
   }));
 }
 
+fuse_status_t fuse_kivi_quantize(const fuse_layer_desc_t* desc, const fuse_chunks_t* src,
+                                 const fuse_chunks_t* dst, fuse_stream_t stream) {
+  fuse_status_t st = check_desc(desc);
+  if (st != FUSE_OK) return st;
+  if (!src || !dst) return FUSE_ERR_INVALID_ARG;
+  if (src->kv_layout != FUSE_KV_CONTIGUOUS || dst->kv_layout != FUSE_KV_CONTIGUOUS ||
+      src->kv_storage != desc->dtype ||
+      (dst->kv_storage != FUSE_U8_ASYM && dst->kv_storage != FUSE_U4_ASYM))
+    return FUSE_ERR_UNSUPPORTED;
+  if (src->n_chunks != dst->n_chunks) return FUSE_ERR_INVALID_ARG;
+  int max_len = 0, max_len_dst = 0;
+  st = check_chunks(*desc, src, INT64_MAX / 2, &max_len);
+  if (st != FUSE_OK) return st;
+  st = check_chunks(*desc, dst, INT64_MAX / 2, &max_len_dst);
+  if (st != FUSE_OK) return st;
+  for (int i = 0; i < src->n_chunks; ++i)
+    if (src->h_chunks[i].len != dst->h_chunks[i].len) return FUSE_ERR_INVALID_ARG;
+  if (src->n_chunks == 0 || max_len == 0) return FUSE_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  return cuda_status(traced("kivi_quantize", s, [&] {
+    return launch_kivi_quantize(*desc, *src, *dst, max_len, s);
+  }));
+}
+
 fuse_status_t fuse_check_errors(void* ws, fuse_stream_t stream, uint32_t* detail) {
   if (!ws) return FUSE_ERR_WORKSPACE;
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return FUSE_ERR_CUDA;

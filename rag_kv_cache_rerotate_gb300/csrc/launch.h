@@ -122,6 +122,11 @@ cudaError_t launch_project_pic(const fuse_layer_desc_t& desc, int n_chunks, int 
                                const RopeFreqs& freqs, const void* H, const void* Wk, const void* Wv,
                                const fuse_chunk_t* d_chunks, uint32_t* err, cudaStream_t s);
 
+// KIVI quantisation of layer-type chunk caches into codes with fp16 scale / zero
+// (input preparation).
+cudaError_t launch_kivi_quantize(const fuse_layer_desc_t& d, const fuse_chunks_t& src,
+                                 const fuse_chunks_t& dst, int max_len, cudaStream_t s);
+
 // Query projection of packed work rows (Q heads only, RoPE at each row's position).
 cudaError_t launch_project_query_simt(const fuse_layer_desc_t& desc, int64_t n_rows,
                                       const WorkRow* rows, const float2* rope, const void* H,

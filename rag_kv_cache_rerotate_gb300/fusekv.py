@@ -126,6 +126,7 @@ _SIGS = {
     "fuse_stack_pipeline_plan": (_c.c_int, [_c.c_int32, _c.c_int32, _P, _c.c_int32, _P,
                                             _c.c_int32, _c.POINTER(_c.c_int32)]),
     "fuse_stack_step": (_c.c_int, [_P, _P, _c.c_int32, _c.c_int32, _P, _P, _P, _P, _c.c_size_t, _P]),
+    "fuse_kivi_quantize": (_c.c_int, [_P, _P, _P, _P]),
     "fuse_check_errors": (_c.c_int, [_P, _P, _c.POINTER(_c.c_uint32)]),
     "fuse_static_select_count": (_c.c_int, [_P, _P, _c.c_int32, _c.c_int32, _P]),
     "fuse_static_select": (_c.c_int, [_P, _P, _c.c_int32, _c.c_int32, _P, _P]),
@@ -408,6 +409,13 @@ def pic_precompute(desc, chunks: ChunkTable, H_clean, Wk, Wv, ws, stream=None):
     _check(load().fuse_pic_precompute(_c.byref(desc), _c.byref(chunks.c), _ptr(H_clean),
                                       _ptr(Wk), _ptr(Wv), _ptr(ws), ws.numel(), _stream(stream)),
            "fuse_pic_precompute")
+
+
+def kivi_quantize(desc, src: ChunkTable, dst: ChunkTable, stream=None):
+    """KIVI codes and fp16 scale / zero of layer-type chunk caches (KVBoost
+    Eq. 7): input preparation for the int8 / int4 storage modes."""
+    _check(load().fuse_kivi_quantize(_c.byref(desc), _c.byref(src.c), _c.byref(dst.c),
+                                     _stream(stream)), "fuse_kivi_quantize")
 
 
 def check_errors(ws, stream=None):

@@ -214,3 +214,47 @@ def gpu_pic_caches(cfg: FusionConfig, layouts, H_clean, Wk, Wv, device="cuda") -
                       Wv.to(device).contiguous(), ws)
     fk.check_errors(ws)
     return ChunkCaches(K, V)
+
+
+def gpu_kivi_caches(cfg: FusionConfig, layouts, caches: ChunkCaches, device="cuda") -> ChunkCaches:
+    """KIVI codes of layer-type chunk caches (``fuse_kivi_quantize``), in the
+    storage ``cfg.kv_storage`` ("u8" or "u4"), laid out as ``ChunkCaches``
+    expects: codes ``[sum len, Hkv, d]`` (``d / 2`` bytes for 4 bits), key
+    scale / zero ``[n_chunks, Hkv, d]`` and value scale / zero
+    ``[sum len, Hkv]`` in fp16."""
+    rows = chunk_token_rows(layouts)
+    Hkv, d = cfg.n_kv_heads, cfg.head_dim
+    n_tot = sum(n for (*_, n) in rows)
+    dk = d // 2 if cfg.kv_storage == "u4" else d
+    f16 = torch.float16
+    out = ChunkCaches(torch.empty(n_tot, Hkv, dk, dtype=torch.uint8, device=device),
+                      torch.empty(n_tot, Hkv, dk, dtype=torch.uint8, device=device),
+                      torch.empty(len(rows), Hkv, d, dtype=f16, device=device),
+                      torch.empty(len(rows), Hkv, d, dtype=f16, device=device),
+                      torch.empty(n_tot, Hkv, dtype=f16, device=device),
+                      torch.empty(n_tot, Hkv, dtype=f16, device=device))
+    K, V = caches.K.to(device).contiguous(), caches.V.to(device).contiguous()
+    src_row = K[0].numel() * K.element_size()
+    src, dst = [], []
+    c0 = 0
+    for ci, (_, _, row, pos, n) in enumerate(rows):
+        e = fk.Chunk()
+        e.k = K.data_ptr() + c0 * src_row
+        e.v = V.data_ptr() + c0 * src_row
+        e.dst_row, e.pos, e.len = row, pos, n
+        src.append(e)
+        q = fk.Chunk()
+        q.k = out.K.data_ptr() + c0 * Hkv * dk
+        q.v = out.V.data_ptr() + c0 * Hkv * dk
+        q.k_scale = out.k_scale.data_ptr() + ci * Hkv * d * 2
+        q.k_zero = out.k_zero.data_ptr() + ci * Hkv * d * 2
+        q.v_scale = out.v_scale.data_ptr() + c0 * Hkv * 2
+        q.v_zero = out.v_zero.data_ptr() + c0 * Hkv * 2
+        q.dst_row, q.pos, q.len = row, pos, n
+        dst.append(q)
+        c0 += n
+    t_src = fk.ChunkTable(src, fk.FUSE_KV_CONTIGUOUS, _FUSE[cfg.dtype], keep=[K, V], device=device)
+    t_dst = fk.ChunkTable(dst, fk.FUSE_KV_CONTIGUOUS, _FUSE[cfg.kv_storage], device=device)
+    fk.kivi_quantize(desc_of(cfg), t_src, t_dst)
+    torch.cuda.synchronize()
+    return out
