@@ -24,3 +24,27 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Print how far the bf16 attention rows of each parity test went past
+    the flat 2e-2 tolerance (within their rounding allowances); with
+    FUSEKV_PARITY_LOG set, also write the records there as JSON lines."""
+    try:
+        import rounding
+    except Exception:  # pragma: no cover
+        return
+    if not rounding.RECORDS:
+        return
+    tr = terminalreporter
+    tr.section("bf16 attention rows past the flat tolerance")
+    for r in rounding.RECORDS:
+        tr.write_line(f"{r['test']}: {r['over_flat']}/{r['pairs']} (row, head) pairs over 2e-2 "
+                      f"(max {r['max_err_over_flat']:.3g}x), {r['widened']} widened, "
+                      f"{r['widened_over_2x']} beyond 2x, {r['rows']} rows")
+    path = os.environ.get("FUSEKV_PARITY_LOG")
+    if path:
+        import json
+        with open(path, "w") as f:
+            for r in rounding.RECORDS:
+                f.write(json.dumps(r) + "\n")

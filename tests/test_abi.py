@@ -275,3 +275,43 @@ def test_more_than_65535_requests_are_unsupported(fk):
     with pytest.raises(fk.FuseError) as e:
         fk.workspace_size(_desc(fk), big)
     assert e.value.status == fk.FUSE_ERR_UNSUPPORTED
+
+
+def test_noalloc_topk_request_table_limit(fk):
+    lib = fk.load()
+    fn = lib.fuse_select_topk_noalloc
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p] * 4
+    big = fk.plan_requests([1] * 65536, [0] * 65536, 0.5, device=None)
+    big.c.d_req = 4096                                  # a non-null stand-in, never dereferenced
+    assert fn(ctypes.byref(big.c), 4096, 4096, None) == fk.FUSE_ERR_UNSUPPORTED
+
+
+def test_kivi_quantize_argument_errors(fk):
+    lib = fk.load()
+    desc = fk.layer_desc(256, 4, 2, 64, 1e4, fk.FUSE_BF16)
+
+    def table(storage, lens, scales=True):
+        es = []
+        for n in lens:
+            e = fk.Chunk()
+            e.k, e.v, e.len = 4096, 4096, n
+            if scales:
+                e.k_scale, e.k_zero, e.v_scale, e.v_zero = 4096, 4096, 4096, 4096
+            es.append(e)
+        t = fk.ChunkTable(es, fk.FUSE_KV_CONTIGUOUS, storage, device=None)
+        t.c.d_chunks = 4096
+        return t
+
+    def call(src, dst):
+        return lib.fuse_kivi_quantize(ctypes.byref(desc), ctypes.byref(src.c), ctypes.byref(dst.c),
+                                      None)
+
+    src = table(fk.FUSE_BF16, [8, 3], scales=False)
+    assert call(src, table(fk.FUSE_U8_ASYM, [8, 4])) == fk.FUSE_ERR_INVALID_ARG     # lengths differ
+    assert call(src, table(fk.FUSE_U8_ASYM, [8])) == fk.FUSE_ERR_INVALID_ARG        # chunk counts
+    assert call(src, table(fk.FUSE_U8_ASYM, [8, 3], scales=False)) == fk.FUSE_ERR_INVALID_ARG
+    assert call(src, table(fk.FUSE_BF16, [8, 3])) == fk.FUSE_ERR_UNSUPPORTED        # not codes
+    assert call(table(fk.FUSE_F32, [8, 3]), table(fk.FUSE_U4_ASYM, [8, 3])) == fk.FUSE_ERR_UNSUPPORTED
+    empty = table(fk.FUSE_BF16, [0, 0], scales=False)
+    assert call(empty, table(fk.FUSE_U8_ASYM, [0, 0])) == fk.FUSE_OK                # nothing to do

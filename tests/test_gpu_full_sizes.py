@@ -1,15 +1,20 @@
 """GPU parity at the workloads' full sizes, in the launch configuration the
 benchmark uses (one call per layer-step / stack), on outputs the oracle can
-compute one by one: every score, the whole selection, stitched rows and
-attention rows sampled per request.
+compute one by one: every score, the whole selection, every refreshed K/V
+row, stitched rows, and attention rows (all of them for four requests of the
+paged batch, a sample elsewhere).
 
 * llama3_8b_paged_batch16: 16 requests, paged pool, end to end.
-* llama3_70b_int8_long: 33 024 tokens, int8 caches; checked step by step
-  (its LogNormal(-3, 2) perturbations make end-to-end rows ill-conditioned
-  in bf16; see test_gpu_parity.py).
+* llama3_70b_int8_long: 33 024 tokens, int8 caches, end to end through
+  fuse_layer_step on the cache the GPU stitched (dequantised and rotated).
 * qwen3_8b_stack36: 36 layers scored at layer 2; three distinct draw sets
   cycled over the layers (each layer has its own buffers), layers 0, 2 and
   35 checked.
+
+Attention rows of these bf16 layers are compared within the rounding
+allowance of tests/rounding.py (the stated 2e-2 plus what equally correct
+bf16 roundings of q, k, v and of the stitched entries can move a row), with
+its 2 % guard.
 """
 
 import numpy as np
@@ -39,23 +44,28 @@ def _sample(n, m):
     return np.unique(np.linspace(0, n - 1, min(n, m)).astype(int))
 
 
-def _check_request_rows(cfg, H, Wq, Wk, Wv, idx, n, T, Ks, Vs, Kf, Vf, O, out0, n_rows=8):
-    """Recompute of one request against the oracle on its stitched cache."""
+def _check_request_rows(label, cfg, H, Wq, Wk, Wv, idx, n, T, Ks, Vs, Kf, Vf, O, out0, stitched,
+                        n_rows=8):
+    """Recompute of one request against the oracle on its stitched cache:
+    every refreshed K/V row, every reused stitched row, and `n_rows` attention
+    rows (None: all) plus the last."""
     Kf0 = np.zeros((T, cfg.n_kv_heads, cfg.head_dim))
     Vf0 = np.zeros_like(Kf0)
     Kf0[:n], Vf0[:n] = Ks, Vs
     S = orc.selected_rows(idx, n, T)
-    rows = _sample(len(S), n_rows)
+    rows = np.arange(len(S)) if n_rows is None else _sample(len(S), n_rows)
     rows = np.unique(np.concatenate([rows, [len(S) - 1]]))
     Ko, Vo, Oo, _ = orc.recompute_selected(H, Wq, Wk, Wv, idx, n, Kf0, Vf0, cfg.n_q_heads,
                                            cfg.n_kv_heads, cfg.head_dim, cfg.rope_base,
                                            out_rows=rows, store=STORE)
     assert max_rel(Kf[S], Ko[S]) <= 2e-2
     assert max_rel(Vf[S], Vo[S]) <= 2e-2
-    allow, base, _ = rounding.allowance(H, Wq, Wk, Wv, S, Ko, Vo, Oo, rows, cfg.n_q_heads,
-                                        cfg.n_kv_heads, cfg.head_dim, cfg.rope_base, 2e-2)
-    err = np.max(np.abs(O[out0 + rows] - Oo), axis=-1)
-    assert np.all(err <= allow), float(np.max(err / allow))
+    keep = np.setdiff1d(np.arange(n), S)
+    assert max_row_rel(Kf[keep], Ko[keep]) <= 2.0 ** -7
+    assert max_row_rel(Vf[keep], Vo[keep]) <= 2.0 ** -7
+    rounding.check_rows(label, O[out0 + rows], H, Wq, Wk, Wv, S, Ko, Vo, Oo, rows,
+                        cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.rope_base, 2e-2,
+                        stitched=stitched)
 
 
 def test_paged_batch16_full_size_end_to_end():
@@ -81,44 +91,47 @@ def test_paged_batch16_full_size_end_to_end():
         assert orc.select_topk(s_gpu, q.k).tolist() == idx.tolist()
         rest = np.setdiff1d(np.arange(n), idx)
         assert s_orc[idx].min() >= s_orc[rest].max() - 2e-3
-        keep = _sample(len(rest), 64)
-        assert max_row_rel(Kf[row0 + rest[keep]], Ks[rest[keep]]) <= 2.0 ** -7
-        assert np.array_equal(Vf[row0 + rest[keep]], Vs[rest[keep]])
-        _check_request_rows(cfg, H[row0:row0 + T], Wq, Wk, Wv, idx, n, T, Ks, Vs,
-                            Kf[row0:row0 + T], Vf[row0:row0 + T], O, q.out0, n_rows=6)
+        assert np.array_equal(Vf[row0 + rest], Vs[rest])
+        st = rounding.stitched_bounds([case.K_cached[i] for i in cis],
+                                      [case.V_cached[i] for i in cis], cfg.rope_base, False)
+        # every attention row of the first four requests, a sample of the rest
+        _check_request_rows(f"paged_batch16[req {r}]", cfg, H[row0:row0 + T], Wq, Wk, Wv, idx, n,
+                            T, Ks, Vs, Kf[row0:row0 + T], Vf[row0:row0 + T], O, q.out0, st,
+                            n_rows=None if r < 4 else 6)
 
 
-def test_int8_long_context_full_size_step_by_step():
+def test_int8_long_context_full_size_end_to_end():
+    # the whole layer-step through fuse_layer_step, on the cache the GPU
+    # stitched from the int8 codes (dequantise + re-rotate, KVBoost Eq. 7,
+    # QCFuse Eq. 4), compared with the oracle step by step
     cfg = C["llama3_70b_int8_long"]
     case = make_case(cfg)
     b = buffers(case)
     q = b.reqs[0]
     n, T = q.n_ctx, q.n_ctx + q.n_query
-    assert (n, T) == (32768, 33024)
-    # stitch (int8 dequantise + re-rotate at offsets up to 31 744)
-    fk.stitch_rerotate(b.desc, b.chunks, b.Kf, b.Vf, b.ws)
-    fk.check_errors(b.ws)
-    Kr, Vr = orc.stitch_rerotate(case.K_cached, case.V_cached, cfg.rope_base)
-    rows = _sample(n, 512)
-    assert max_row_rel(f64(b.Kf[rows]), Kr[rows]) <= stitch_tol(cfg)
-    assert max_row_rel(f64(b.Vf[rows]), Vr[rows]) <= stitch_tol(cfg)
-    # deviation scores and selection, on the oracle's stored cache
-    Ks, Vs = orc.stitch_rerotate(case.K_cached, case.V_cached, cfg.rope_base, STORE)
-    b.Kf[:n] = torch.from_numpy(Ks).to(b.Kf.dtype).cuda()
-    b.Vf[:n] = torch.from_numpy(Vs).to(b.Vf.dtype).cuda()
-    fk.score_deviation(b.desc, b.reqs, b.H, b.Wv, b.Vf, b.score, b.ws)
-    fk.select_topk(b.reqs, b.score, b.idx, b.ws)
-    fk.recompute_selected(b.desc, b.reqs, b.H, b.Wq, b.Wk, b.Wv, b.idx, b.Kf, b.Vf, b.O, b.ws)
+    assert (n, T, q.k) == (32768, 33024, 3276)
+    fk.layer_step(b.desc, b.chunks, b.reqs, b.H, b.Wq, b.Wk, b.Wv, True, b.idx, b.Kf, b.Vf, b.O,
+                  b.score, b.ws)
     fk.check_errors(b.ws)
     H, Wq, Wk, Wv = f64(b.H), f64(b.Wq), f64(b.Wk), f64(b.Wv)
-    s_gpu = b.score.cpu().numpy()[:n]
+    Kf, Vf, O = f64(b.Kf), f64(b.Vf), f64(b.O)
+    # the oracle's stitched cache: before and after its bf16 storage rounding
+    Kr, Vr = orc.stitch_rerotate(case.K_cached, case.V_cached, cfg.rope_base)
+    Ks, Vs = STORE(Kr), STORE(Vr)
+    score = b.score.cpu().numpy()[:n]
     s_orc = orc.deviation_scores(H[:n], Wv, Vs, cfg.n_kv_heads, cfg.head_dim)
-    assert np.max(np.abs(s_gpu - s_orc)) <= 1e-3
+    assert np.max(np.abs(score - s_orc)) <= 1e-3
     idx = b.idx.cpu().numpy()[:q.k].astype(np.int64)
-    assert q.k == 3276
-    assert orc.select_topk(s_gpu, q.k).tolist() == idx.tolist()
-    _check_request_rows(cfg, H, Wq, Wk, Wv, idx, n, T, Ks, Vs, f64(b.Kf), f64(b.Vf), f64(b.O),
-                        q.out0, n_rows=12)
+    assert orc.select_topk(score, q.k).tolist() == idx.tolist()
+    rest = np.setdiff1d(np.arange(n), idx)
+    assert s_orc[idx].min() >= s_orc[rest].max() - 2e-3
+    # the stitched rows the recompute left alone, per row, within the fp32
+    # dequantise-and-rotate error before the bf16 rounding
+    assert max_row_rel(Kf[rest], Kr[rest]) <= stitch_tol(cfg)
+    assert max_row_rel(Vf[rest], Vr[rest]) <= stitch_tol(cfg)
+    st = rounding.stitched_bounds(case.K_cached, case.V_cached, cfg.rope_base, True)
+    _check_request_rows("int8_long_end_to_end", cfg, H, Wq, Wk, Wv, idx, n, T, Ks, Vs, Kf, Vf, O,
+                        q.out0, st, n_rows=48)
 
 
 def test_stack36_full_size():
@@ -143,5 +156,7 @@ def test_stack36_full_size():
     for l in (0, cfg.score_layer, cfg.n_layers - 1):
         case, b = sets[l % 3], bufs[l]
         Ks, Vs = orc.stitch_rerotate(case.K_cached, case.V_cached, cfg.rope_base, STORE)
-        _check_request_rows(cfg, f64(b.H), f64(b.Wq), f64(b.Wk), f64(b.Wv), idx, n, T, Ks, Vs,
-                            f64(b.Kf), f64(b.Vf), f64(b.O), q.out0, n_rows=8)
+        st = rounding.stitched_bounds(case.K_cached, case.V_cached, cfg.rope_base, False)
+        _check_request_rows(f"stack36[layer {l}]", cfg, f64(b.H), f64(b.Wq), f64(b.Wk),
+                            f64(b.Wv), idx, n, T, Ks, Vs, f64(b.Kf), f64(b.Vf), f64(b.O), q.out0,
+                            st, n_rows=24)

@@ -70,4 +70,5 @@ def test_recompute_from_static_selection(name, kind):
     fk.recompute_selected(b2.desc, b2.reqs, b2.H, b2.Wq, b2.Wk, b2.Wv, b2.idx, b2.Kf, b2.Vf, b2.O,
                           b2.ws)
     fk.check_errors(b2.ws)
-    parity._recompute_and_compare(case, b2, idx.cpu().numpy())
+    parity._recompute_and_compare(case, b2, idx.cpu().numpy(), f"static_select[{name},{kind}]",
+                                  gpu_stitched=True)
