@@ -316,6 +316,27 @@ fuse_status_t fuse_stack_step(const fuse_layer_desc_t* desc, const fuse_requests
                               int32_t* idx, float* score, void* ws, size_t ws_bytes,
                               fuse_stream_t stream);
 
+/* The same stack as one CUDA graph ([QCFuse] section 3.5: the layers of a
+ * fusion step run back to back; a graph replays their launches without the
+ * host issuing each one).  fuse_stack_graph_create captures fuse_stack_step
+ * with these arguments on `stream` (not the legacy NULL stream, and not a
+ * stream already being captured) and instantiates it; fuse_graph_launch
+ * replays it on any stream, with every pointer, table and size as captured
+ * (the buffers' contents may change between replays; their addresses and
+ * the request and chunk tables may not).  A replay computes what the eager
+ * call computes, bit for bit.  Argument errors of the captured call are
+ * returned by create; no kernel runs during create.  Keep no kernel trace
+ * open while creating.  fuse_graph_destroy releases the graph (host-side
+ * state; call it after the last replay has been enqueued). */
+typedef struct fuse_graph_st* fuse_graph_t;
+fuse_status_t fuse_stack_graph_create(const fuse_layer_desc_t* desc, const fuse_requests_t* reqs,
+                                      int32_t n_layers, int32_t score_layer,
+                                      const fuse_layer_io_t* layers, int32_t* idx, float* score,
+                                      void* ws, size_t ws_bytes, fuse_stream_t stream,
+                                      fuse_graph_t* out);
+fuse_status_t fuse_graph_launch(fuse_graph_t graph, fuse_stream_t stream);
+void fuse_graph_destroy(fuse_graph_t graph);
+
 /* ---------------------------------------------------------------------- */
 /* Layer-wise loading overlapped with the layers' fusion ([QCFuse] Figure 9,
  * pipeline cache fusion: each layer starts from its loaded PIC entries while

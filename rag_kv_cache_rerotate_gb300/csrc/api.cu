@@ -4,6 +4,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <new>
 #include <vector>
 
 #include "common.cuh"
@@ -27,8 +28,17 @@ cudaError_t launch_project_recompute_tc(const fuse_layer_desc_t& desc, int64_t n
                                         void* Kf, void* Vf, void* Hs, uint32_t* err, cudaStream_t s);
 cudaError_t launch_project_query_tc(const fuse_layer_desc_t& d, int64_t n_rows, const float2* rope,
                                     const void* Wq, void* Q, const void* Hs, uint32_t* err,
-                                    cudaStream_t s);
+                                    cudaStream_t s, float* split_ws = nullptr, int max_splits = 1);
 bool tc_attention_supported(const fuse_layer_desc_t& desc);
+// Query-aware attention mass on the tensor cores (csrc/attention_mass_tc.cu).
+bool mass_tc_supported(const fuse_layer_desc_t& d);
+int mass_tc_chunks(const fuse_layer_desc_t& d, const fuse_requests_t& reqs, int max_ctx,
+                   int max_query);
+cudaError_t launch_attention_mass_tc(const fuse_layer_desc_t& d, const fuse_requests_t& reqs,
+                                     int max_ctx, int max_query, int64_t n_qrows, int64_t n_tok,
+                                     const int32_t* qoff, const void* Q, const void* Kf,
+                                     float2* stats, float* part, int n_chunks, float* score,
+                                     int accumulate, uint32_t* err, cudaStream_t s);
 // Key deviation (csrc/key_deviation.cu).
 cudaError_t launch_key_rows(const fuse_requests_t& reqs, int max_tok, const RopeFreqs& freqs,
                             int head_dim, int64_t n_rows, WorkRow* rows, float2* rope,
@@ -198,7 +208,13 @@ WsLayout ws_layout(const fuse_layer_desc_t& d, const ReqInfo& info) {
   L.qoff = take((size_t)n_req * sizeof(int32_t));
   L.krows = take((size_t)t.n_tok * sizeof(WorkRow));
   L.krope = take((size_t)t.n_tok * (d.head_dim / 2) * sizeof(float2));
-  L.kn = take((size_t)t.n_tok * d.n_kv_heads * d.head_dim * es);
+  // the key deviation's fresh keys; the query-aware scorer uses the same
+  // region for its split-K projection partials and, on the tensor-core path,
+  // for its per-(token, KV head, 128-vector tile, half) mass
+  const int g = d.n_q_heads / d.n_kv_heads;
+  const size_t n_vt = ((size_t)info.max_query * g + 127) / 128;
+  L.kn = take(std::max((size_t)t.n_tok * d.n_kv_heads * d.head_dim * es,
+                       (size_t)t.n_ctx * d.n_kv_heads * n_vt * 2 * sizeof(float)));
   L.total = off;
   return L;
 }
@@ -361,19 +377,35 @@ fuse_status_t do_mass(const fuse_layer_desc_t& d, const fuse_requests_t& r, cons
   if (e == cudaSuccess && nq > 0) {
     if (tc)
       e = traced("query_gemm_tc", s, [&] {
-        return launch_project_query_tc(d, nq, rope, Wq, Q, at<void>(ws, L.mhs), err, s);
+        // the split-K partials use the key deviation's fresh-key region
+        const size_t per_split = (size_t)nq * d.n_q_heads * d.head_dim * sizeof(float);
+        const size_t room = L.total - L.kn;
+        const int max_splits = (int)std::min<size_t>(8, room / std::max<size_t>(per_split, 1));
+        return launch_project_query_tc(d, nq, rope, Wq, Q, at<void>(ws, L.mhs), err, s,
+                                       at<float>(ws, L.kn), max_splits);
       });
     else
       e = traced("query_gemm_simt", s, [&] {
         return launch_project_query_simt(d, nq, rows, rope, H, Wq, Q, err, s);
       });
   }
-  if (e == cudaSuccess)
-    e = traced("attention_mass", s, [&] {
-      return launch_attention_mass(d, r, info.tot.max_ctx, nq, rows, qoff, Q, Kf,
-                                   at<float2>(ws, L.mstats), at<float2>(ws, L.mnorm),
-                                   at<float>(ws, L.partial), score, accumulate, s);
-    });
+  if (e == cudaSuccess) {
+    if (mass_tc_supported(d)) {
+      const int n_chunks = mass_tc_chunks(d, r, info.tot.max_ctx, info.max_query);
+      e = traced("attention_mass_tc", s, [&] {
+        return launch_attention_mass_tc(d, r, info.tot.max_ctx, info.max_query, nq,
+                                        info.tot.n_tok, qoff, Q, Kf, at<float2>(ws, L.mstats),
+                                        at<float>(ws, L.kn), n_chunks, score, accumulate, err,
+                                        s);
+      });
+    } else {
+      e = traced("attention_mass", s, [&] {
+        return launch_attention_mass(d, r, info.tot.max_ctx, nq, rows, qoff, Q, Kf,
+                                     at<float2>(ws, L.mstats), at<float2>(ws, L.mnorm),
+                                     at<float>(ws, L.partial), score, accumulate, s);
+      });
+    }
+  }
   return cuda_status(e);
 }
 
@@ -451,10 +483,11 @@ fuse_status_t do_score_select(const fuse_layer_desc_t& d, const fuse_requests_t&
   return do_reduce_topk(d, r, info, score, idx, ws, s);
 }
 
-// Stitch and score/select of one layer.  On the tensor-core path with
-// same-type chunk caches placed in order, the deviation GEMM reads the cached
-// V rows from the chunks themselves and the stitch runs on the SMs the GEMM
-// leaves free (it waits for the GEMM only at its end); otherwise in sequence.
+// Stitch and score/select of one layer.  On the tensor-core path with chunk
+// caches of the layer's type or int8 codes, placed in order, the deviation
+// GEMM reads the cached V rows from the chunks themselves (dequantising int8
+// codes as the stitch does) and the stitch runs beside it (it waits for the
+// GEMM only at its end); otherwise in sequence.
 fuse_status_t do_stitch_score_select(const fuse_layer_desc_t& d, const fuse_chunks_t& c,
                                      int max_len, const fuse_requests_t& r, const ReqInfo& info,
                                      const void* H, const void* Wv, void* Kf, void* Vf,
@@ -751,6 +784,62 @@ fuse_status_t fuse_stack_step(const fuse_layer_desc_t* desc, const fuse_requests
     if (st != FUSE_OK) return st;
   }
   return FUSE_OK;
+}
+
+struct fuse_graph_st {
+  cudaGraph_t graph;
+  cudaGraphExec_t exec;
+};
+
+fuse_status_t fuse_stack_graph_create(const fuse_layer_desc_t* desc, const fuse_requests_t* reqs,
+                                      int32_t n_layers, int32_t score_layer,
+                                      const fuse_layer_io_t* layers, int32_t* idx, float* score,
+                                      void* ws, size_t ws_bytes, fuse_stream_t stream,
+                                      fuse_graph_t* out) {
+  if (!out) return FUSE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!stream) return FUSE_ERR_INVALID_ARG;     // the legacy stream cannot be captured
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return FUSE_ERR_CUDA;
+  if (cs != cudaStreamCaptureStatusNone) return FUSE_ERR_INVALID_ARG;
+  // relaxed mode: the once-per-device set-up of a first call (shared-memory
+  // limits, occupancy queries) is not a stream operation and may run inside
+  if (cudaStreamBeginCapture(s, cudaStreamCaptureModeRelaxed) != cudaSuccess) return FUSE_ERR_CUDA;
+  const fuse_status_t st =
+      fuse_stack_step(desc, reqs, n_layers, score_layer, layers, idx, score, ws, ws_bytes, stream);
+  cudaGraph_t g = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(s, &g);
+  if (st != FUSE_OK || e != cudaSuccess || !g) {
+    if (g) cudaGraphDestroy(g);
+    cudaGetLastError();
+    return st != FUSE_OK ? st : FUSE_ERR_CUDA;
+  }
+  cudaGraphExec_t x = nullptr;
+  if (cudaGraphInstantiate(&x, g, 0) != cudaSuccess) {
+    cudaGraphDestroy(g);
+    return FUSE_ERR_CUDA;
+  }
+  fuse_graph_st* h = new (std::nothrow) fuse_graph_st{g, x};
+  if (!h) {
+    cudaGraphExecDestroy(x);
+    cudaGraphDestroy(g);
+    return FUSE_ERR_INVALID_ARG;
+  }
+  *out = h;
+  return FUSE_OK;
+}
+
+fuse_status_t fuse_graph_launch(fuse_graph_t graph, fuse_stream_t stream) {
+  if (!graph) return FUSE_ERR_INVALID_ARG;
+  return cuda_status(cudaGraphLaunch(graph->exec, (cudaStream_t)stream));
+}
+
+void fuse_graph_destroy(fuse_graph_t graph) {
+  if (!graph) return;
+  cudaGraphExecDestroy(graph->exec);
+  cudaGraphDestroy(graph->graph);
+  delete graph;
 }
 
 fuse_status_t fuse_stack_pipeline_plan(int32_t n_layers, int32_t score_layer,

@@ -270,6 +270,8 @@ __global__ void __launch_bounds__(1024) query_offsets_kernel(const fuse_request_
                                                              int32_t* qoff) {
   __shared__ int s_warp[32];
   __shared__ int s_carry;
+  pdl_trigger();
+  pdl_wait();
   const int t = threadIdx.x, lane = t % 32, warp = t / 32;
   if (t == 0) s_carry = 0;
   __syncthreads();
@@ -302,16 +304,37 @@ __global__ void __launch_bounds__(1024) query_offsets_kernel(const fuse_request_
 }
 
 // One block per (query token, request): its packed work row, RoPE table at
-// position N + u, and (tensor-core projection) its gathered input row.
+// position N + u, and (tensor-core projection) its gathered input row.  With
+// own_offsets (few requests) each block sums the query counts of the
+// requests before its own, and the first block of a request writes qoff;
+// otherwise query_offsets_kernel wrote qoff before.
 __global__ void __launch_bounds__(256) prepare_query_rows_kernel(
-    const fuse_request_t* reqs, const int32_t* qoff, RopeFreqs f, int half_dim,
+    const fuse_request_t* reqs, int32_t* qoff, RopeFreqs f, int half_dim,
     const __nv_bfloat16* H, int hidden, WorkRow* rows, float2* rope, int64_t n_rows,
-    __nv_bfloat16* Hs, uint32_t* err) {
+    __nv_bfloat16* Hs, uint32_t* err, int own_offsets) {
+  __shared__ int s_off[8];
   const int r = blockIdx.y;
-  const fuse_request_t R = reqs[r];
+  const fuse_request_t R = reqs[r];   // the caller's table: no kernel writes it
   const int u = blockIdx.x;
-  if (u >= R.n_query) return;
-  const int64_t m = (int64_t)qoff[r] + u;
+  pdl_trigger();
+  pdl_wait();
+  if (u >= R.n_query) return;         // block-uniform
+  int off;
+  if (own_offsets) {
+    int acc = 0;
+    for (int i = threadIdx.x; i < r; i += 256) acc += reqs[i].n_query;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if ((threadIdx.x & 31) == 0) s_off[threadIdx.x >> 5] = acc;
+    __syncthreads();
+    off = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) off += s_off[w];
+    if (u == 0 && threadIdx.x == 0) qoff[r] = off;
+  } else {
+    off = qoff[r];
+  }
+  const int64_t m = (int64_t)off + u;
   if (m < 0 || m >= n_rows) {                 // the device table differs from the host's
     if (threadIdx.x == 0) report_error(err, FUSE_ERR_DEVICE_BOUNDS, SITE_MASS_ROWS, r);
     return;
@@ -370,12 +393,17 @@ cudaError_t launch_query_rows(const fuse_requests_t& reqs, int max_query, const 
                               int64_t n_rows, void* Hs, int32_t* qoff, uint32_t* err,
                               cudaStream_t s) {
   if (reqs.n_req == 0) return cudaSuccess;
-  query_offsets_kernel<<<1, 1024, 0, s>>>(reqs.d_req, reqs.n_req, qoff);
-  if (max_query > 0 && n_rows > 0)
-    prepare_query_rows_kernel<<<dim3(max_query, reqs.n_req), 256, 0, s>>>(
-        reqs.d_req, qoff, freqs, head_dim / 2, reinterpret_cast<const __nv_bfloat16*>(H), hidden,
-        rows, rope, n_rows, reinterpret_cast<__nv_bfloat16*>(Hs), err);
-  return cudaGetLastError();
+  // few requests: the row kernel forms the offsets itself (one launch); else
+  // a block scan first
+  const int own = reqs.n_req <= 1024 && max_query > 0 && n_rows > 0;
+  cudaError_t e = cudaSuccess;
+  if (!own) e = launch_pdl(query_offsets_kernel, dim3(1), dim3(1024), 0, s, reqs.d_req,
+                           reqs.n_req, qoff);
+  if (e == cudaSuccess && max_query > 0 && n_rows > 0)
+    e = launch_pdl(prepare_query_rows_kernel, dim3(max_query, reqs.n_req), dim3(256), 0, s,
+                   reqs.d_req, qoff, freqs, head_dim / 2, reinterpret_cast<const __nv_bfloat16*>(H),
+                   hidden, rows, rope, n_rows, reinterpret_cast<__nv_bfloat16*>(Hs), err, own);
+  return e;
 }
 
 cudaError_t launch_attention_mass(const fuse_layer_desc_t& d, const fuse_requests_t& reqs,

@@ -32,6 +32,7 @@ enum ErrSite : uint32_t {
   SITE_ATTN_TIMEOUT = 7,     // attention pipeline wait gave up
   SITE_STITCH_TIMEOUT = 8,   // stitch bulk-copy wait gave up
   SITE_MASS_ROWS = 9,        // query rows past the host's count (device table differs)
+  SITE_MASS_TIMEOUT = 10,    // tensor-core attention-mass pipeline wait gave up
 };
 
 __device__ __forceinline__ void report_error(uint32_t* err, fuse_status_t code, uint32_t site,
@@ -200,8 +201,12 @@ __host__ __device__ inline int64_t rope_index(int j, int64_t m, int64_t n_rows) 
 // index, clamped to the request like the row tables, or n_ctx + query row).
 // Run by every thread of one block of a multiple of 32 threads, at most 1024
 // (the caller's branch must be block-uniform); requests past kTileReqsSmem
-// are enumerated by one thread (slower, same result).
+// are enumerated by one thread (slower, same result).  Up to kTileSortMax
+// tiles are ordered by key blocks, ascending and stable, so that the
+// attention kernel (which takes the last tiles first) starts the heaviest
+// tiles of every request of a batch first; more stay in request order.
 constexpr int kTileReqsSmem = 1024;
+constexpr int kTileSortMax = 1024;
 __device__ inline void build_attn_tiles(const fuse_request_t* reqs, int n_req, const int32_t* idx,
                                         int rtile, int4* tiles) {
   __shared__ int s_first[kTileReqsSmem + 1];     // first tile of each request, then the total
@@ -258,6 +263,8 @@ __device__ inline void build_attn_tiles(const fuse_request_t* reqs, int n_req, c
   if (tid == 0) s_first[n_req] = carry;
   __syncthreads();
   const int nt = s_first[n_req];
+  __shared__ int4 s_rec[kTileSortMax];
+  const bool sort = nt <= kTileSortMax;          // block-uniform
   for (int t = tid; t < nt; t += nth) {
     int lo = 0, hi = n_req - 1;                  // the request: last q with s_first[q] <= t
     while (lo < hi) {
@@ -269,7 +276,24 @@ __device__ inline void build_attn_tiles(const fuse_request_t* reqs, int n_req, c
     const int rows = min(rtile, R.k + R.n_query - r0);
     const int o = r0 + rows - 1;
     const int pos = o < R.k ? min(max(idx[R.sel0 + o], 0), max(R.n_ctx - 1, 0)) : R.n_ctx + (o - R.k);
-    tiles[t] = make_int4((int)R.out0 + r0, (int)R.row0, rows, pos / 128 + 1);
+    const int4 rec = make_int4((int)R.out0 + r0, (int)R.row0, rows, pos / 128 + 1);
+    if (sort)
+      s_rec[t] = rec;
+    else
+      tiles[t] = rec;
+  }
+  if (!sort) return;
+  __syncthreads();
+  // stable rank by key blocks: the tiles with fewer blocks, and those with as
+  // many that come earlier
+  for (int t = tid; t < nt; t += nth) {
+    const int w = s_rec[t].w;
+    int rank = 0;
+    for (int q = 0; q < nt; ++q) {
+      const int wq = s_rec[q].w;
+      rank += (wq < w) || (wq == w && q < t);
+    }
+    tiles[rank] = s_rec[t];
   }
 }
 #endif

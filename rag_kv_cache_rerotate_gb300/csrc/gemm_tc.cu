@@ -54,7 +54,7 @@ constexpr int kTmemCols = 2 * kAccCols;             // two accumulators: all 512
 constexpr int kEpiThreads = 256;                    // two warpgroups, one per head
 constexpr int kThreads = 64 + kEpiThreads;
 
-enum Mode : int { MODE_DEVIATION = 0, MODE_RECOMPUTE = 1 };
+enum Mode : int { MODE_DEVIATION = 0, MODE_RECOMPUTE = 1, MODE_SPLITK = 2 };
 
 struct TcArgs {
   int M;                 // rows of A
@@ -71,6 +71,7 @@ struct TcArgs {
   // of Vf, so that the stitch may run alongside; null: read Vf
   const fuse_chunk_t* chunks;    // sorted by dst_row, non-overlapping
   int n_chunks;
+  int kv_u8;                     // chunk caches hold KIVI int8 codes (dequantised here)
   int kv_paged;
   int block_size;
   int64_t n_pool_blocks;
@@ -86,6 +87,12 @@ struct TcArgs {
   __nv_bfloat16* Vout;
   uint32_t* err;
   int st32;              // Q, Kf and Vout 32-byte aligned: one 256-bit store per 16 values
+  // split over K (MODE_SPLITK): tile t of the K range [ks K / k_splits,
+  // (ks + 1) K / k_splits) writes its fp32 accumulator to
+  // split_out[(ks * M + m) * split_cols + head * 128 + c]
+  int k_splits;
+  float* split_out;
+  int split_cols;
 };
 
 struct SharedCtl {
@@ -138,35 +145,68 @@ struct DevPre {
 };
 
 // Where the cached V row of packed row m lives: in the chunk cache whose
-// fused rows hold m (what the stitch copies to Vf[m]), else in Vf itself (a
-// row no chunk covers keeps its contents).
-__device__ __forceinline__ const __nv_bfloat16* cached_v_row(const TcArgs& a, int m, int head) {
-  const int64_t fused = ((int64_t)m * a.n_kv_heads + head) * BN;
-  if (!a.chunks || a.n_chunks == 0) return a.Vf + fused;
+// fused rows hold m (what the stitch writes to Vf[m]), else in Vf itself (a
+// row no chunk covers keeps its contents).  Returns the chunk (null for Vf)
+// and the source row (pool row when paged; -1 for an out-of-pool block id,
+// which the stitch reports).
+__device__ __forceinline__ const fuse_chunk_t* cached_v_chunk(const TcArgs& a, int m,
+                                                              int64_t* tok) {
+  if (!a.chunks || a.n_chunks == 0) return nullptr;
   int lo = 0, hi = a.n_chunks - 1;
   while (lo < hi) {                       // last chunk with dst_row <= m
     const int mid = (lo + hi + 1) >> 1;
     if (a.chunks[mid].dst_row <= m) lo = mid; else hi = mid - 1;
   }
-  const fuse_chunk_t& c = a.chunks[lo];
-  const int64_t r = m - c.dst_row;
-  if (r < 0 || r >= c.len) return a.Vf + fused;
-  int64_t tok = r;
+  const fuse_chunk_t* c = &a.chunks[lo];
+  const int64_t r = m - c->dst_row;
+  if (r < 0 || r >= c->len) return nullptr;
+  *tok = r;
   if (a.kv_paged) {
-    const int32_t b = __ldg(c.block_table + r / a.block_size);
-    if (b < 0 || b >= a.n_pool_blocks) return nullptr;   // reported by the stitch
-    tok = (int64_t)b * a.block_size + r % a.block_size;
+    const int32_t b = __ldg(c->block_table + r / a.block_size);
+    *tok = (b < 0 || b >= a.n_pool_blocks) ? -1 : (int64_t)b * a.block_size + r % a.block_size;
   }
-  return reinterpret_cast<const __nv_bfloat16*>(c.v) + (tok * a.n_kv_heads + head) * BN;
+  return c;
 }
 
 __device__ __forceinline__ void pre_deviation(const TcArgs& a, int m, int head, DevPre& p) {
   p.slot = m < a.M ? row_slot(a, m) : -1;
-  if (p.slot >= 0) {
-    const uint4* vrow = reinterpret_cast<const uint4*>(cached_v_row(a, m, head));
+  if (p.slot < 0) return;
+  int64_t tok = 0;
+  const fuse_chunk_t* c = cached_v_chunk(a, m, &tok);
+  if (c && tok < 0) {
 #pragma unroll
-    for (int q = 0; q < BN / 8; ++q) p.v[q] = vrow ? __ldg(vrow + q) : make_uint4(0u, 0u, 0u, 0u);
+    for (int q = 0; q < BN / 8; ++q) p.v[q] = make_uint4(0u, 0u, 0u, 0u);
+    return;
   }
+  if (c && a.kv_u8) {
+    // KIVI int8 value codes: x = zero + q * scale per token, rounded to bf16
+    // as the stitch stores it
+    const int64_t th = tok * a.n_kv_heads + head;
+    const uint4* qrow = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(c->v) + th * BN);
+    uint4 qv[BN / 16];
+#pragma unroll
+    for (int q = 0; q < BN / 16; ++q) qv[q] = __ldg(qrow + q);
+    const float sc = __half2float(reinterpret_cast<const __half*>(c->v_scale)[th]);
+    const float z = __half2float(reinterpret_cast<const __half*>(c->v_zero)[th]);
+#pragma unroll
+    for (int q = 0; q < BN / 16; ++q) {
+      const uint32_t w[4] = {qv[q].x, qv[q].y, qv[q].z, qv[q].w};
+      uint32_t o[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t ww = w[e >> 1] >> (16 * (e & 1));
+        o[e] = pack_bf16x2(fmaf((float)(ww & 0xFFu), sc, z), fmaf((float)((ww >> 8) & 0xFFu), sc, z));
+      }
+      p.v[2 * q] = make_uint4(o[0], o[1], o[2], o[3]);
+      p.v[2 * q + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+    return;
+  }
+  const uint4* vrow = reinterpret_cast<const uint4*>(
+      c ? reinterpret_cast<const __nv_bfloat16*>(c->v) + (tok * a.n_kv_heads + head) * BN
+        : a.Vf + ((int64_t)m * a.n_kv_heads + head) * BN);
+#pragma unroll
+  for (int q = 0; q < BN / 8; ++q) p.v[q] = __ldg(vrow + q);
 }
 
 // Cosine of this row and head (0 for rows without a score slot).
@@ -303,6 +343,50 @@ __device__ __forceinline__ void epi_recompute(const TcArgs& a, uint32_t taddr, i
   }
 }
 
+// Tile t of the pair grid: row tile, column tile (two heads) and K split.
+// The dimension with fewer tiles varies fastest, so the pairs running at one
+// time share the other operand's tiles: a row tile of a tall A (the
+// deviation's H) is read from memory once for all its column tiles, a
+// weight tile of a wide B (the recompute's) once for all row tiles.
+struct TileIdx {
+  int mt, nt, kb0, kb1, ks;
+};
+__device__ __forceinline__ TileIdx tile_idx(const TcArgs& a, int t, int k_blocks) {
+  TileIdx x;
+  const int mn = a.m_tiles * a.n_tiles;
+  x.ks = t / mn;
+  const int r = t % mn;
+  if (a.n_tiles <= a.m_tiles) {
+    x.nt = r % a.n_tiles;
+    x.mt = r / a.n_tiles;
+  } else {
+    x.mt = r % a.m_tiles;
+    x.nt = r / a.m_tiles;
+  }
+  x.kb0 = x.ks * k_blocks / a.k_splits;
+  x.kb1 = (x.ks + 1) * k_blocks / a.k_splits;
+  return x;
+}
+
+// Split-K epilogue: this row's fp32 accumulator of one head, as it is.
+__device__ __forceinline__ void epi_splitk(const TcArgs& a, uint32_t taddr, int m, int head,
+                                           int ks) {
+#pragma unroll
+  for (int c0 = 0; c0 < BN; c0 += 32) {
+    uint32_t r[32];
+    tc::tmem_ld_32x32b_x32(taddr + c0, r);
+    tc::tmem_ld_wait();
+    if (m < a.M) {
+      float4* dst = reinterpret_cast<float4*>(
+          a.split_out + ((int64_t)ks * a.M + m) * a.split_cols + head * BN + c0);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                             __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+    }
+  }
+}
+
 // B tensor map and first row of head `head` (the heads of map 0, then 1, then 2).
 __device__ __forceinline__ void b_map_of(const TcArgs& a, int head, const CUtensorMap* m0,
                                          const CUtensorMap* m1, const CUtensorMap* m2,
@@ -330,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const uint32_t rank = tc::cluster_rank();          // 0: issues the pair's MMAs
-  const int total = a.m_tiles * a.n_tiles;
+  const int total = a.m_tiles * a.n_tiles * a.k_splits;
   const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
   const int k_blocks = a.K / BK;
 
@@ -381,18 +465,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       // B of the first tile's first stages, before the wait
       int pre = 0;
       if (pair < total) {
-        const int head = 2 * (pair / a.m_tiles) + (int)rank;
+        const TileIdx t0 = tile_idx(a, pair, k_blocks);
+        const int head = 2 * t0.nt + (int)rank;
         const CUtensorMap* mb;
         int nrow;
         b_map_of(a, head, &mapB0, &mapB1, &mapB2, mb, nrow);
-        pre = k_blocks < STAGES ? k_blocks : STAGES;
-        for (int kb = 0; kb < pre; ++kb) {          // stage kb, first use: no wait for it
-          uint8_t* sa = smem + kb * kStageBytes;
+        pre = t0.kb1 - t0.kb0 < STAGES ? t0.kb1 - t0.kb0 : STAGES;
+        for (int i = 0; i < pre; ++i) {             // stage i, first use: no wait for it
+          uint8_t* sa = smem + i * kStageBytes;
+          const int kb = t0.kb0 + i;
           if (rank == 0) {
-            tc::mbar_arrive_expect_tx(&ctl->full[kb], 2 * kStageBytes);
-            tc::tma_load_2d(sa + kTileBytes, mb, &ctl->full[kb], kb * BK, nrow);
+            tc::mbar_arrive_expect_tx(&ctl->full[i], 2 * kStageBytes);
+            tc::tma_load_2d(sa + kTileBytes, mb, &ctl->full[i], kb * BK, nrow);
           } else {
-            tc::tma_load_2d_pair(sa + kTileBytes, mb, leader_full + kb * (uint32_t)sizeof(uint64_t),
+            tc::tma_load_2d_pair(sa + kTileBytes, mb, leader_full + i * (uint32_t)sizeof(uint64_t),
                                  kb * BK, nrow);
           }
         }
@@ -400,21 +486,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       pdl_wait();
       pdl_trigger();
       for (int tile = pair; tile < total && ok; tile += n_pairs) {
-        const int mt = tile % a.m_tiles;
-        const int nt = tile / a.m_tiles;
-        const int head = 2 * nt + (int)rank;
+        const TileIdx tx = tile_idx(a, tile, k_blocks);
+        const int head = 2 * tx.nt + (int)rank;
         const CUtensorMap* mb;
         int nrow;
         b_map_of(a, head, &mapB0, &mapB1, &mapB2, mb, nrow);
-        const int arow = mt * BMP + (int)rank * BM;
-        for (int kb = 0; kb < k_blocks; ++kb) {
+        const int arow = tx.mt * BMP + (int)rank * BM;
+        for (int kb = tx.kb0; kb < tx.kb1; ++kb) {
           if (!wait_or_abort(&ctl->empty[s], ph ^ 1, ctl)) {
             abort_kernel(ctl, a.err);
             ok = false;
             break;
           }
           uint8_t* sa = smem + s * kStageBytes;
-          const bool b_done = tile == pair && kb < pre;   // armed and B requested above
+          const bool b_done = tile == pair && kb - tx.kb0 < pre;   // armed and B requested above
           if (rank == 0) {
             // the stage is full once both CTAs' bytes have landed
             if (!b_done) tc::mbar_arrive_expect_tx(&ctl->full[s], 2 * kStageBytes);
@@ -458,7 +543,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kAccCols;
-        for (int kb = 0; kb < k_blocks; ++kb) {
+        const TileIdx tx = tile_idx(a, tile, k_blocks);
+        for (int kb = tx.kb0; kb < tx.kb1; ++kb) {
           if (!wait_or_abort(&ctl->full[s], ph, ctl)) {
             abort_kernel(ctl, a.err);
             ok = false;
@@ -470,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t db = tc::smem_desc_k128(sa + kTileBytes);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            tc::mma_bf16_pair(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+            tc::mma_bf16_pair(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb != tx.kb0) || k != 0);
           tc::mma_commit_pair(&ctl->empty[s], 0x3);
           if (++s == STAGES) {
             s = 0;
@@ -505,16 +591,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_ph = 0;
     for (int tile = pair; tile < total; tile += n_pairs) {
-      const int mt = tile % a.m_tiles;
-      const int nt = tile / a.m_tiles;
-      const int m = mt * BMP + (int)rank * BM + row;
+      const TileIdx tx = tile_idx(a, tile, k_blocks);
+      const int nt = tx.nt;
+      const int m = tx.mt * BMP + (int)rank * BM + row;
       const int head = 2 * nt + hb;
       // one of the two is used (MODE is a compile-time constant)
       DevPre dp;
       RecPre rp;
       if constexpr (MODE == MODE_DEVIATION)
         pre_deviation(a, m, head, dp);
-      else
+      else if constexpr (MODE == MODE_RECOMPUTE)
         pre_recompute(a, m, head, rp);
       if (!tc::mbar_wait_warp(&ctl->tfull[acc], acc_ph, &ctl->abort_flag)) {
         abort_kernel(ctl, a.err);
@@ -537,8 +623,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (dp.slot >= 0) a.partial[(int64_t)dp.slot * (a.n_kv_heads / 2) + nt] = c + ctl->xc[acc][row];
         }
-      } else {
+      } else if constexpr (MODE == MODE_RECOMPUTE) {
         epi_recompute(a, taddr, m, rp);
+      } else {
+        epi_splitk(a, taddr, m, head, tx.ks);
       }
       tc::tc_fence_before();
       tc::mbar_arrive(&ctl->tempty[acc]);
@@ -619,9 +707,11 @@ int resident_pairs(const void* kernel) {
 
 cudaError_t launch(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtensorMap& mB1,
                    const CUtensorMap& mB2, const TcArgs& a, cudaStream_t s) {
-  const int total = a.m_tiles * a.n_tiles;
+  const int total = a.m_tiles * a.n_tiles * a.k_splits;
   if (total == 0) return cudaSuccess;
-  auto kernel = a.mode == MODE_DEVIATION ? gemm_tc_kernel<MODE_DEVIATION> : gemm_tc_kernel<MODE_RECOMPUTE>;
+  auto kernel = a.mode == MODE_DEVIATION   ? gemm_tc_kernel<MODE_DEVIATION>
+                : a.mode == MODE_RECOMPUTE ? gemm_tc_kernel<MODE_RECOMPUTE>
+                                           : gemm_tc_kernel<MODE_SPLITK>;
   cudaError_t e = set_dyn_smem_once(reinterpret_cast<const void*>(kernel), kSmemBytes);
   if (e != cudaSuccess) return e;
   const int pairs = std::min(total, resident_pairs(reinterpret_cast<const void*>(kernel)));
@@ -673,6 +763,7 @@ cudaError_t launch_deviation_partials_tc(const fuse_layer_desc_t& d, int64_t n_r
   a.h0 = d.n_kv_heads;
   a.h1 = 0;
   a.mode = MODE_DEVIATION;
+  a.k_splits = 1;
   a.n_q_heads = d.n_q_heads;
   a.n_kv_heads = d.n_kv_heads;
   a.Vf = reinterpret_cast<const __nv_bfloat16*>(Vf);
@@ -683,6 +774,7 @@ cudaError_t launch_deviation_partials_tc(const fuse_layer_desc_t& d, int64_t n_r
   if (v_chunks) {
     a.chunks = v_chunks->d_chunks;
     a.n_chunks = v_chunks->n_chunks;
+    a.kv_u8 = v_chunks->kv_storage == FUSE_U8_ASYM;
     a.kv_paged = v_chunks->kv_layout == FUSE_KV_PAGED;
     a.block_size = v_chunks->block_size > 0 ? v_chunks->block_size : 1;
     a.n_pool_blocks = v_chunks->n_pool_blocks;
@@ -718,6 +810,7 @@ cudaError_t launch_project_recompute_tc(const fuse_layer_desc_t& d, int64_t n_ro
   a.h0 = d.n_q_heads;
   a.h1 = d.n_kv_heads;
   a.mode = MODE_RECOMPUTE;
+  a.k_splits = 1;
   a.n_q_heads = d.n_q_heads;
   a.n_kv_heads = d.n_kv_heads;
   a.rows = rows;
@@ -731,10 +824,49 @@ cudaError_t launch_project_recompute_tc(const fuse_layer_desc_t& d, int64_t n_ro
   return launch(mA, mQ, mK, mV, a, s);
 }
 
+namespace {
+
+// Sum of the K splits in a fixed order, RoPE at each row's position, bf16 out:
+// one block per (row, head), one thread per rotation pair.
+__global__ void __launch_bounds__(64) splitk_rope_kernel(const float* part, int k_splits, int M,
+                                                         int n_heads, const float2* rope,
+                                                         __nv_bfloat16* Q) {
+  pdl_trigger();
+  pdl_wait();
+  const int m = blockIdx.x, head = blockIdx.y, j = threadIdx.x;   // pair (j, j + 64)
+  const int cols = n_heads * BN;
+  float x = 0.f, y = 0.f;
+  for (int ks = 0; ks < k_splits; ++ks) {
+    const float* p = part + ((int64_t)ks * M + m) * cols + head * BN;
+    x += p[j];
+    y += p[j + BN / 2];
+  }
+  const float2 c = rope[rope_index(j, m, M)];
+  __nv_bfloat16* o = Q + ((int64_t)m * n_heads + head) * BN;
+  o[j] = __float2bfloat16_rn(fmaf(x, c.x, -y * c.y));
+  o[j + BN / 2] = __float2bfloat16_rn(fmaf(y, c.x, x * c.y));
+}
+
+}  // namespace
+
+// Splits over K for a projection of n_rows rows onto n_heads heads: enough
+// for the pair tiles to cover the resident pairs, at least four 64-deep
+// steps each, at most 8.
+int query_k_splits(const fuse_layer_desc_t& d, int64_t n_rows, int n_heads) {
+  const int64_t tiles = ((n_rows + BMP - 1) / BMP) * (n_heads / 2);
+  const int pairs = resident_pairs(reinterpret_cast<const void*>(gemm_tc_kernel<MODE_SPLITK>));
+  int64_t ks = std::max<int64_t>(1, pairs / std::max<int64_t>(tiles, 1));
+  ks = std::min<int64_t>(ks, std::max(1, d.hidden / BK / 4));
+  return (int)std::min<int64_t>(ks, 8);
+}
+
 // Q heads only (query-aware scoring): Q[m] = R^{pos} W_Q Hs[m]; no K/V scatter.
+// With split_ws (room for max_splits * n_rows * Hq * 128 floats) and more
+// than one split, the pair tiles split K and a second launch sums the splits
+// in order and rotates; otherwise the recompute epilogue rotates.
 cudaError_t launch_project_query_tc(const fuse_layer_desc_t& d, int64_t n_rows, const float2* rope,
                                     const void* Wq, void* Q, const void* Hs, uint32_t* err,
-                                    cudaStream_t s) {
+                                    cudaStream_t s, float* split_ws, int max_splits) {
   if (n_rows == 0) return cudaSuccess;
   CUtensorMap mA, mQ;
   if (!make_map(&mA, Hs, n_rows, d.hidden) ||
@@ -748,13 +880,24 @@ cudaError_t launch_project_query_tc(const fuse_layer_desc_t& d, int64_t n_rows, 
   a.h0 = d.n_q_heads;
   a.h1 = 0;
   a.mode = MODE_RECOMPUTE;
+  a.k_splits = 1;
   a.n_q_heads = d.n_q_heads;
   a.n_kv_heads = d.n_kv_heads;
   a.rope = rope;
   a.Q = reinterpret_cast<__nv_bfloat16*>(Q);
   a.st32 = (reinterpret_cast<uintptr_t>(Q) & 31u) == 0;
   a.err = err;
-  return launch(mA, mQ, mQ, mQ, a, s);
+  const int ks = split_ws ? std::min(max_splits, query_k_splits(d, n_rows, d.n_q_heads)) : 1;
+  if (ks <= 1) return launch(mA, mQ, mQ, mQ, a, s);
+  a.mode = MODE_SPLITK;
+  a.k_splits = ks;
+  a.split_out = split_ws;
+  a.split_cols = d.n_q_heads * BN;
+  cudaError_t e = launch(mA, mQ, mQ, mQ, a, s);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(splitk_rope_kernel, dim3((unsigned)n_rows, d.n_q_heads), dim3(BN / 2), 0, s,
+                    (const float*)split_ws, ks, (int)n_rows, d.n_q_heads, rope,
+                    reinterpret_cast<__nv_bfloat16*>(Q));
 }
 
 }  // namespace fusekv

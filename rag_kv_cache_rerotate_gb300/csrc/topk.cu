@@ -14,8 +14,9 @@ namespace fusekv {
 
 namespace {
 
-constexpr int kTopkThreads = 1024;
+constexpr int kTopkThreads = 512;    // 128 registers per thread: no spills in the radix rounds
 constexpr int kTopkSmemKeys = 40 * 1024;   // keys kept in shared memory (160 KB)
+constexpr int kTopkBatch = 8;              // tokens per thread whose loads are in flight together
 
 __device__ __forceinline__ uint32_t float_key(float f, bool* is_nan) {
   uint32_t b = __float_as_uint(f);
@@ -95,23 +96,23 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const fuse_request_t
 
   bool nan_seen = false;
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-  // four tokens per thread at a time: their loads are all issued before the
+  // kTopkBatch tokens per thread at a time: their loads are all issued before the
   // first store, so their latencies overlap
-  for (int i0 = t; i0 < n; i0 += 4 * kTopkThreads) {
-    float v[4];
+  for (int i0 = t; i0 < n; i0 += kTopkBatch * kTopkThreads) {
+    float v[kTopkBatch];
     if (partial && n_parts == 4) {                 // one 16-byte load per token
-      float4 pv[4];
+      float4 pv[kTopkBatch];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < kTopkBatch; ++q) {
         const int i = i0 + q * kTopkThreads;
         if (i < n) pv[q] = __ldg(reinterpret_cast<const float4*>(partial) + (R.score0 + i));
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
+      for (int q = 0; q < kTopkBatch; ++q)
         if (i0 + q * kTopkThreads < n) v[q] = head_mean_score4(pv[q], n_kv_heads);
     } else {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < kTopkBatch; ++q) {
         const int i = i0 + q * kTopkThreads;
         if (i < n)
           v[q] = partial ? head_mean_score(partial + (R.score0 + i) * n_parts, n_parts, n_kv_heads)
@@ -119,7 +120,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const fuse_request_t
       }
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < kTopkBatch; ++q) {
       const int i = i0 + q * kTopkThreads;
       if (i < n) {
         if (partial) score_out[R.score0 + i] = v[q];
@@ -145,7 +146,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const fuse_request_t
   }
   __syncthreads();
   if (t < 32) {
-    uint32_t a = warp_buf[t], b = hist[t];
+    constexpr int kWarps = kTopkThreads / 32;
+    uint32_t a = t < kWarps ? warp_buf[t] : 0xFFFFFFFFu, b = t < kWarps ? hist[t] : 0u;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       a = min(a, __shfl_xor_sync(0xffffffffu, a, o));

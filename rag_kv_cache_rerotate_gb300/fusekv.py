@@ -127,6 +127,10 @@ _SIGS = {
                                             _c.c_int32, _c.POINTER(_c.c_int32)]),
     "fuse_stack_step": (_c.c_int, [_P, _P, _c.c_int32, _c.c_int32, _P, _P, _P, _P, _c.c_size_t, _P]),
     "fuse_kivi_quantize": (_c.c_int, [_P, _P, _P, _P]),
+    "fuse_stack_graph_create": (_c.c_int, [_P, _P, _c.c_int32, _c.c_int32, _P, _P, _P, _P,
+                                           _c.c_size_t, _P, _c.POINTER(_c.c_void_p)]),
+    "fuse_graph_launch": (_c.c_int, [_c.c_void_p, _P]),
+    "fuse_graph_destroy": (None, [_c.c_void_p]),
     "fuse_check_errors": (_c.c_int, [_P, _P, _c.POINTER(_c.c_uint32)]),
     "fuse_static_select_count": (_c.c_int, [_P, _P, _c.c_int32, _c.c_int32, _P]),
     "fuse_static_select": (_c.c_int, [_P, _P, _c.c_int32, _c.c_int32, _P, _P]),
@@ -361,6 +365,39 @@ def stack_step(desc, reqs: RequestTable, layers, score_layer: int, idx, score, w
     _check(load().fuse_stack_step(_c.byref(desc), _c.byref(reqs.c), len(layers), int(score_layer),
                                   arr, _ptr(idx), _ptr(score), _ptr(ws), ws.numel(),
                                   _stream(stream)), "fuse_stack_step")
+
+
+class StackGraph:
+    """``fuse_stack_step`` captured once as a CUDA graph (``fuse_stack_graph_create``)
+    and replayed with ``launch()``; the buffers must stay where they are."""
+
+    def __init__(self, desc, reqs: RequestTable, layers, score_layer: int, idx, score, ws,
+                 stream=None):
+        arr = (LayerIO * len(layers))()
+        for i, b in enumerate(layers):
+            arr[i] = LayerIO(_c.addressof(b.chunks.c), _ptr(b.H), _ptr(b.Wq), _ptr(b.Wk),
+                             _ptr(b.Wv), _ptr(b.Kf), _ptr(b.Vf), _ptr(b.O))
+        self.keep = (desc, reqs, layers, arr, idx, score, ws)
+        h = _c.c_void_p(None)
+        _check(load().fuse_stack_graph_create(_c.byref(desc), _c.byref(reqs.c), len(layers),
+                                              int(score_layer), arr, _ptr(idx), _ptr(score),
+                                              _ptr(ws), ws.numel(), _stream(stream), _c.byref(h)),
+               "fuse_stack_graph_create")
+        self.h = h
+
+    def launch(self, stream=None):
+        _check(load().fuse_graph_launch(self.h, _stream(stream)), "fuse_graph_launch")
+
+    def close(self):
+        if self.h:
+            load().fuse_graph_destroy(self.h)
+            self.h = _c.c_void_p(None)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def stack_pipeline_plan(n_layers: int, score_layer: int, slot_of_layer: Sequence[int],

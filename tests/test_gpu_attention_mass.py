@@ -26,7 +26,11 @@ pytestmark = pytest.mark.gpu
 # fp32 (SIMT projection), bf16 d = 64 ragged/paged with empty queries (SIMT
 # projection in bf16), the Qwen3-8B-shaped layer and three requests of the
 # batched paged workload (tensor-core projection)
-CASES = ["tiny_fp32", "ragged_fp32", "ragged_paged_bf16_d64", "paged3", "qwen3_8b_layer"]
+# the tensor-core scorer: three requests of the batched paged workload, the
+# Qwen3-8B-shaped layer, and four 1024-token chunks of the Llama-3-70B shape
+# (eight query heads per KV head: four 128-vector tiles per KV head)
+CASES = ["tiny_fp32", "ragged_fp32", "ragged_paged_bf16_d64", "paged3", "qwen3_8b_layer",
+         "int8_4x1024"]
 
 
 def _tol(cfg):
@@ -126,5 +130,40 @@ def test_attention_mass_edges():
             assert np.array_equal(g_r, np.zeros(n))
         else:
             assert np.all(np.abs(g_r - want) <= 1e-4 * want + 1e-6), i
+        row += n + qn
+    assert np.array_equal(got[t.n_ctx:], [7.0, 7.0, 7.0])
+
+
+def test_attention_mass_tensor_core_edges():
+    # the tensor-core path (bf16, head_dim 128): a request with no query
+    # scores 0, one with no context is skipped, ragged vector and key tiles
+    # (160 vectors: two 128-vector tiles; 300 keys: a partial key tile), and
+    # entries outside every request are left untouched
+    desc = fk.layer_desc(512, 8, 2, 128, 5e5, fk.FUSE_BF16)
+    n_ctx, n_query = [300, 0, 5, 129, 77], [40, 4, 0, 1, 32]
+    reqs = fk.plan_requests(n_ctx, n_query, 0.25)
+    t = reqs.totals()
+    g = torch.Generator().manual_seed(5)
+    H = torch.randn(t.n_tok, 512, generator=g).to(torch.bfloat16).cuda()
+    Wq = (torch.randn(8 * 128, 512, generator=g) / 22.6).to(torch.bfloat16).cuda()
+    Kf = torch.randn(t.n_tok, 2, 128, generator=g).to(torch.bfloat16).cuda()
+    score = torch.full((t.n_ctx + 3,), 7.0, device="cuda")
+    ws = fk.alloc_workspace(desc, reqs)
+    fk.score_attention_mass(desc, reqs, H, Wq, Kf, score, ws)
+    fk.check_errors(ws)
+    got = score.cpu().numpy().astype(np.float64)
+    Hn, Wn, Kn = f64(H), f64(Wq), f64(Kf)
+    row = 0
+    for i, (n, qn) in enumerate(zip(n_ctx, n_query)):
+        q = reqs[i]
+        g_r = got[q.score0:q.score0 + n]
+        if qn == 0:
+            assert np.array_equal(g_r, np.zeros(n))
+        elif n:
+            want = orc.attention_mass_scores(Hn[row + n:row + n + qn], Wn, Kn[row:row + n], 8, 2,
+                                             128, 5e5, orc.round_bf16)
+            floor = 1e-6 * qn * 8 / n
+            assert np.all(np.abs(g_r - want) <= 2e-3 * want + floor), i
+            assert abs(g_r.sum() - qn * 8) <= 1e-4 * qn * 8
         row += n + qn
     assert np.array_equal(got[t.n_ctx:], [7.0, 7.0, 7.0])
