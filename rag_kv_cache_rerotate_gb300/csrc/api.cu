@@ -484,10 +484,9 @@ fuse_status_t do_score_select(const fuse_layer_desc_t& d, const fuse_requests_t&
 }
 
 // Stitch and score/select of one layer.  On the tensor-core path with chunk
-// caches of the layer's type or int8 codes, placed in order, the deviation
-// GEMM reads the cached V rows from the chunks themselves (dequantising int8
-// codes as the stitch does) and the stitch runs beside it (it waits for the
-// GEMM only at its end); otherwise in sequence.
+// caches of the layer's type placed in order, the deviation GEMM reads the
+// cached V rows from the chunks themselves and the stitch runs beside it (it
+// waits for the GEMM only at its end); otherwise in sequence.
 fuse_status_t do_stitch_score_select(const fuse_layer_desc_t& d, const fuse_chunks_t& c,
                                      int max_len, const fuse_requests_t& r, const ReqInfo& info,
                                      const void* H, const void* Wv, void* Kf, void* Vf,

@@ -71,7 +71,6 @@ struct TcArgs {
   // of Vf, so that the stitch may run alongside; null: read Vf
   const fuse_chunk_t* chunks;    // sorted by dst_row, non-overlapping
   int n_chunks;
-  int kv_u8;                     // chunk caches hold KIVI int8 codes (dequantised here)
   int kv_paged;
   int block_size;
   int64_t n_pool_blocks;
@@ -176,30 +175,6 @@ __device__ __forceinline__ void pre_deviation(const TcArgs& a, int m, int head, 
   if (c && tok < 0) {
 #pragma unroll
     for (int q = 0; q < BN / 8; ++q) p.v[q] = make_uint4(0u, 0u, 0u, 0u);
-    return;
-  }
-  if (c && a.kv_u8) {
-    // KIVI int8 value codes: x = zero + q * scale per token, rounded to bf16
-    // as the stitch stores it
-    const int64_t th = tok * a.n_kv_heads + head;
-    const uint4* qrow = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(c->v) + th * BN);
-    uint4 qv[BN / 16];
-#pragma unroll
-    for (int q = 0; q < BN / 16; ++q) qv[q] = __ldg(qrow + q);
-    const float sc = __half2float(reinterpret_cast<const __half*>(c->v_scale)[th]);
-    const float z = __half2float(reinterpret_cast<const __half*>(c->v_zero)[th]);
-#pragma unroll
-    for (int q = 0; q < BN / 16; ++q) {
-      const uint32_t w[4] = {qv[q].x, qv[q].y, qv[q].z, qv[q].w};
-      uint32_t o[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const uint32_t ww = w[e >> 1] >> (16 * (e & 1));
-        o[e] = pack_bf16x2(fmaf((float)(ww & 0xFFu), sc, z), fmaf((float)((ww >> 8) & 0xFFu), sc, z));
-      }
-      p.v[2 * q] = make_uint4(o[0], o[1], o[2], o[3]);
-      p.v[2 * q + 1] = make_uint4(o[4], o[5], o[6], o[7]);
-    }
     return;
   }
   const uint4* vrow = reinterpret_cast<const uint4*>(
@@ -774,7 +749,6 @@ cudaError_t launch_deviation_partials_tc(const fuse_layer_desc_t& d, int64_t n_r
   if (v_chunks) {
     a.chunks = v_chunks->d_chunks;
     a.n_chunks = v_chunks->n_chunks;
-    a.kv_u8 = v_chunks->kv_storage == FUSE_U8_ASYM;
     a.kv_paged = v_chunks->kv_layout == FUSE_KV_PAGED;
     a.block_size = v_chunks->block_size > 0 ? v_chunks->block_size : 1;
     a.n_pool_blocks = v_chunks->n_pool_blocks;
@@ -827,19 +801,34 @@ cudaError_t launch_project_recompute_tc(const fuse_layer_desc_t& d, int64_t n_ro
 namespace {
 
 // Sum of the K splits in a fixed order, RoPE at each row's position, bf16 out:
-// one block per (row, head), one thread per rotation pair.
-__global__ void __launch_bounds__(64) splitk_rope_kernel(const float* part, int k_splits, int M,
-                                                         int n_heads, const float2* rope,
-                                                         __nv_bfloat16* Q) {
+// one block per (row, four heads), one thread per (head, rotation pair); the
+// splits' loads are all issued before the sum.
+constexpr int kMaxSplits = 8;
+__global__ void __launch_bounds__(256) splitk_rope_kernel(const float* part, int k_splits, int M,
+                                                          int n_heads, const float2* rope,
+                                                          __nv_bfloat16* Q) {
   pdl_trigger();
   pdl_wait();
-  const int m = blockIdx.x, head = blockIdx.y, j = threadIdx.x;   // pair (j, j + 64)
+  const int m = blockIdx.x;
+  const int head = blockIdx.y * 4 + threadIdx.x / (BN / 2), j = threadIdx.x % (BN / 2);
+  if (head >= n_heads) return;
   const int cols = n_heads * BN;
+  float xs[kMaxSplits], ys[kMaxSplits];
+#pragma unroll
+  for (int ks = 0; ks < kMaxSplits; ++ks) {
+    if (ks < k_splits) {
+      const float* p = part + ((int64_t)ks * M + m) * cols + head * BN;
+      xs[ks] = __ldg(p + j);
+      ys[ks] = __ldg(p + j + BN / 2);
+    }
+  }
   float x = 0.f, y = 0.f;
-  for (int ks = 0; ks < k_splits; ++ks) {
-    const float* p = part + ((int64_t)ks * M + m) * cols + head * BN;
-    x += p[j];
-    y += p[j + BN / 2];
+#pragma unroll
+  for (int ks = 0; ks < kMaxSplits; ++ks) {
+    if (ks < k_splits) {
+      x += xs[ks];
+      y += ys[ks];
+    }
   }
   const float2 c = rope[rope_index(j, m, M)];
   __nv_bfloat16* o = Q + ((int64_t)m * n_heads + head) * BN;
@@ -857,7 +846,7 @@ int query_k_splits(const fuse_layer_desc_t& d, int64_t n_rows, int n_heads) {
   const int pairs = resident_pairs(reinterpret_cast<const void*>(gemm_tc_kernel<MODE_SPLITK>));
   int64_t ks = std::max<int64_t>(1, pairs / std::max<int64_t>(tiles, 1));
   ks = std::min<int64_t>(ks, std::max(1, d.hidden / BK / 4));
-  return (int)std::min<int64_t>(ks, 8);
+  return (int)std::min<int64_t>(ks, kMaxSplits);
 }
 
 // Q heads only (query-aware scoring): Q[m] = R^{pos} W_Q Hs[m]; no K/V scatter.
@@ -895,8 +884,8 @@ cudaError_t launch_project_query_tc(const fuse_layer_desc_t& d, int64_t n_rows, 
   a.split_cols = d.n_q_heads * BN;
   cudaError_t e = launch(mA, mQ, mQ, mQ, a, s);
   if (e != cudaSuccess) return e;
-  return launch_pdl(splitk_rope_kernel, dim3((unsigned)n_rows, d.n_q_heads), dim3(BN / 2), 0, s,
-                    (const float*)split_ws, ks, (int)n_rows, d.n_q_heads, rope,
+  return launch_pdl(splitk_rope_kernel, dim3((unsigned)n_rows, (d.n_q_heads + 3) / 4), dim3(256),
+                    0, s, (const float*)split_ws, ks, (int)n_rows, d.n_q_heads, rope,
                     reinterpret_cast<__nv_bfloat16*>(Q));
 }
 

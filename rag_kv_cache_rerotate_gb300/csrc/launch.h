@@ -69,7 +69,7 @@ inline cudaError_t launch_pdl_pairs(void (*kernel)(KArgs...), dim3 grid, dim3 bl
 // Stitch + re-rotate (+ dequantise, + paged gather) every chunk.  free_sms
 // < 0: after the previous kernel; otherwise alongside it (the previous kernel
 // reads no output of the stitch and leaves free_sms SMs free), which needs
-// stitch_streamed(): chunk caches of the layer's type, or int8 codes.
+// stitch_streamed(): chunk caches of the layer's type.
 cudaError_t launch_stitch(const fuse_layer_desc_t& desc, const fuse_chunks_t& chunks,
                           const RopeFreqs& freqs, int max_len, void* Kf, void* Vf, uint32_t* err,
                           cudaStream_t s, int free_sms = -1);

@@ -12,9 +12,9 @@
 // SM), each working through a contiguous range of row tiles with a 3-stage
 // shared-memory ring filled by 1-D bulk copies; the threads rotate the key
 // tile in place and bulk stores write both tiles to the fused cache (values
-// pass through untouched).  For int8 codes stitch_u8_kernel: one CTA moves a
-// few rows of one chunk; each thread owns 16 key pairs and two groups of 16
-// values, and every load of the CTA (16-byte code loads, the values'
+// pass through untouched).  For int8 codes stitch_u8_kernel: tiles of a few
+// rows of one chunk; each thread owns 16 key pairs and two groups of 16
+// values, and every load of a tile (16-byte code loads, the values'
 // per-token scales, the chunk's per-channel key scales into shared memory) is
 // issued before the first use.  Otherwise (int4 codes, or a type change)
 // stitch_kernel, the same scheme with 8-element groups.  Either way the chunk
@@ -263,17 +263,18 @@ __global__ void __launch_bounds__(kStitchThreads) stitch_kernel(const StitchArgs
   }
 }
 
-// ---- int8 codes: 16-byte code loads, all loads of a CTA issued first --------
-// One CTA moves `rows_per_cta` rows of one chunk (the rows of a tile lie in
-// one pool block when paged).  Thread t owns one key item -- 16 pairs
-// (j, j + d/2) of one (row, head), two 16-byte code loads -- and two value
-// items of 16 codes each, with their per-token scale and zero.  The chunk's
-// per-channel key scales and zeros go to shared memory (one 16-byte load
-// each per thread), read back as 16-byte vectors.  Every global load of the
-// CTA is issued before the first use, so the CTA makes one round trip to
-// memory before it computes and stores.
-constexpr int kU8Threads = 256;
-constexpr int kU8MaxRowElems = 2048;                 // Hkv * d of one row (rows per CTA >= 4)
+// ---- int8 codes: 16-byte code loads, all loads of a tile issued first -------
+// A CTA of 128 threads moves tiles of `rows_per_cta` rows of one chunk (the
+// rows of a tile lie in one pool block when paged).  Thread t owns one key
+// item -- 16 pairs (j, j + d/2) of one (row, head), two 16-byte code loads --
+// and two value items of 16 codes each, with their per-token scale and zero.
+// The chunk's per-channel key scales and zeros go to shared memory (16-byte
+// loads), read back as 16-byte vectors.  Every global load of a tile is
+// issued before the first use, so a tile takes one round trip to memory
+// before it is computed and stored.  The kernel walks a contiguous range of
+// tiles per CTA; it is launched with one CTA per tile.
+constexpr int kU8Threads = 128;
+constexpr int kU8MaxRowElems = 2048;                 // Hkv * d of one row (rows per CTA >= 2)
 
 // Element i of 16 fp16 values held as two 16-byte words, as a float.
 __device__ __forceinline__ float half16(const uint4 (&w)[2], int i) {
@@ -290,7 +291,7 @@ __device__ __forceinline__ void codes16(const uint4 q, float (&x)[16]) {
 }
 
 template <typename TO, int D, bool PAGED>
-__global__ void __launch_bounds__(kU8Threads, 4) stitch_u8_kernel(const StitchArgs a) {
+__global__ void __launch_bounds__(kU8Threads, 8) stitch_u8_kernel(const StitchArgs a, int n_tiles) {
   constexpr int H2 = D / 2;
   constexpr int KG = H2 / 16;          // 16-pair key items per head
   constexpr int VG = D / 16;           // 16-code value items per head
@@ -298,112 +299,117 @@ __global__ void __launch_bounds__(kU8Threads, 4) stitch_u8_kernel(const StitchAr
   __shared__ float s_cs[kMaxHalfDim], s_sn[kMaxHalfDim];
   pdl_trigger();
   if (a.wait_first) pdl_wait();
-  const int chunk = blockIdx.x / a.tiles_per_chunk;
-  const int tile = blockIdx.x % a.tiles_per_chunk;
-  const fuse_chunk_t c = a.chunks[chunk];
-  const int r0 = tile * a.rows_per_cta;
-  // completing implies the previous kernel completed, for the kernels after
-  if (r0 >= c.len) {
-    if (!a.wait_first) pdl_wait();
-    return;
-  }
-  const int nrows = min(a.rows_per_cta, c.len - r0);
   const int Hkv = a.n_kv_heads;
   const int t = threadIdx.x;
-  int64_t tok0 = r0;                   // source row of r0 (pool row when paged)
-  if (PAGED) {
-    const int32_t b = __ldg(c.block_table + r0 / a.block_size);
-    if (b < 0 || b >= a.n_pool_blocks) {                 // CTA-uniform
-      if (t == 0) report_error(a.err, FUSE_ERR_DEVICE_BOUNDS, SITE_STITCH_BLOCK, chunk);
-      if (!a.wait_first) pdl_wait();
-      return;
+  const int per = (n_tiles + gridDim.x - 1) / gridDim.x;
+  const int t0 = blockIdx.x * per, t1 = min(n_tiles, t0 + per);
+  int table_chunk = -1;                // chunk whose scales and cos/sin are in shared memory
+  for (int tile = t0; tile < t1; ++tile) {
+    const int chunk = tile / a.tiles_per_chunk;
+    const fuse_chunk_t c = a.chunks[chunk];
+    const int r0 = (tile % a.tiles_per_chunk) * a.rows_per_cta;
+    if (r0 >= c.len) continue;         // CTA-uniform
+    const int nrows = min(a.rows_per_cta, c.len - r0);
+    int64_t tok0 = r0;                 // source row of r0 (pool row when paged)
+    if (PAGED) {
+      const int32_t b = __ldg(c.block_table + r0 / a.block_size);
+      if (b < 0 || b >= a.n_pool_blocks) {               // CTA-uniform
+        if (t == 0) report_error(a.err, FUSE_ERR_DEVICE_BOUNDS, SITE_STITCH_BLOCK, chunk);
+        continue;
+      }
+      tok0 = (int64_t)b * a.block_size + r0 % a.block_size;
     }
-    tok0 = (int64_t)b * a.block_size + r0 % a.block_size;
-  }
-  const uint8_t* kc = reinterpret_cast<const uint8_t*>(c.k);
-  const uint8_t* vc = reinterpret_cast<const uint8_t*>(c.v);
-  const int k_items = nrows * Hkv * KG, v_items = nrows * Hkv * VG;
+    const uint8_t* kc = reinterpret_cast<const uint8_t*>(c.k);
+    const uint8_t* vc = reinterpret_cast<const uint8_t*>(c.v);
+    const int k_items = nrows * Hkv * KG, v_items = nrows * Hkv * VG;
 
-  // 1. every load first
-  uint4 kq0 = make_uint4(0, 0, 0, 0), kq1 = kq0, vq[2] = {kq0, kq0};
-  float vs[2] = {0.f, 0.f}, vz[2] = {0.f, 0.f};
-  if (t < k_items) {
-    const int rh = t / KG;
-    const int64_t e = ((tok0 + rh / Hkv) * Hkv + rh % Hkv) * D + (t % KG) * 16;
-    kq0 = __ldg(reinterpret_cast<const uint4*>(kc + e));
-    kq1 = __ldg(reinterpret_cast<const uint4*>(kc + e + H2));
-  }
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const int it = t + q * kU8Threads;
-    if (it < v_items) {
-      const int rh = it / VG;
-      const int64_t th = (tok0 + rh / Hkv) * Hkv + rh % Hkv;
-      vq[q] = __ldg(reinterpret_cast<const uint4*>(vc + th * D + (it % VG) * 16));
-      vs[q] = __half2float(reinterpret_cast<const __half*>(c.v_scale)[th]);
-      vz[q] = __half2float(reinterpret_cast<const __half*>(c.v_zero)[th]);
+    // 1. every load of the tile first
+    uint4 kq0 = make_uint4(0, 0, 0, 0), kq1 = kq0, vq[2] = {kq0, kq0};
+    float vs[2] = {0.f, 0.f}, vz[2] = {0.f, 0.f};
+    if (t < k_items) {
+      const int rh = t / KG;
+      const int64_t e = ((tok0 + rh / Hkv) * Hkv + rh % Hkv) * D + (t % KG) * 16;
+      kq0 = __ldg(reinterpret_cast<const uint4*>(kc + e));
+      kq1 = __ldg(reinterpret_cast<const uint4*>(kc + e + H2));
     }
-  }
-  for (int i = t * 8; i < Hkv * D; i += kU8Threads * 8) {
-    *reinterpret_cast<uint4*>(s_ks + i) = __ldg(reinterpret_cast<const uint4*>(
-        reinterpret_cast<const __half*>(c.k_scale) + i));
-    *reinterpret_cast<uint4*>(s_kz + i) = __ldg(reinterpret_cast<const uint4*>(
-        reinterpret_cast<const __half*>(c.k_zero) + i));
-  }
-  // 2. the chunk offset's cos/sin of every frequency, while the loads fly
-  const bool rotate = c.pos != 0;
-  if (rotate && t < H2) rope_cos_sin(c.pos, a.freqs.hi[t], a.freqs.mid[t], a.freqs.lo[t], s_cs[t], s_sn[t]);
-  __syncthreads();
-
-  // 3. keys: x = zero + q * scale per channel, rotated by R^{pos}
-  if (t < k_items) {
-    const int rh = t / KG;
-    const int r = rh / Hkv, h = rh % Hkv;
-    const int j0 = (t % KG) * 16;
-    float x[16], y[16];
-    codes16(kq0, x);
-    codes16(kq1, y);
-    const uint4* ks = reinterpret_cast<const uint4*>(s_ks + h * D + j0);
-    const uint4* kz = reinterpret_cast<const uint4*>(s_kz + h * D + j0);
-    const uint4 sx[2] = {ks[0], ks[1]}, zx[2] = {kz[0], kz[1]};
-    const uint4 sy[2] = {ks[H2 / 8], ks[H2 / 8 + 1]}, zy[2] = {kz[H2 / 8], kz[H2 / 8 + 1]};
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      x[i] = fmaf(x[i], half16(sx, i), half16(zx, i));
-      y[i] = fmaf(y[i], half16(sy, i), half16(zy, i));
-    }
-    if (rotate) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float cs = s_cs[j0 + i], sn = s_sn[j0 + i];
-        const float xr = fmaf(x[i], cs, -y[i] * sn);
-        const float yr = fmaf(y[i], cs, x[i] * sn);
-        x[i] = xr;
-        y[i] = yr;
+    for (int q = 0; q < 2; ++q) {
+      const int it = t + q * kU8Threads;
+      if (it < v_items) {
+        const int rh = it / VG;
+        const int64_t th = (tok0 + rh / Hkv) * Hkv + rh % Hkv;
+        vq[q] = __ldg(reinterpret_cast<const uint4*>(vc + th * D + (it % VG) * 16));
+        vs[q] = __half2float(reinterpret_cast<const __half*>(c.v_scale)[th]);
+        vz[q] = __half2float(reinterpret_cast<const __half*>(c.v_zero)[th]);
       }
     }
-    TO* dst = reinterpret_cast<TO*>(a.Kf) + ((c.dst_row + r0 + r) * Hkv + h) * D + j0;
-    Vec8<TO>::store(dst, *reinterpret_cast<float(*)[8]>(x));
-    Vec8<TO>::store(dst + 8, *reinterpret_cast<float(*)[8]>(x + 8));
-    Vec8<TO>::store(dst + H2, *reinterpret_cast<float(*)[8]>(y));
-    Vec8<TO>::store(dst + H2 + 8, *reinterpret_cast<float(*)[8]>(y + 8));
-  }
-  // 4. values: x = zero + q * scale per token
+    const bool rotate = c.pos != 0;
+    if (chunk != table_chunk) {        // CTA-uniform
+      __syncthreads();                 // the previous chunk's tables are read out
+      for (int i = t * 8; i < Hkv * D; i += kU8Threads * 8) {
+        *reinterpret_cast<uint4*>(s_ks + i) = __ldg(reinterpret_cast<const uint4*>(
+            reinterpret_cast<const __half*>(c.k_scale) + i));
+        *reinterpret_cast<uint4*>(s_kz + i) = __ldg(reinterpret_cast<const uint4*>(
+            reinterpret_cast<const __half*>(c.k_zero) + i));
+      }
+      // 2. the chunk offset's cos/sin of every frequency, while the loads fly
+      if (rotate && t < H2)
+        rope_cos_sin(c.pos, a.freqs.hi[t], a.freqs.mid[t], a.freqs.lo[t], s_cs[t], s_sn[t]);
+      __syncthreads();
+      table_chunk = chunk;
+    }
+
+    // 3. keys: x = zero + q * scale per channel, rotated by R^{pos}
+    if (t < k_items) {
+      const int rh = t / KG;
+      const int r = rh / Hkv, h = rh % Hkv;
+      const int j0 = (t % KG) * 16;
+      float x[16], y[16];
+      codes16(kq0, x);
+      codes16(kq1, y);
+      const uint4* ks = reinterpret_cast<const uint4*>(s_ks + h * D + j0);
+      const uint4* kz = reinterpret_cast<const uint4*>(s_kz + h * D + j0);
+      const uint4 sx[2] = {ks[0], ks[1]}, zx[2] = {kz[0], kz[1]};
+      const uint4 sy[2] = {ks[H2 / 8], ks[H2 / 8 + 1]}, zy[2] = {kz[H2 / 8], kz[H2 / 8 + 1]};
 #pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const int it = t + q * kU8Threads;
-    if (it < v_items) {
-      const int rh = it / VG;
-      float x[16];
-      codes16(vq[q], x);
+      for (int i = 0; i < 16; ++i) {
+        x[i] = fmaf(x[i], half16(sx, i), half16(zx, i));
+        y[i] = fmaf(y[i], half16(sy, i), half16(zy, i));
+      }
+      if (rotate) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) x[i] = fmaf(x[i], vs[q], vz[q]);
-      TO* dst = reinterpret_cast<TO*>(a.Vf) + ((c.dst_row + r0 + rh / Hkv) * Hkv + rh % Hkv) * D +
-                (it % VG) * 16;
+        for (int i = 0; i < 16; ++i) {
+          const float cs = s_cs[j0 + i], sn = s_sn[j0 + i];
+          const float xr = fmaf(x[i], cs, -y[i] * sn);
+          const float yr = fmaf(y[i], cs, x[i] * sn);
+          x[i] = xr;
+          y[i] = yr;
+        }
+      }
+      TO* dst = reinterpret_cast<TO*>(a.Kf) + ((c.dst_row + r0 + r) * Hkv + h) * D + j0;
       Vec8<TO>::store(dst, *reinterpret_cast<float(*)[8]>(x));
       Vec8<TO>::store(dst + 8, *reinterpret_cast<float(*)[8]>(x + 8));
+      Vec8<TO>::store(dst + H2, *reinterpret_cast<float(*)[8]>(y));
+      Vec8<TO>::store(dst + H2 + 8, *reinterpret_cast<float(*)[8]>(y + 8));
+    }
+    // 4. values: x = zero + q * scale per token
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int it = t + q * kU8Threads;
+      if (it < v_items) {
+        const int rh = it / VG;
+        float x[16];
+        codes16(vq[q], x);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = fmaf(x[i], vs[q], vz[q]);
+        TO* dst = reinterpret_cast<TO*>(a.Vf) + ((c.dst_row + r0 + rh / Hkv) * Hkv + rh % Hkv) * D +
+                  (it % VG) * 16;
+        Vec8<TO>::store(dst, *reinterpret_cast<float(*)[8]>(x));
+        Vec8<TO>::store(dst + 8, *reinterpret_cast<float(*)[8]>(x + 8));
+      }
     }
   }
+  // completing implies the previous kernel completed, for the kernels after
   if (!a.wait_first) pdl_wait();
 }
 
@@ -601,8 +607,6 @@ cudaError_t launch_d(const StitchArgs& a, int n_chunks, int D, bool paged, cudaS
 bool stitch_streamed(const fuse_layer_desc_t& desc, const fuse_chunks_t& chunks) {
   const int64_t row_bytes =
       (int64_t)desc.n_kv_heads * desc.head_dim * (desc.dtype == FUSE_F32 ? 4 : 2);
-  if (chunks.kv_storage == FUSE_U8_ASYM)
-    return desc.n_kv_heads * desc.head_dim <= kU8MaxRowElems;   // stitch_u8_kernel
   return chunks.kv_storage == desc.dtype && row_bytes <= kBulkTileBytes;
 }
 
@@ -651,17 +655,18 @@ cudaError_t launch_stitch(const fuse_layer_desc_t& desc, const fuse_chunks_t& ch
   a.freqs = freqs;
   a.wait_first = free_sms < 0;
   if (chunks.kv_storage == FUSE_U8_ASYM && desc.n_kv_heads * D <= kU8MaxRowElems) {
-    // one key item (16 pairs) per thread: rows_per_cta * Hkv * d / 32 = 256
+    // one key item (16 pairs) per thread: rows_per_cta * Hkv * d / 32 = 128
     int rows = std::max(1, kU8Threads * 32 / (desc.n_kv_heads * D));
     if (paged)
       while (a.block_size % rows != 0) --rows;   // a tile never leaves its page
     a.rows_per_cta = rows;
     a.tiles_per_chunk = (max_len + rows - 1) / rows;
-    const int grid = chunks.n_chunks * a.tiles_per_chunk;
-    if (grid == 0) return cudaSuccess;
+    const int n_tiles = chunks.n_chunks * a.tiles_per_chunk;
+    if (n_tiles == 0) return cudaSuccess;
+    const int grid = n_tiles;                  // one CTA per tile
     const bool bf = desc.dtype == FUSE_BF16;
 #define FUSEKV_U8(TO, DD, PG) \
-    return launch_pdl(stitch_u8_kernel<TO, DD, PG>, dim3(grid), dim3(kU8Threads), 0, s, a)
+    return launch_pdl(stitch_u8_kernel<TO, DD, PG>, dim3(grid), dim3(kU8Threads), 0, s, a, n_tiles)
     if (D == 128) {
       if (bf) { if (paged) FUSEKV_U8(__nv_bfloat16, 128, true); FUSEKV_U8(__nv_bfloat16, 128, false); }
       if (paged) FUSEKV_U8(float, 128, true);

@@ -14,9 +14,9 @@ namespace fusekv {
 
 namespace {
 
-constexpr int kTopkThreads = 512;    // 128 registers per thread: no spills in the radix rounds
+constexpr int kTopkThreads = 1024;
 constexpr int kTopkSmemKeys = 40 * 1024;   // keys kept in shared memory (160 KB)
-constexpr int kTopkBatch = 8;              // tokens per thread whose loads are in flight together
+constexpr int kTopkBatch = 4;              // tokens per thread whose loads are in flight together
 
 __device__ __forceinline__ uint32_t float_key(float f, bool* is_nan) {
   uint32_t b = __float_as_uint(f);
@@ -24,41 +24,6 @@ __device__ __forceinline__ uint32_t float_key(float f, bool* is_nan) {
   if (*is_nan) return 0u;
   if (b == 0x80000000u) b = 0u;                       // -0 -> +0
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-
-// Exclusive block-wide scan of a pair of values per thread (one pass of
-// barriers for both); the buffer is not reused after it.
-__device__ __forceinline__ uint2 block_exclusive_scan2(uint32_t a, uint32_t b, uint2* wbuf) {
-  const int lane = threadIdx.x % 32;
-  const int warp = threadIdx.x / 32;
-  uint32_t xa = a, xb = b;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t ya = __shfl_up_sync(0xffffffffu, xa, o);
-    const uint32_t yb = __shfl_up_sync(0xffffffffu, xb, o);
-    if (lane >= o) {
-      xa += ya;
-      xb += yb;
-    }
-  }
-  if (lane == 31) wbuf[warp] = make_uint2(xa, xb);
-  __syncthreads();
-  if (warp == 0) {
-    uint2 w = lane < (int)(blockDim.x / 32) ? wbuf[lane] : make_uint2(0u, 0u);
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t ya = __shfl_up_sync(0xffffffffu, w.x, o);
-      const uint32_t yb = __shfl_up_sync(0xffffffffu, w.y, o);
-      if (lane >= o) {
-        w.x += ya;
-        w.y += yb;
-      }
-    }
-    wbuf[lane] = w;   // inclusive prefix over warps
-  }
-  __syncthreads();
-  const uint2 pw = warp > 0 ? wbuf[warp - 1] : make_uint2(0u, 0u);
-  return make_uint2(pw.x + xa - a, pw.y + xb - b);
 }
 
 // With partial != null the scores are first formed from the cosine partials
@@ -76,6 +41,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const fuse_request_t
   __shared__ uint32_t warp_buf[32];
   __shared__ uint32_t sel_digit, sel_remaining;
   __shared__ uint2 pair_buf[32];
+  __shared__ uint2 sel_scan[32];
   const int r = blockIdx.x;
   const fuse_request_t R = reqs[r];     // the caller's table: no kernel writes it
   pdl_trigger();
@@ -173,9 +139,18 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const fuse_request_t
     const uint32_t dmask = (1u << w) - 1u;
     for (int b = t; b < 256; b += kTopkThreads) hist[b] = 0u;
     __syncthreads();
-    for (int i = t; i < n; i += kTopkThreads) {
-      const uint32_t key = keys[i];
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & dmask], 1u);
+    // Scores crowd into few bins, and same-address shared-memory atomics of a
+    // warp serialise: the lanes whose key falls in lane 0's bin add their
+    // count with one atomic, the others one each.
+    for (int base = t - (t & 31); base < n; base += kTopkThreads) {   // warp-uniform
+      const int i = base + (t & 31);
+      const uint32_t key = i < n ? keys[i] : 0u;
+      const bool act = i < n && (key & mask) == prefix;
+      const uint32_t bin = act ? (key >> shift) & dmask : 0xFFFFFFFFu;
+      const uint32_t lead = __shfl_sync(0xffffffffu, bin, 0);
+      const uint32_t same = __ballot_sync(0xffffffffu, act && bin == lead);
+      if ((t & 31) == 0 && same) atomicAdd(&hist[lead], (uint32_t)__popc(same));
+      if (act && bin != lead) atomicAdd(&hist[bin], 1u);
     }
     __syncthreads();
     if (t < 32) {
@@ -217,31 +192,60 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const fuse_request_t
   const uint32_t tau = prefix;
   const uint32_t need_eq = remaining;
 
-  // compaction in index order: thread t owns indices [i0, i1)
-  const int per = (n + kTopkThreads - 1) / kTopkThreads;
-  const int i0 = min(n, t * per);
-  const int i1 = min(n, i0 + per);
-  uint32_t n_gt = 0, n_eq = 0;
-  for (int i = i0; i < i1; ++i) {
-    const uint32_t key = keys[i] & mask;
-    n_gt += key > tau;
-    n_eq += key == tau;
+  // compaction in index order: warp w owns the contiguous range [w0, w1),
+  // walked 32 keys at a time (lane l takes key base + l: consecutive lanes
+  // read consecutive words, no bank conflicts); ballots give each lane's
+  // rank within a step
+  const int lane = t & 31, warp = t >> 5;
+  constexpr int kWarps = kTopkThreads / 32;
+  const int per_w = (((n + kWarps - 1) / kWarps) + 31) & ~31;
+  const int w0 = min(n, warp * per_w);
+  const int w1 = min(n, w0 + per_w);
+  uint32_t n_gt = 0, n_eq = 0;                     // warp-uniform
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const uint32_t key = i < w1 ? keys[i] & mask : 0u;
+    n_gt += __popc(__ballot_sync(0xffffffffu, i < w1 && key > tau));
+    n_eq += __popc(__ballot_sync(0xffffffffu, i < w1 && key == tau));
   }
-  // outputs before this thread's range: every key above tau there, and of
-  // the keys equal to it the first need_eq in index order
-  const uint2 before = block_exclusive_scan2(n_gt, n_eq, pair_buf);
-  const uint32_t eq_before = before.y;
-  const uint32_t take_eq = eq_before >= need_eq ? 0u : min(n_eq, need_eq - eq_before);
-  const uint32_t out_before = before.x + min(eq_before, need_eq);
-  int32_t* out = idx + R.sel0;
-  uint32_t o = out_before, eq_taken = 0;
-  for (int i = i0; i < i1; ++i) {
-    const uint32_t key = keys[i] & mask;
-    if (key > tau || (key == tau && eq_taken < take_eq)) {
-      eq_taken += key == tau;
-      if (o < (uint32_t)k) out[o] = i;
-      ++o;
+  // outputs before this warp's range: every key above tau there, and of the
+  // keys equal to it the first need_eq in index order (one scan over warps)
+  if (lane == 0) pair_buf[warp] = make_uint2(n_gt, n_eq);
+  __syncthreads();
+  if (warp == 0) {
+    uint2 v = lane < kWarps ? pair_buf[lane] : make_uint2(0u, 0u);
+    uint32_t ga = v.x, ea = v.y;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t yg = __shfl_up_sync(0xffffffffu, ga, o);
+      const uint32_t ye = __shfl_up_sync(0xffffffffu, ea, o);
+      if (lane >= o) {
+        ga += yg;
+        ea += ye;
+      }
     }
+    if (lane < kWarps) sel_scan[lane] = make_uint2(ga - v.x, ea - v.y);   // exclusive
+  }
+  __syncthreads();
+  const uint32_t gt_before = sel_scan[warp].x, eq_before = sel_scan[warp].y;
+  uint32_t out_pos = gt_before + min(eq_before, need_eq);   // warp-uniform
+  uint32_t eq_seen = eq_before;                              // warp-uniform
+  int32_t* out = idx + R.sel0;
+  const uint32_t below = (1u << lane) - 1u;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const uint32_t key = i < w1 ? keys[i] & mask : 0u;
+    const bool gt = i < w1 && key > tau;
+    const bool eq = i < w1 && key == tau;
+    const uint32_t be = __ballot_sync(0xffffffffu, eq);
+    const bool take = gt || (eq && eq_seen + __popc(be & below) < need_eq);
+    const uint32_t bt = __ballot_sync(0xffffffffu, take);
+    if (take) {
+      const uint32_t o = out_pos + __popc(bt & below);
+      if (o < (uint32_t)k) out[o] = i;
+    }
+    out_pos += __popc(bt);
+    eq_seen += __popc(be);
   }
 }
 

@@ -33,6 +33,10 @@ SMALL = {
     # some rows lie wholly before the first key of a piece
     "sparse_long_bf16": synth.scaled(C["qwen3_8b_layer"], chunks_per_request=16, ratio=0.01,
                                      seed=21),
+    # hidden 9216: the row gather copies a row in more than one round of
+    # 16-byte loads per thread
+    "wide_hidden_bf16": synth.scaled(C["qwen3_8b_layer"], hidden=9216, chunks_per_request=3,
+                                     chunk_len=96, query_len=8, ratio=0.2, seed=23),
     # ragged: odd chunk lengths, 1-token chunks, a short query, fp32
     "ragged_fp32": synth.scaled(C["tiny_fp32"], chunks_per_request=None, chunk_len=None,
                                 query_len=None, chunk_count_range=(1, 6),
@@ -277,7 +281,8 @@ def test_recompute_selected(name):
 # difference in a stitched key (fp32 versus fp64 dequantise-and-rotate) moves
 # them by more than 2e-2: the allowance covers exactly those flips.
 @pytest.mark.parametrize("name", ["tiny_fp32", "qwen3_8b_layer", "paged3", "ragged_fp32",
-                                  "ragged_paged_bf16_d64", "sparse_long_bf16", "int8_4x1024"])
+                                  "ragged_paged_bf16_d64", "sparse_long_bf16", "int8_4x1024",
+                                  "wide_hidden_bf16"])
 def test_layer_step(name):
     case = case_of(name)
     b = buffers(case)
