@@ -53,6 +53,7 @@ constexpr int kD = 128;
 constexpr int kKB = 128;                      // keys per block
 constexpr int kHalf = 128 * 64 * 2;           // one 64-column half of a 128-row tile (16 KB)
 constexpr int kTile = 2 * kHalf;              // 32 KB
+constexpr int kQBufs = 2;                     // Q tiles in flight (next unit's while this one runs)
 constexpr int kKStages = 3;
 constexpr int kVStages = 2;
 constexpr int kWarpQK = 0, kWarpS = 1, kWarpV = 2, kWarpPV = 3, kWarpSoft = 4, kWarpOut = 12;
@@ -97,7 +98,7 @@ struct Ctl {
   volatile int abort_flag;
   float xl[128];          // [row] softmax row sum of the unit being written
 };
-constexpr int kSmemBytes = (2 + kKStages + kVStages) * kTile + 1024 + (int)sizeof(Ctl);
+constexpr int kSmemBytes = (kQBufs + kKStages + kVStages) * kTile + 1024 + (int)sizeof(Ctl);
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ctl* ctl) {
@@ -188,9 +189,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;                               // Q buffer q at sQ + q * kTile
-  uint8_t* sK = smem + 2 * kTile;                   // K stage s at sK + s * kTile
+  uint8_t* sK = smem + kQBufs * kTile;              // K stage s at sK + s * kTile
   uint8_t* sV = sK + kKStages * kTile;              // V stage s at sV + s * kTile
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + (2 + kKStages + kVStages) * kTile);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + (kQBufs + kKStages + kVStages) * kTile);
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   pdl_trigger();
@@ -260,8 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int4 cur = T;
         if (unit_at(i + 1) < n_units) T = tile_of(a, unit_at(i + 1));   // next unit's record
         const int kvh = u % a.Hkv;
-        const int qb = i & 1;
-        if (!wait_or_abort(&ctl->q_empty[qb], ((i >> 1) & 1) ^ 1, ctl)) {
+        const int qb = i % kQBufs;
+        if (!wait_or_abort(&ctl->q_empty[qb], ((i / kQBufs) & 1) ^ 1, ctl)) {
           abort_kernel(ctl, a.err, W_Q_EMPTY, 0);
           break;
         }
@@ -284,7 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // let copies in flight land before the CTA may exit
-      for (int k = (i > 2 ? i - 2 : 0); k < i; ++k) tc::mbar_wait(&ctl->q_full[k & 1], (k >> 1) & 1);
+      for (int k = (i > kQBufs ? i - kQBufs : 0); k < i; ++k)
+        tc::mbar_wait(&ctl->q_full[k % kQBufs], (k / kQBufs) & 1);
       for (uint32_t c = (kc > (uint32_t)kKStages ? kc - kKStages : 0); c < kc; ++c)
         tc::mbar_wait(&ctl->k_full[c % kKStages], (c / kKStages) & 1);
     }
@@ -326,8 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; unit_at(i) < n_units && ok; ++i) {
         const int nkb = T.w;
         if (unit_at(i + 1) < n_units) T = tile_of(a, unit_at(i + 1));
-        const int qb = i & 1;
-        if (!wait_or_abort(&ctl->q_full[qb], (i >> 1) & 1, ctl)) {
+        const int qb = i % kQBufs;
+        if (!wait_or_abort(&ctl->q_full[qb], (i / kQBufs) & 1, ctl)) {
           abort_kernel(ctl, a.err, W_Q_FULL, 0);
           break;
         }
