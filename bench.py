@@ -78,6 +78,9 @@ _PROFILED = {
     ("deviation_gemm_tc", "qwen3_8b_layer"): "gemm_tc_kernel_qwen3_8b_layer.md",
     ("attention_tc", "llama3_70b_int8_long"): "attn_tc_kernel_llama3_70b_int8_long.md",
     ("stitch_rerotate", "llama3_70b_int8_long"): "stitch_kernel_llama3_70b_int8_long.md",
+    ("qkv_gemm_tc", "llama3_70b_int8_long"): "gemm_tc_kernel_llama3_70b_int8_long.md",
+    ("deviation_gemm_tc", "llama3_70b_int8_long"): "gemm_tc_kernel_llama3_70b_int8_long.md",
+    ("stitch_rerotate", "qwen3_8b_layer"): "stitch_topk_prepare_qwen3_8b_layer.md",
 }
 
 
@@ -532,10 +535,13 @@ def trace_kernels(fk, fn, steps):
     return per, n / max(1, steps)
 
 
-def kernel_table(per, work, hbm_gbs, bf16_tf):
+def kernel_table(per, work, hbm_gbs, bf16_tf, wl=None):
     kernels = {}
     for n, (c, tot) in per.items():
         kernels[n] = {"launches": c, "avg_us": 1e3 * tot / c}
+        t = _traffic(n, wl) if wl else None
+        if t is not None:
+            kernels[n]["traffic"] = t
         if n in work:
             bound, amount = work[n]
             avg_s = tot / c / 1e3
@@ -588,7 +594,7 @@ def run_workload(fk, name, args, ws, stream, peaks, keep=False):
     res = {"value": job_rate(ws, T, args.steps, ms), "unit": UNIT,
            "ms_per_step": ms / args.steps, "regions_ms": regions,
            "config": config_json(cfg, layouts, ws), "counts": counts,
-           "kernels": kernel_table(per, work, hbm_gbs, bf16_tf),
+           "kernels": kernel_table(per, work, hbm_gbs, bf16_tf, name),
            "roofline": roofline(per, work, name, hbm_gbs, bf16_tf, peak_src),
            "launches_per_step": per_step}
     if cfg.n_layers > 1:
@@ -875,7 +881,7 @@ def native_run(args, ws, rank, local):
     hbm_gbs, bf16_tf, _, peak_src = peaks
     per, per_step = trace_kernels(fk, fn, args.steps)
     work, counts = work_per_launch(cfg, sets[cfg.score_layer] if cfg.n_layers > 1 else sets[0])
-    kernels = kernel_table(per, work, hbm_gbs, bf16_tf)
+    kernels = kernel_table(per, work, hbm_gbs, bf16_tf, args.workload)
     roof = roofline(per, work, args.workload, hbm_gbs, bf16_tf, peak_src)
     T = sum(l.n_tok for l in layouts) * cfg.n_layers
 
