@@ -194,7 +194,10 @@ def config_json(cfg, layouts, ws):
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples (every 50 ms) of the SM clock, the power draw and
+    the throttle reasons; stop() keeps the samples taken inside the timed
+    window when it is given one."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -209,7 +212,7 @@ class ClockSampler:
         except Exception:
             sel = []
         self.cmd = ["nvidia-smi"] + sel + ["--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                                           "-lms", "100"]
+                                           "-lms", "50"]
 
     def start(self):
         try:
@@ -218,7 +221,15 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
-    def stop(self):
+    @staticmethod
+    def _when(stamp):
+        import datetime
+        try:
+            return datetime.datetime.strptime(stamp, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
+    def stop(self, window=None):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         self.proc.terminate()
@@ -227,28 +238,35 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.f.close()
-        sm, smax, reasons = [], [], set()
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 8:
+                if len(parts) < 9:
                     continue
                 try:
-                    sm.append(float(parts[0]))
-                    smax.append(float(parts[1]))
+                    rows.append((self._when(parts[0]), float(parts[1]), float(parts[2]),
+                                 float(parts[3]), parts[5:9]))
                 except ValueError:
                     continue
-                for n, v in zip(names, parts[4:8]):
-                    if v.lower().startswith("active"):
-                        reasons.add(n)
         try:
             os.remove(self.path)
         except OSError:
             pass
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        inside = [r for r in rows if window and r[0] is not None and window[0] <= r[0] <= window[1]]
+        use = inside or rows
+        reasons = set()
+        for r in use:
+            for n, v in zip(names, r[4]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[1] for r in use) if use else None,
+                "sm_min_mhz": min(r[1] for r in use) if use else None,
+                "sm_max_mhz": max(r[2] for r in use) if use else None,
+                "power_w": statistics.median(r[3] for r in use) if use else None,
+                "reasons": sorted(reasons), "samples": len(use),
+                "window": "timed regions" if inside else "whole sampling period"}
 
 
 # ---------------------------------------------------------------------------
@@ -865,13 +883,16 @@ def native_run(args, ws, rank, local):
     # throughout, median region reported
     sampler = ClockSampler(local)
     sampler.start()
-    time.sleep(0.3)
+    time.sleep(0.5)
     if ws > 1:
         dist.barrier()
+    t_win = time.time()
     regions = time_regions(fn, args.steps, args.regions, stream)
     if ws > 1:
         dist.barrier()
-    clocks = sampler.stop()
+    t_win = (t_win, time.time())
+    time.sleep(0.1)
+    clocks = sampler.stop(t_win)
     ms = max_over_ranks(statistics.median(regions), ws, "cuda")
     for b in sets:
         fk.check_errors(b.ws)
@@ -974,7 +995,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--regions", type=int, default=5, help="timed regions of K steps (median)")
+    ap.add_argument("--regions", type=int, default=10, help="timed regions of K steps (median)")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--profile", action="store_true",
