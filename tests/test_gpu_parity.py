@@ -63,6 +63,22 @@ STORAGE = {
     # two requests of the batched paged workload with 4-bit codes in the
     # block pool (d / 2 bytes per token and head, partial tail blocks)
     "int4_paged2": synth.scaled(C["llama3_8b_paged_batch16"], n_requests=2, kv_storage="u4"),
+    # int8 codes in the block pool (16-token blocks, partial tail blocks): the
+    # ring-buffered int8 stitch, paged
+    "int8_paged2": synth.scaled(C["llama3_8b_paged_batch16"], n_requests=2, kv_storage="u8",
+                                seed=9),
+    # int8, d = 64, ragged chunks of 1..70 tokens: the ring stitch's partial
+    # tiles and chunk changes inside a CTA's range of tiles
+    "int8_ragged_d64": synth.scaled(C["llama3_70b_int8_long"], hidden=1024, n_q_heads=16,
+                                    head_dim=64, w_std=1.0 / 32.0, chunks_per_request=None,
+                                    chunk_len=None, query_len=None, chunk_count_range=(2, 6),
+                                    chunk_len_range=(1, 70), query_len_range=(1, 9),
+                                    n_requests=3, ratio=0.3, seed=13),
+    # int8 with 4 KV heads: the per-thread int8 stitch (the ring one needs a
+    # multiple of 8 heads)
+    "int8_hkv4": synth.scaled(C["llama3_70b_int8_long"], hidden=1024, n_q_heads=8, n_kv_heads=4,
+                              w_std=1.0 / 32.0, chunks_per_request=3, chunk_len=100, query_len=8,
+                              seed=14),
 }
 
 _CASES = {}
