@@ -615,31 +615,49 @@ def run_workload(fk, name, args, ws, stream, peaks, keep=False):
            "kernels": kernel_table(per, work, hbm_gbs, bf16_tf, name),
            "roofline": roofline(per, work, name, hbm_gbs, bf16_tf, peak_src),
            "launches_per_step": per_step}
-    if cfg.n_layers > 1:
-        # the same stack captured once as a CUDA graph and replayed
-        try:
-            # captured on a stream of its own (the legacy stream cannot be
-            # captured), replayed on the timing stream
-            g = fk.StackGraph(b0.desc, b0.reqs, sets, cfg.score_layer, b0.idx, b0.score, b0.ws,
-                              stream=torch.cuda.Stream())
-            for i in range(args.warmup):
-                g.launch(stream)
-            gms = statistics.median(time_regions(lambda i: g.launch(stream), args.steps,
-                                                 args.regions, stream))
-            fk.check_errors(b0.ws)
-            g.close()
-            res["graph"] = {"value": job_rate(ws, T, args.steps, gms), "unit": UNIT,
-                            "ms_per_step": gms / args.steps,
-                            "what": "fuse_stack_step captured once (fuse_stack_graph_create), "
-                                    "replayed per step"}
-        except Exception as ex:                # reported, not fatal
-            res["graph"] = {"error": f"{type(ex).__name__}: {ex}"}
+    res["graph"] = graph_timing(fk, cfg, sets, args, stream, T, ws)
     if not keep:
         del sets, fn
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
         return res, None
     return res, sets
+
+
+def graph_timing(fk, cfg, sets, args, stream, T, ws):
+    """The same steps replayed from CUDA graphs: the stack captured once
+    (fuse_stack_graph_create), or for a single layer one graph per input set
+    (a one-layer stack that scores its layer is the layer-step), replayed in
+    the same alternation.  Reported, not fatal."""
+    graphs = []
+    try:
+        if cfg.n_layers > 1:
+            b0 = sets[cfg.score_layer]
+            graphs = [fk.StackGraph(b0.desc, b0.reqs, sets, cfg.score_layer, b0.idx, b0.score,
+                                    b0.ws, stream=torch.cuda.Stream())]
+            what = "fuse_stack_step captured once (fuse_stack_graph_create), replayed per step"
+        else:
+            # captured on a stream of its own (the legacy stream cannot be
+            # captured), replayed on the timing stream
+            cap = torch.cuda.Stream()
+            graphs = [fk.StackGraph(b.desc, b.reqs, [b], 0, b.idx, b.score, b.ws, stream=cap)
+                      for b in sets]
+            what = ("fuse_layer_step of each input set captured once as a one-layer "
+                    "fuse_stack_graph_create, replayed alternately")
+        n = len(graphs)
+        for i in range(args.warmup):
+            graphs[i % n].launch(stream)
+        gms = statistics.median(time_regions(lambda i: graphs[i % n].launch(stream), args.steps,
+                                             args.regions, stream))
+        for b in sets:
+            fk.check_errors(b.ws)
+        return {"value": job_rate(ws, T, args.steps, gms), "unit": UNIT,
+                "ms_per_step": gms / args.steps, "what": what}
+    except Exception as ex:
+        return {"error": f"{type(ex).__name__}: {ex}"}
+    finally:
+        for g in graphs:
+            g.close()
 
 
 def e2e_run(fk, bufs, args, ws, stream, T):
@@ -906,6 +924,7 @@ def native_run(args, ws, rank, local):
     roof = roofline(per, work, args.workload, hbm_gbs, bf16_tf, peak_src)
     T = sum(l.n_tok for l in layouts) * cfg.n_layers
 
+    graph = None if args.profile else graph_timing(fk, cfg, sets, args, stream, T, ws)
     e2e = None
     if args.e2e_steps > 0 and not args.profile and cfg.n_layers == 1:
         e2e = e2e_run(fk, sets[:2], args, ws, stream, T)
@@ -960,7 +979,7 @@ def native_run(args, ws, rank, local):
         "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": int(round(per_step * args.steps * args.regions)),
         "launches_per_step": per_step, "timed_regions": args.regions, "regions_ms": regions,
-        "counts": counts, "clocks": clocks, "impl": "native",
+        "counts": counts, "clocks": clocks, "graph": graph, "impl": "native",
     }
     if extra:
         out["workloads"] = extra
