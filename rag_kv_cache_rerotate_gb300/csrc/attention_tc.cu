@@ -35,7 +35,20 @@
 // blocks) one unit ahead.  The kernel is persistent; units are taken heaviest
 // first, snake-ordered over the CTAs (round r visits the CTAs upwards when r
 // is even and downwards when r is odd).
+// Tiles go in pairs: a cluster of two CTAs takes two neighbouring tiles (by
+// key-block count) of one KV head, and when both belong to one request every
+// K and V block is fetched from L2 once for both: each CTA loads one
+// 64-column half with TMA multicast into both CTAs' rings, and a stage is
+// refilled once both CTAs' MMAs have released it (their commits arrive on
+// both CTAs' barriers).  On long contexts this halves the ~16 GB of K and V
+// a layer-step moves from L2 to the SMs; the time at a fixed clock is the
+// same, but the energy saved lets the SMs hold a higher clock under the
+// board's power cap, where long steps run.
 #include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <map>
+#include <mutex>
 
 #include "common.cuh"
 #include "launch.h"
@@ -54,6 +67,7 @@ constexpr int kKB = 128;                      // keys per block
 constexpr int kHalf = 128 * 64 * 2;           // one 64-column half of a 128-row tile (16 KB)
 constexpr int kTile = 2 * kHalf;              // 32 KB
 constexpr int kQBufs = 2;                     // Q tiles in flight (next unit's while this one runs)
+constexpr int64_t kPairMinTokens = 16384;     // longest request from which tiles go in pairs
 constexpr int kKStages = 3;
 constexpr int kVStages = 2;
 constexpr int kWarpQK = 0, kWarpS = 1, kWarpV = 2, kWarpPV = 3, kWarpSoft = 4, kWarpOut = 12;
@@ -89,7 +103,7 @@ struct AttnArgs {
 };
 
 struct Ctl {
-  uint64_t q_full[2], q_empty[2];
+  uint64_t q_full[kQBufs], q_empty[kQBufs];
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
   uint64_t s_full[kSBufs], p_full[kSBufs], pv_done[kSBufs];   // [block % 3]
@@ -125,16 +139,47 @@ __device__ __forceinline__ void abort_kernel(Ctl* ctl, uint32_t* err, uint32_t w
                  (which << 20) | ((blockIdx.x & 0xFFu) << 12) | ((uint32_t)j & 0xFFFu));
 }
 
-// The i-th unit of this CTA: round i visits CTAs upwards when i is even and
-// downwards when i is odd.  Units past the end stay past it in later rounds.
+// The unit that a CTA (a cluster of two CTAs when PAIR) takes in its i-th
+// round: round i visits them upwards when i is even and downwards when i is
+// odd.  Units past the end stay past it in later rounds.
+template <bool PAIR>
 __device__ __forceinline__ int unit_at(int i) {
-  const int G = gridDim.x;
-  return i * G + ((i & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x);
+  const int G = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
+  const int c = PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x;
+  return i * G + ((i & 1) ? G - 1 - c : c);
 }
 
-// Tile record of unit u (heaviest tiles, the last ones, first).
-__device__ __forceinline__ int4 tile_of(const AttnArgs& a, int u) {
-  return a.tiles[a.n_tiles - 1 - u / a.Hkv];
+// What one CTA does for a unit.
+struct Unit {
+  int4 t;       // its tile record; rows 0 and key blocks 0 when it has no tile
+  int kvh;
+  int nkb;      // key blocks its K and V rings step through
+  int shared;   // PAIR: both tiles start at the same fused row, and each CTA
+                // loads one 64-column half of every K and V block for both
+};
+
+// Unit u.  Single CTAs: the tile u / Hkv places from the heaviest end of the
+// list.  Pairs: the tiles 2p and 2p + 1 places from the heaviest end
+// (p = u / Hkv), the first for cluster rank 0 and the second for rank 1;
+// both CTAs' rings step through the larger key-block count of the two, so
+// that they stay in step (a CTA past its own blocks only passes stages on).
+template <bool PAIR>
+__device__ __forceinline__ Unit unit_rec(const AttnArgs& a, int u, uint32_t rank) {
+  Unit r;
+  r.kvh = u % a.Hkv;
+  if (!PAIR) {
+    r.t = a.tiles[a.n_tiles - 1 - u / a.Hkv];
+    r.nkb = r.t.w;
+    r.shared = 0;
+    return r;
+  }
+  const int i0 = a.n_tiles - 1 - 2 * (u / a.Hkv);
+  const int4 t0 = a.tiles[i0];
+  const int4 t1 = i0 > 0 ? a.tiles[i0 - 1] : make_int4(t0.x, t0.y, 0, 0);
+  r.t = rank ? t1 : t0;
+  r.nkb = max(t0.w, t1.w);
+  r.shared = t0.y == t1.y;
+  return r;
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -177,12 +222,40 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return d;
 }
 
+// 3-D tiled load delivered to the same shared-memory offset in every CTA of
+// `mask` (bit r: cluster rank r); each destination CTA counts the bytes on the
+// mbarrier at `bar`'s offset in its own shared memory.
+__device__ __forceinline__ void tma_load_3d_multicast(void* dst, const CUtensorMap* map,
+                                                      uint64_t* bar, int x, int y, int z,
+                                                      uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(tc::smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(tc::smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+
+// Arrive on the mbarrier at this offset in every CTA of `mask` once every
+// tcgen05.mma issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(tc::smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+
 // descriptor of K-step kk (16 columns) of a 128-row K-major tile stored as two
 // 64-column halves
 __device__ __forceinline__ uint64_t kmajor_step(uint32_t tile, int kk) {
   return tc::smem_desc_k128(tile + (kk >> 2) * kHalf + (kk & 3) * 32);
 }
 
+// PAIR: clusters of two CTAs, each on its own tile of one KV head; when both
+// tiles read the same fused rows, every K and V block is read from L2 once
+// for the pair (each CTA loads one half with TMA multicast into both), and a
+// ring stage is refilled once both CTAs' MMAs are done with it.
+template <bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                    const __grid_constant__ CUtensorMap mapV, const AttnArgs a) {
@@ -194,20 +267,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + (kQBufs + kKStages + kVStages) * kTile);
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
+  const uint32_t rank = PAIR ? tc::cluster_rank() : 0u;
+  constexpr uint16_t kBoth = 0x3;                   // both CTAs of the cluster
+  constexpr uint32_t kUsers = PAIR ? 2 : 1;         // MMA warps that release a K / V stage
   pdl_trigger();
 
   if (threadIdx.x == 0) {
-    for (int q = 0; q < 2; ++q) {
+    for (int q = 0; q < kQBufs; ++q) {
       tc::mbar_init(&ctl->q_full[q], 1);
       tc::mbar_init(&ctl->q_empty[q], 1);
     }
     for (int s = 0; s < kKStages; ++s) {
       tc::mbar_init(&ctl->k_full[s], 1);
-      tc::mbar_init(&ctl->k_empty[s], 1);
+      tc::mbar_init(&ctl->k_empty[s], kUsers);
     }
     for (int s = 0; s < kVStages; ++s) {
       tc::mbar_init(&ctl->v_full[s], 1);
-      tc::mbar_init(&ctl->v_empty[s], 1);
+      tc::mbar_init(&ctl->v_empty[s], kUsers);
     }
     for (int s = 0; s < kSBufs; ++s) {
       tc::mbar_init(&ctl->s_full[s], 1);
@@ -225,24 +301,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == kWarpS) tc::tmem_alloc(&ctl->tmem_base, kTmemCols);
   tc::tc_fence_before();
-  __syncthreads();
+  if (PAIR) {
+    __syncwarp();
+    tc::cluster_sync_all();   // both CTAs' barriers exist before any copy or arrival crosses
+  } else {
+    __syncthreads();
+  }
   tc::tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   const int n_units = a.n_units;
-  // The first unit's tile record, and for the softmax threads the positions of
+  // The first unit's records, and for the softmax threads the positions of
   // their rows.  When the records come from a kernel that finished before the
   // previous one could release its dependents, they are read before waiting.
-  const bool have0 = unit_at(0) < n_units;
-  int4 T0 = make_int4(0, 0, 1, 0);
+  const bool have0 = unit_at<PAIR>(0) < n_units;
+  Unit U0;
+  U0.t = make_int4(0, 0, 0, 0);
+  U0.kvh = U0.nkb = U0.shared = 0;
   int pos0[3] = {0, 0, 0};                          // softmax: rows R0, R1, the tile's first
   auto first_records = [&]() {
     if (!have0) return;
-    T0 = tile_of(a, unit_at(0));
-    if (warp >= kWarpSoft && warp < kWarpOut) {
+    U0 = unit_rec<PAIR>(a, unit_at<PAIR>(0), rank);
+    if (warp >= kWarpSoft && warp < kWarpOut && U0.t.z > 0) {
       const int R0 = (warp & 3) * 32 + ((warp - kWarpSoft) >> 2) * 16 + (lane >> 2);
-      pos0[0] = a.rows[T0.x + min(R0 / a.g, T0.z - 1)].pos;
-      pos0[1] = a.rows[T0.x + min((R0 + 8) / a.g, T0.z - 1)].pos;
-      pos0[2] = a.rows[T0.x].pos;
+      pos0[0] = a.rows[U0.t.x + min(R0 / a.g, U0.t.z - 1)].pos;
+      pos0[1] = a.rows[U0.t.x + min((R0 + 8) / a.g, U0.t.z - 1)].pos;
+      pos0[2] = a.rows[U0.t.x].pos;
     }
   };
   if (a.records_ready) first_records();
@@ -255,22 +338,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t kc = 0;
       int i = 0;
       bool ok = true;
-      int4 T = T0;
-      for (; unit_at(i) < n_units && ok; ++i) {
-        const int u = unit_at(i);
-        const int4 cur = T;
-        if (unit_at(i + 1) < n_units) T = tile_of(a, unit_at(i + 1));   // next unit's record
-        const int kvh = u % a.Hkv;
+      Unit U = U0;
+      for (; unit_at<PAIR>(i) < n_units && ok; ++i) {
+        const Unit cur = U;
+        if (unit_at<PAIR>(i + 1) < n_units) U = unit_rec<PAIR>(a, unit_at<PAIR>(i + 1), rank);
         const int qb = i % kQBufs;
         if (!wait_or_abort(&ctl->q_empty[qb], ((i / kQBufs) & 1) ^ 1, ctl)) {
           abort_kernel(ctl, a.err, W_Q_EMPTY, 0);
           break;
         }
         uint8_t* q = sQ + qb * kTile;
-        tc::mbar_arrive_expect_tx(&ctl->q_full[qb], kTile);
-        tc::tma_load_3d(q, &mapQ, &ctl->q_full[qb], 0, kvh * a.g, cur.x);
-        tc::tma_load_3d(q + kHalf, &mapQ, &ctl->q_full[qb], 64, kvh * a.g, cur.x);
-        for (int j = 0; j < cur.w; ++j, ++kc) {
+        if (cur.t.z > 0) {
+          tc::mbar_arrive_expect_tx(&ctl->q_full[qb], kTile);
+          tc::tma_load_3d(q, &mapQ, &ctl->q_full[qb], 0, cur.kvh * a.g, cur.t.x);
+          tc::tma_load_3d(q + kHalf, &mapQ, &ctl->q_full[qb], 64, cur.kvh * a.g, cur.t.x);
+        } else {
+          tc::mbar_arrive(&ctl->q_full[qb]);
+        }
+        for (int j = 0; j < cur.nkb; ++j, ++kc) {
           const int st = kc % kKStages;
           if (!wait_or_abort(&ctl->k_empty[st], ((kc / kKStages) & 1) ^ 1, ctl)) {
             abort_kernel(ctl, a.err, W_K_EMPTY, j);
@@ -278,30 +363,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           uint8_t* k = sK + st * kTile;
-          const int z = cur.y + j * kKB;
-          tc::mbar_arrive_expect_tx(&ctl->k_full[st], kTile);
-          tc::tma_load_3d(k, &mapK, &ctl->k_full[st], 0, kvh, z);
-          tc::tma_load_3d(k + kHalf, &mapK, &ctl->k_full[st], 64, kvh, z);
+          const int z = cur.t.y + j * kKB;
+          // the stage counts kTile bytes: both halves from this CTA, or one
+          // from each CTA of the pair (the other's may land first)
+          if (PAIR && cur.shared) {
+            tc::mbar_arrive_expect_tx(&ctl->k_full[st], kTile);
+            tma_load_3d_multicast(k + rank * kHalf, &mapK, &ctl->k_full[st], 64 * (int)rank,
+                                      cur.kvh, z, kBoth);
+          } else if (j < cur.t.w) {
+            tc::mbar_arrive_expect_tx(&ctl->k_full[st], kTile);
+            tc::tma_load_3d(k, &mapK, &ctl->k_full[st], 0, cur.kvh, z);
+            tc::tma_load_3d(k + kHalf, &mapK, &ctl->k_full[st], 64, cur.kvh, z);
+          } else {
+            tc::mbar_arrive(&ctl->k_full[st]);
+          }
         }
       }
-      // let copies in flight land before the CTA may exit
+      // let copies in flight land (and, in a pair, the other CTA's releases
+      // of the last stages arrive) before the CTA may exit
       for (int k = (i > kQBufs ? i - kQBufs : 0); k < i; ++k)
         tc::mbar_wait(&ctl->q_full[k % kQBufs], (k / kQBufs) & 1);
-      for (uint32_t c = (kc > (uint32_t)kKStages ? kc - kKStages : 0); c < kc; ++c)
+      for (uint32_t c = (kc > (uint32_t)kKStages ? kc - kKStages : 0); c < kc; ++c) {
         tc::mbar_wait(&ctl->k_full[c % kKStages], (c / kKStages) & 1);
+        if (PAIR) tc::mbar_wait(&ctl->k_empty[c % kKStages], (c / kKStages) & 1);
+      }
     }
   } else if (warp == kWarpV) {
     // ------------------------------ V loads ------------------------------
     if (lane == 0) {
       uint32_t vc = 0;
       bool ok = true;
-      int4 T = T0;
-      for (int i = 0; unit_at(i) < n_units && ok; ++i) {
-        const int u = unit_at(i);
-        const int4 cur = T;
-        if (unit_at(i + 1) < n_units) T = tile_of(a, unit_at(i + 1));
-        const int kvh = u % a.Hkv;
-        for (int j = 0; j < cur.w; ++j, ++vc) {
+      Unit U = U0;
+      for (int i = 0; unit_at<PAIR>(i) < n_units && ok; ++i) {
+        const Unit cur = U;
+        if (unit_at<PAIR>(i + 1) < n_units) U = unit_rec<PAIR>(a, unit_at<PAIR>(i + 1), rank);
+        for (int j = 0; j < cur.nkb; ++j, ++vc) {
           const int st = vc % kVStages;
           if (!wait_or_abort(&ctl->v_empty[st], ((vc / kVStages) & 1) ^ 1, ctl)) {
             abort_kernel(ctl, a.err, W_V_EMPTY, j);
@@ -309,14 +405,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           uint8_t* v = sV + st * kTile;
-          const int z = cur.y + j * kKB;
-          tc::mbar_arrive_expect_tx(&ctl->v_full[st], kTile);
-          tc::tma_load_3d(v, &mapV, &ctl->v_full[st], 0, kvh, z);
-          tc::tma_load_3d(v + kHalf, &mapV, &ctl->v_full[st], 64, kvh, z);
+          const int z = cur.t.y + j * kKB;
+          if (PAIR && cur.shared) {
+            tc::mbar_arrive_expect_tx(&ctl->v_full[st], kTile);
+            tma_load_3d_multicast(v + rank * kHalf, &mapV, &ctl->v_full[st], 64 * (int)rank,
+                                      cur.kvh, z, kBoth);
+          } else if (j < cur.t.w) {
+            tc::mbar_arrive_expect_tx(&ctl->v_full[st], kTile);
+            tc::tma_load_3d(v, &mapV, &ctl->v_full[st], 0, cur.kvh, z);
+            tc::tma_load_3d(v + kHalf, &mapV, &ctl->v_full[st], 64, cur.kvh, z);
+          } else {
+            tc::mbar_arrive(&ctl->v_full[st]);
+          }
         }
       }
-      for (uint32_t c = (vc > (uint32_t)kVStages ? vc - kVStages : 0); c < vc; ++c)
+      for (uint32_t c = (vc > (uint32_t)kVStages ? vc - kVStages : 0); c < vc; ++c) {
         tc::mbar_wait(&ctl->v_full[c % kVStages], (c / kVStages) & 1);
+        if (PAIR) tc::mbar_wait(&ctl->v_empty[c % kVStages], (c / kVStages) & 1);
+      }
     }
   } else if (warp == kWarpS) {
     // ------------------------------ S = Q K^T ------------------------------
@@ -324,38 +430,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_s = tc::idesc_bf16_f32(128, kKB);
       uint32_t kc = 0, b = 0;
       bool ok = true;
-      int4 T = T0;
-      for (int i = 0; unit_at(i) < n_units && ok; ++i) {
-        const int nkb = T.w;
-        if (unit_at(i + 1) < n_units) T = tile_of(a, unit_at(i + 1));
+      Unit U = U0;
+      for (int i = 0; unit_at<PAIR>(i) < n_units && ok; ++i) {
+        const Unit cur = U;
+        if (unit_at<PAIR>(i + 1) < n_units) U = unit_rec<PAIR>(a, unit_at<PAIR>(i + 1), rank);
         const int qb = i % kQBufs;
         if (!wait_or_abort(&ctl->q_full[qb], (i / kQBufs) & 1, ctl)) {
           abort_kernel(ctl, a.err, W_Q_FULL, 0);
           break;
         }
         const uint32_t q_addr = tc::smem_u32(sQ + qb * kTile);
-        for (int j = 0; j < nkb; ++j, ++kc, ++b) {
+        for (int j = 0; j < cur.nkb; ++j, ++kc) {
           const int st = kc % kKStages;
+          // a stage is released only after its copies have landed, also when
+          // this CTA does not use it (the next copies into it count on the
+          // next phase)
           if (!wait_or_abort(&ctl->k_full[st], (kc / kKStages) & 1, ctl)) {
             abort_kernel(ctl, a.err, W_K_FULL, j);
             ok = false;
             break;
           }
-          // buffer b % 3 holds P of block b - 3 until that block's P.V is done
-          const uint32_t sb = b % kSBufs;
-          if (!wait_or_abort(&ctl->pv_done[sb], ((b / kSBufs) & 1) ^ 1, ctl)) {
-            abort_kernel(ctl, a.err, W_S_FREE, j);
-            ok = false;
-            break;
-          }
-          tc::tc_fence_after();
-          const uint32_t kaddr = tc::smem_u32(sK + st * kTile);
-          const uint32_t d = tmem + sb * kKB;
+          if (j < cur.t.w) {
+            // buffer b % 3 holds P of block b - 3 until that block's P.V is done
+            const uint32_t sb = b % kSBufs;
+            if (!wait_or_abort(&ctl->pv_done[sb], ((b / kSBufs) & 1) ^ 1, ctl)) {
+              abort_kernel(ctl, a.err, W_S_FREE, j);
+              ok = false;
+              break;
+            }
+            tc::tc_fence_after();
+            const uint32_t kaddr = tc::smem_u32(sK + st * kTile);
+            const uint32_t d = tmem + sb * kKB;
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk)
-            tc::mma_bf16(d, kmajor_step(q_addr, kk), kmajor_step(kaddr, kk), idesc_s, kk != 0);
-          tc::mma_commit(&ctl->s_full[sb]);
-          tc::mma_commit(&ctl->k_empty[st]);
+            for (int kk = 0; kk < kD / 16; ++kk)
+              tc::mma_bf16(d, kmajor_step(q_addr, kk), kmajor_step(kaddr, kk), idesc_s, kk != 0);
+            tc::mma_commit(&ctl->s_full[sb]);
+            ++b;
+          }
+          if (PAIR)
+            mma_commit_multicast(&ctl->k_empty[st], kBoth);
+          else
+            tc::mma_commit(&ctl->k_empty[st]);
         }
         if (!ok) break;
         tc::mma_commit(&ctl->q_empty[qb]);
@@ -367,38 +482,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_o = tc::idesc_bf16_f32(128, kD, /*b_mn_major=*/true);
       uint32_t vc = 0, b = 0;
       bool ok = true;
-      int4 T = T0;
-      for (int i = 0; unit_at(i) < n_units && ok; ++i) {
-        const int nkb = T.w;
-        if (unit_at(i + 1) < n_units) T = tile_of(a, unit_at(i + 1));
+      Unit U = U0;
+      for (int i = 0; unit_at<PAIR>(i) < n_units && ok; ++i) {
+        const Unit cur = U;
+        if (unit_at<PAIR>(i + 1) < n_units) U = unit_rec<PAIR>(a, unit_at<PAIR>(i + 1), rank);
         const uint32_t o = tmem + kColO;
         // O was last read by the output warps for unit i - 1
         if (!wait_or_abort(&ctl->o_empty, (i & 1) ^ 1, ctl)) {
           abort_kernel(ctl, a.err, W_O_EMPTY, 0);
           break;
         }
-        for (int j = 0; j < nkb; ++j, ++vc, ++b) {
+        for (int j = 0; j < cur.nkb; ++j, ++vc) {
+          const int st = vc % kVStages;
+          const bool use = j < cur.t.w;
           const uint32_t sb = b % kSBufs;
-          if (!wait_or_abort(&ctl->p_full[sb], (b / kSBufs) & 1, ctl)) {
+          if (use && !wait_or_abort(&ctl->p_full[sb], (b / kSBufs) & 1, ctl)) {
             abort_kernel(ctl, a.err, W_P_FULL, j);
             ok = false;
             break;
           }
-          const int st = vc % kVStages;
           if (!wait_or_abort(&ctl->v_full[st], (vc / kVStages) & 1, ctl)) {
             abort_kernel(ctl, a.err, W_V_FULL, j);
             ok = false;
             break;
           }
-          tc::tc_fence_after();
-          const uint32_t vaddr = tc::smem_u32(sV + st * kTile);
-          const uint32_t pa = tmem + sb * kKB;
+          if (use) {
+            tc::tc_fence_after();
+            const uint32_t vaddr = tc::smem_u32(sV + st * kTile);
+            const uint32_t pa = tmem + sb * kKB;
 #pragma unroll
-          for (int kk = 0; kk < kKB / 16; ++kk)
-            tc::mma_bf16_ts(o, pa + kk * 8, tc::smem_desc_mn128(vaddr + kk * 16 * 128, kHalf),
-                            idesc_o, (j | kk) != 0 ? 1u : 0u);
-          tc::mma_commit(&ctl->pv_done[sb]);
-          tc::mma_commit(&ctl->v_empty[st]);
+            for (int kk = 0; kk < kKB / 16; ++kk)
+              tc::mma_bf16_ts(o, pa + kk * 8, tc::smem_desc_mn128(vaddr + kk * 16 * 128, kHalf),
+                              idesc_o, (j | kk) != 0 ? 1u : 0u);
+            tc::mma_commit(&ctl->pv_done[sb]);
+            ++b;
+          }
+          if (PAIR)
+            mma_commit_multicast(&ctl->v_empty[st], kBoth);
+          else
+            tc::mma_commit(&ctl->v_empty[st]);
         }
         if (!ok) break;
         tc::mma_commit(&ctl->o_full);
@@ -415,14 +537,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float scale = a.scale_log2;
     uint32_t b = 0;
     // this unit's record and positions, read one unit ahead
-    int4 T = T0;
+    Unit U = U0;
     int p0n = pos0[0], p1n = pos0[1], pfn = pos0[2];
-    for (int i = 0; unit_at(i) < n_units; ++i) {
-      const int nkb = T.w;
+    for (int i = 0; unit_at<PAIR>(i) < n_units; ++i) {
+      const int nkb = U.t.w;
       const int p0 = p0n, p1 = p1n;
       const int p_first = pfn;                         // rows ascend: the tile's smallest
-      const bool more = unit_at(i + 1) < n_units;
-      if (more) T = tile_of(a, unit_at(i + 1));
+      const bool more = unit_at<PAIR>(i + 1) < n_units;
+      if (more) U = unit_rec<PAIR>(a, unit_at<PAIR>(i + 1), rank);
       const uint32_t tO = tmem + lane_off + kColO;
       float mu0 = kFloor, mu1 = kFloor;                // running maxima (log2 units)
       float l0 = 0.f, l1 = 0.f;                        // this thread's part of the row sums
@@ -532,10 +654,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mu1 = mn1;
       }
       if (!ok) break;
-      if (more) {
-        p0n = a.rows[T.x + min(rl0, T.z - 1)].pos;
-        p1n = a.rows[T.x + min(rl1, T.z - 1)].pos;
-        pfn = a.rows[T.x].pos;
+      if (more && U.t.z > 0) {
+        p0n = a.rows[U.t.x + min(rl0, U.t.z - 1)].pos;
+        p1n = a.rows[U.t.x + min(rl1, U.t.z - 1)].pos;
+        pfn = a.rows[U.t.x].pos;
       }
       // row sums: the four threads of a row, in a fixed order
       l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
@@ -560,12 +682,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int rl = m / a.g;
     const int hh = m % a.g;
-    int4 T = T0;
-    for (int i = 0; unit_at(i) < n_units; ++i) {
-      const int u = unit_at(i);
-      const int4 cur = T;
-      if (unit_at(i + 1) < n_units) T = tile_of(a, unit_at(i + 1));
-      const int kvh = u % a.Hkv;
+    Unit U = U0;
+    for (int i = 0; unit_at<PAIR>(i) < n_units; ++i) {
+      const Unit cu = U;
+      const int4 cur = cu.t;
+      if (unit_at<PAIR>(i + 1) < n_units) U = unit_rec<PAIR>(a, unit_at<PAIR>(i + 1), rank);
+      const int kvh = cu.kvh;
       if (!warp_wait_or_abort(&ctl->o_full, i & 1, ctl)) {
         abort_kernel(ctl, a.err, W_O_FULL, cur.w);
         break;
@@ -617,6 +739,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc::tc_fence_before();
   __syncthreads();
+  if (PAIR) {
+    // the other CTA has no copy into, nor arrival on, this one's shared
+    // memory in flight (its producers waited for the last phases above)
+    __syncwarp();
+    tc::cluster_sync_all();
+  }
   tc::tc_fence_after();
   if (warp == kWarpS) tc::tmem_dealloc(tmem, kTmemCols);
 }
@@ -626,6 +754,38 @@ __global__ void attn_tiles_kernel(const fuse_request_t* reqs, int n_req, const i
   pdl_trigger();
   pdl_wait();
   build_attn_tiles(reqs, n_req, idx, rtile, tiles);
+}
+
+// Clusters of two CTAs of the paired kernel that can be resident at once
+// (two free SMs of one GPC each), per device; 0 when none can.
+int resident_pairs() {
+  static std::mutex mu;
+  static std::map<int, int> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(dev);
+  if (it != cache.end()) return it->second;
+  const void* kernel = reinterpret_cast<const void*>(attn_tc_kernel<true>);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (set_dyn_smem_once(kernel, kSmemBytes) != cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess || clusters < 0) {
+    cudaGetLastError();
+    clusters = 0;
+  }
+  cache[dev] = clusters;
+  return clusters;
 }
 
 int sm_count() {
@@ -684,7 +844,6 @@ cudaError_t launch_attention_tc(const fuse_layer_desc_t& d, const fuse_requests_
   AttnArgs a;
   a.tiles = tiles;
   a.n_tiles = n_tiles;
-  a.n_units = n_tiles * d.n_kv_heads;
   a.reqs = reqs.d_req;
   a.rows = rows;
   a.O = reinterpret_cast<__nv_bfloat16*>(O);
@@ -699,10 +858,26 @@ cudaError_t launch_attention_tc(const fuse_layer_desc_t& d, const fuse_requests_
   // finished before the QKV projection (launched after it) let this kernel
   // start; otherwise the tile kernel launched just above is still running
   a.records_ready = tiles_ready ? 1 : 0;
-  e = set_dyn_smem_once(reinterpret_cast<const void*>(attn_tc_kernel), kSmemBytes);
+  // tiles in pairs (clusters of two CTAs) for long contexts, where K and V
+  // dominate the data the kernel moves: on a 33 024-token request the pairs
+  // raise the power-capped clock and the layer-step's rate by ~1 %; on
+  // requests of 4–10 K tokens they cost 0.5–3 % at the full clock
+  int64_t longest = 0;
+  for (int r = 0; r < reqs.n_req; ++r)
+    longest = std::max<int64_t>(longest, reqs.h_req[r].n_ctx + reqs.h_req[r].n_query);
+  const int pairs = (n_tiles >= 2 && longest >= kPairMinTokens) ? resident_pairs() : 0;
+  if (pairs > 0) {
+    a.n_units = (n_tiles + 1) / 2 * d.n_kv_heads;
+    const int grid = 2 * (a.n_units < pairs ? a.n_units : pairs);
+    return launch_pdl_pairs(attn_tc_kernel<true>, dim3(grid), dim3(kThreads), kSmemBytes, s, mQ,
+                            mK, mV, a);
+  }
+  a.n_units = n_tiles * d.n_kv_heads;
+  e = set_dyn_smem_once(reinterpret_cast<const void*>(attn_tc_kernel<false>), kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = a.n_units < sm_count() ? a.n_units : sm_count();
-  return launch_pdl(attn_tc_kernel, dim3(grid), dim3(kThreads), kSmemBytes, s, mQ, mK, mV, a);
+  return launch_pdl(attn_tc_kernel<false>, dim3(grid), dim3(kThreads), kSmemBytes, s, mQ, mK, mV,
+                    a);
 }
 
 }  // namespace fusekv

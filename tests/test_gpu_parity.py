@@ -63,22 +63,32 @@ STORAGE = {
     # two requests of the batched paged workload with 4-bit codes in the
     # block pool (d / 2 bytes per token and head, partial tail blocks)
     "int4_paged2": synth.scaled(C["llama3_8b_paged_batch16"], n_requests=2, kv_storage="u4"),
-    # int8 codes in the block pool (16-token blocks, partial tail blocks): the
-    # ring-buffered int8 stitch, paged
+    # int8 codes in the block pool (16-token blocks, partial tail blocks)
     "int8_paged2": synth.scaled(C["llama3_8b_paged_batch16"], n_requests=2, kv_storage="u8",
                                 seed=9),
-    # int8, d = 64, ragged chunks of 1..70 tokens: the ring stitch's partial
-    # tiles and chunk changes inside a CTA's range of tiles
+    # int8, d = 64, ragged chunks of 1..70 tokens: partial row tiles of the
+    # int8 stitch and 1-token chunks
     "int8_ragged_d64": synth.scaled(C["llama3_70b_int8_long"], hidden=1024, n_q_heads=16,
                                     head_dim=64, w_std=1.0 / 32.0, chunks_per_request=None,
                                     chunk_len=None, query_len=None, chunk_count_range=(2, 6),
                                     chunk_len_range=(1, 70), query_len_range=(1, 9),
                                     n_requests=3, ratio=0.3, seed=13),
-    # int8 with 4 KV heads: the per-thread int8 stitch (the ring one needs a
-    # multiple of 8 heads)
+    # int8 with 4 KV heads: eight rows per stitch tile instead of four
     "int8_hkv4": synth.scaled(C["llama3_70b_int8_long"], hidden=1024, n_q_heads=8, n_kv_heads=4,
                               w_std=1.0 / 32.0, chunks_per_request=3, chunk_len=100, query_len=8,
                               seed=14),
+}
+
+# Requests of 16 384 tokens and more: the attention takes its tiles in pairs
+# on clusters of two CTAs.  Two such requests with few selected rows (the
+# oracle's attention stays cheap) and a GQA group of 2 (64-row tiles): pairs
+# inside a request share their K/V fetches, pairs across the two requests do
+# not, and an odd tile count leaves one tile without a partner.
+LONG = {
+    "long_pairs2": synth.scaled(C["llama3_70b_int8_long"], hidden=1024, n_q_heads=16,
+                                w_std=1.0 / 32.0, n_requests=2, chunks_per_request=None,
+                                chunk_count_range=(16, 17), chunk_len=1024, query_len=16,
+                                ratio=0.0029, seed=15),
 }
 
 _CASES = {}
@@ -86,7 +96,8 @@ _CASES = {}
 
 def case_of(name):
     if name not in _CASES:
-        _CASES[name] = make_case(SMALL[name] if name in SMALL else STORAGE[name])
+        cfg = SMALL.get(name) or STORAGE.get(name) or LONG[name]
+        _CASES[name] = make_case(cfg)
     return _CASES[name]
 
 
@@ -298,7 +309,7 @@ def test_recompute_selected(name):
 # them by more than 2e-2: the allowance covers exactly those flips.
 @pytest.mark.parametrize("name", ["tiny_fp32", "qwen3_8b_layer", "paged3", "ragged_fp32",
                                   "ragged_paged_bf16_d64", "sparse_long_bf16", "int8_4x1024",
-                                  "wide_hidden_bf16"])
+                                  "wide_hidden_bf16", "long_pairs2"])
 def test_layer_step(name):
     case = case_of(name)
     b = buffers(case)
