@@ -35,8 +35,9 @@
 // blocks) one unit ahead.  The kernel is persistent; units are taken heaviest
 // first, snake-ordered over the CTAs (round r visits the CTAs upwards when r
 // is even and downwards when r is odd).
-// Tiles go in pairs: a cluster of two CTAs takes two neighbouring tiles (by
-// key-block count) of one KV head, and when both belong to one request every
+// For requests of 16 384 tokens and more, tiles go in pairs: a cluster of
+// two CTAs takes two neighbouring tiles (by key-block count) of one KV head
+// (units are then pairs of tiles), and when both belong to one request every
 // K and V block is fetched from L2 once for both: each CTA loads one
 // 64-column half with TMA multicast into both CTAs' rings, and a stage is
 // refilled once both CTAs' MMAs have released it (their commits arrive on
