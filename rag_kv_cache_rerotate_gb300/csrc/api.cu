@@ -30,6 +30,12 @@ cudaError_t launch_project_query_tc(const fuse_layer_desc_t& d, int64_t n_rows, 
                                     const void* Wq, void* Q, const void* Hs, uint32_t* err,
                                     cudaStream_t s, float* split_ws = nullptr, int max_splits = 1);
 bool tc_attention_supported(const fuse_layer_desc_t& desc);
+// Query rows projected head by head with the rows on the MMA's short side
+// (csrc/query_proj_tc.cu).
+bool qproj_tc_supported(const fuse_layer_desc_t& d, int64_t n_rows);
+cudaError_t launch_qproj_tc(const fuse_layer_desc_t& d, int64_t n_rows, const float2* rope,
+                            const void* Wq, const void* X, void* Q, float* part, int max_splits,
+                            uint32_t* err, cudaStream_t s);
 // Query-aware attention mass on the tensor cores (csrc/attention_mass_tc.cu).
 bool mass_tc_supported(const fuse_layer_desc_t& d);
 int mass_tc_chunks(const fuse_layer_desc_t& d, const fuse_requests_t& reqs, int max_ctx,
@@ -381,6 +387,9 @@ fuse_status_t do_mass(const fuse_layer_desc_t& d, const fuse_requests_t& r, cons
         const size_t per_split = (size_t)nq * d.n_q_heads * d.head_dim * sizeof(float);
         const size_t room = L.total - L.kn;
         const int max_splits = (int)std::min<size_t>(8, room / std::max<size_t>(per_split, 1));
+        if (max_splits >= 1 && qproj_tc_supported(d, nq))
+          return launch_qproj_tc(d, nq, rope, Wq, at<void>(ws, L.mhs), Q, at<float>(ws, L.kn),
+                                 max_splits, err, s);
         return launch_project_query_tc(d, nq, rope, Wq, Q, at<void>(ws, L.mhs), err, s,
                                        at<float>(ws, L.kn), max_splits);
       });

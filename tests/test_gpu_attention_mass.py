@@ -24,13 +24,14 @@ import test_gpu_parity as parity
 pytestmark = pytest.mark.gpu
 
 # fp32 (SIMT projection), bf16 d = 64 ragged/paged with empty queries (SIMT
-# projection in bf16), the Qwen3-8B-shaped layer and three requests of the
-# batched paged workload (tensor-core projection)
-# the tensor-core scorer: three requests of the batched paged workload, the
-# Qwen3-8B-shaped layer, and four 1024-token chunks of the Llama-3-70B shape
-# (eight query heads per KV head: four 128-vector tiles per KV head)
+# projection in bf16); the tensor-core scorer: three requests of the batched
+# paged workload (172 query rows: the layer GEMM's pair tiles split over K),
+# the Qwen3-8B-shaped layer (64 rows), four 1024-token chunks of the
+# Llama-3-70B shape (eight query heads per KV head: four 128-vector tiles per
+# KV head) and 70 query rows (a partial second group of 64 rows) -- up to 128
+# rows the projection is formed transposed, rows on the MMA's short side
 CASES = ["tiny_fp32", "ragged_fp32", "ragged_paged_bf16_d64", "paged3", "qwen3_8b_layer",
-         "int8_4x1024"]
+         "int8_4x1024", "qwen3_q70"]
 
 
 def _tol(cfg):

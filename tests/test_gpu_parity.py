@@ -73,6 +73,9 @@ STORAGE = {
                                     chunk_len=None, query_len=None, chunk_count_range=(2, 6),
                                     chunk_len_range=(1, 70), query_len_range=(1, 9),
                                     n_requests=3, ratio=0.3, seed=13),
+    # 70 query rows: the scorer's short-side query projection with a partial
+    # second group of 64 rows
+    "qwen3_q70": synth.scaled(C["qwen3_8b_layer"], chunks_per_request=2, query_len=70, seed=16),
     # int8 with 4 KV heads: eight rows per stitch tile instead of four
     "int8_hkv4": synth.scaled(C["llama3_70b_int8_long"], hidden=1024, n_q_heads=8, n_kv_heads=4,
                               w_std=1.0 / 32.0, chunks_per_request=3, chunk_len=100, query_len=8,
