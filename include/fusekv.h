@@ -507,6 +507,17 @@ typedef struct {
 fuse_status_t fuse_trace_begin(int32_t max_records);
 fuse_status_t fuse_trace_end(fuse_trace_entry_t* out, int32_t max_out, int32_t* n_out);
 
+/* Self-test of the device-side failure detection (no counterpart on the
+ * pages; a diagnostic).  Launches one CTA on `stream` whose thread waits,
+ * through the same bounded mbarrier wait every pipeline of the library uses,
+ * on a barrier that nothing arrives on.  When the wait gives up (after its
+ * one-second limit) the kernel records FUSE_ERR_TIMEOUT in the workspace's
+ * error word and returns, so the context stays usable: fuse_check_errors then
+ * returns FUSE_ERR_TIMEOUT.  ws: a workspace of at least 256 bytes (only its
+ * header is used), 256-byte aligned.  No fault, trap or endless wait is
+ * involved. */
+fuse_status_t fuse_selftest_wait_timeout(void* ws, size_t ws_bytes, fuse_stream_t stream);
+
 /* A static, human-readable name of a status code. */
 const char* fuse_status_string(fuse_status_t status);
 

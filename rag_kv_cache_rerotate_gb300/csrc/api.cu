@@ -30,6 +30,7 @@ cudaError_t launch_project_query_tc(const fuse_layer_desc_t& d, int64_t n_rows, 
                                     const void* Wq, void* Q, const void* Hs, uint32_t* err,
                                     cudaStream_t s, float* split_ws = nullptr, int max_splits = 1);
 bool tc_attention_supported(const fuse_layer_desc_t& desc);
+cudaError_t launch_selftest_wait(uint32_t* err, cudaStream_t s);
 // Query rows projected head by head with the rows on the MMA's short side
 // (csrc/query_proj_tc.cu).
 bool qproj_tc_supported(const fuse_layer_desc_t& d, int64_t n_rows);
@@ -626,6 +627,12 @@ fuse_status_t fuse_workspace_size(const fuse_layer_desc_t* desc, const fuse_requ
 fuse_status_t fuse_workspace_reset(void* ws, size_t ws_bytes, fuse_stream_t stream) {
   if (!ws || ws_bytes < sizeof(WsHeader)) return FUSE_ERR_WORKSPACE;
   return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes, (cudaStream_t)stream));
+}
+
+fuse_status_t fuse_selftest_wait_timeout(void* ws, size_t ws_bytes, fuse_stream_t stream) {
+  const fuse_status_t st = check_ws(ws, ws_bytes, sizeof(WsHeader));
+  if (st != FUSE_OK) return st;
+  return cuda_status(launch_selftest_wait(at<uint32_t>(ws, 0), (cudaStream_t)stream));
 }
 
 fuse_status_t fuse_stitch_rerotate(const fuse_layer_desc_t* desc, const fuse_chunks_t* chunks,

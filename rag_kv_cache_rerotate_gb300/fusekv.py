@@ -109,6 +109,7 @@ _SIGS = {
     "fuse_plan_requests": (_c.c_int, [_c.c_int32, _P, _P, _c.c_double, _P, _P]),
     "fuse_workspace_size": (_c.c_int, [_P, _P, _c.POINTER(_c.c_size_t)]),
     "fuse_workspace_reset": (_c.c_int, [_P, _c.c_size_t, _P]),
+    "fuse_selftest_wait_timeout": (_c.c_int, [_P, _c.c_size_t, _P]),
     "fuse_stitch_rerotate": (_c.c_int, [_P, _P, _P, _P, _c.c_int64, _P, _c.c_size_t, _P]),
     "fuse_score_deviation": (_c.c_int, [_P, _P, _P, _P, _P, _P, _P, _c.c_size_t, _P]),
     "fuse_score_attention_mass": (_c.c_int, [_P, _P, _P, _P, _P, _c.c_int32, _P, _P,
@@ -461,6 +462,14 @@ def check_errors(ws, stream=None):
     st = load().fuse_check_errors(_ptr(ws), _stream(stream), _c.byref(detail))
     if st != FUSE_OK:
         raise FuseError(st, f"device (site {detail.value >> 24}, info {detail.value & 0xFFFFFF})")
+
+
+def selftest_wait_timeout(ws, stream=None):
+    """Launch the library's failure-detection self-test: a bounded wait on a
+    barrier nothing arrives on, reported as FUSE_ERR_TIMEOUT in ws's error
+    word after the wait's one-second limit (read it with check_errors)."""
+    _check(load().fuse_selftest_wait_timeout(_ptr(ws), ws.numel(), _stream(stream)),
+           "fuse_selftest_wait_timeout")
 
 
 def workspace_reset(ws, stream=None):
