@@ -27,9 +27,10 @@
 // 2^16 (then O and the running sum l are rescaled).  A separate warpgroup
 // writes O / l of a unit while the softmax starts on the next one (whose
 // first P.V waits until O has been read).
-// Roles, each behind its own mbarriers: warp 0 loads Q (two buffers, so the
-// next unit's Q lands while this one's scores are formed) and K blocks (3-stage
-// ring), warp 2 V blocks (2-stage ring), warp 1 issues the S MMAs, warp 3 the
+// Roles, each behind its own mbarriers: warp 0 loads Q (two buffers in the
+// single-CTA form, so that the next unit's Q lands while this one's scores
+// are formed; one in the paired form) and K blocks (a 3-stage ring; 4 in the
+// paired form), warp 2 V blocks (2-stage ring), warp 1 issues the S MMAs, warp 3 the
 // P.V MMAs, warps 4-11 the softmax, warps 12-15 the output.  Every role reads
 // the unit's tile record (first output row, first fused row, rows, key
 // blocks) one unit ahead.  The kernel is persistent; units are taken heaviest
@@ -67,9 +68,20 @@ constexpr int kD = 128;
 constexpr int kKB = 128;                      // keys per block
 constexpr int kHalf = 128 * 64 * 2;           // one 64-column half of a 128-row tile (16 KB)
 constexpr int kTile = 2 * kHalf;              // 32 KB
-constexpr int kQBufs = 2;                     // Q tiles in flight (next unit's while this one runs)
+// Ring depths: the single-CTA form double-buffers Q (its units can be short,
+// and the next unit's Q then lands while this one runs); the paired form, for
+// long requests whose units run over a hundred key blocks, trades the second
+// Q buffer for a fourth K stage (the same shared memory), which keeps the two
+// CTAs' shared rings fed (+0.5 % on the long-context step)
+constexpr int kQBufs = 2;                     // Q tiles in flight, at most
 constexpr int64_t kPairMinTokens = 16384;     // longest request from which tiles go in pairs
-constexpr int kKStages = 3;
+constexpr int kKStages = 4;                   // K stages, at most
+template <bool PAIR> struct Ring {
+  static constexpr int QB = PAIR ? 1 : 2;     // Q buffers
+  static constexpr int KS = PAIR ? 4 : 3;     // K stages
+};
+static_assert(Ring<true>::QB + Ring<true>::KS == Ring<false>::QB + Ring<false>::KS,
+              "both forms lay out the same shared memory");
 constexpr int kVStages = 2;
 constexpr int kWarpQK = 0, kWarpS = 1, kWarpV = 2, kWarpPV = 3, kWarpSoft = 4, kWarpOut = 12;
 constexpr int kSoftThreads = 256;
@@ -113,7 +125,8 @@ struct Ctl {
   volatile int abort_flag;
   float xl[128];          // [row] softmax row sum of the unit being written
 };
-constexpr int kSmemBytes = (kQBufs + kKStages + kVStages) * kTile + 1024 + (int)sizeof(Ctl);
+constexpr int kSmemBytes =
+    (Ring<false>::QB + Ring<false>::KS + kVStages) * kTile + 1024 + (int)sizeof(Ctl);
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ctl* ctl) {
@@ -260,12 +273,13 @@ template <bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                    const __grid_constant__ CUtensorMap mapV, const AttnArgs a) {
+  constexpr int kQB = Ring<PAIR>::QB, kKS = Ring<PAIR>::KS;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;                               // Q buffer q at sQ + q * kTile
-  uint8_t* sK = smem + kQBufs * kTile;              // K stage s at sK + s * kTile
-  uint8_t* sV = sK + kKStages * kTile;              // V stage s at sV + s * kTile
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + (kQBufs + kKStages + kVStages) * kTile);
+  uint8_t* sK = smem + kQB * kTile;              // K stage s at sK + s * kTile
+  uint8_t* sV = sK + kKS * kTile;              // V stage s at sV + s * kTile
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + (kQB + kKS + kVStages) * kTile);
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const uint32_t rank = PAIR ? tc::cluster_rank() : 0u;
@@ -274,11 +288,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_trigger();
 
   if (threadIdx.x == 0) {
-    for (int q = 0; q < kQBufs; ++q) {
+    for (int q = 0; q < kQB; ++q) {
       tc::mbar_init(&ctl->q_full[q], 1);
       tc::mbar_init(&ctl->q_empty[q], 1);
     }
-    for (int s = 0; s < kKStages; ++s) {
+    for (int s = 0; s < kKS; ++s) {
       tc::mbar_init(&ctl->k_full[s], 1);
       tc::mbar_init(&ctl->k_empty[s], kUsers);
     }
@@ -343,8 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (; unit_at<PAIR>(i) < n_units && ok; ++i) {
         const Unit cur = U;
         if (unit_at<PAIR>(i + 1) < n_units) U = unit_rec<PAIR>(a, unit_at<PAIR>(i + 1), rank);
-        const int qb = i % kQBufs;
-        if (!wait_or_abort(&ctl->q_empty[qb], ((i / kQBufs) & 1) ^ 1, ctl)) {
+        const int qb = i % kQB;
+        if (!wait_or_abort(&ctl->q_empty[qb], ((i / kQB) & 1) ^ 1, ctl)) {
           abort_kernel(ctl, a.err, W_Q_EMPTY, 0);
           break;
         }
@@ -357,8 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mbar_arrive(&ctl->q_full[qb]);
         }
         for (int j = 0; j < cur.nkb; ++j, ++kc) {
-          const int st = kc % kKStages;
-          if (!wait_or_abort(&ctl->k_empty[st], ((kc / kKStages) & 1) ^ 1, ctl)) {
+          const int st = kc % kKS;
+          if (!wait_or_abort(&ctl->k_empty[st], ((kc / kKS) & 1) ^ 1, ctl)) {
             abort_kernel(ctl, a.err, W_K_EMPTY, j);
             ok = false;
             break;
@@ -382,11 +396,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // let copies in flight land (and, in a pair, the other CTA's releases
       // of the last stages arrive) before the CTA may exit
-      for (int k = (i > kQBufs ? i - kQBufs : 0); k < i; ++k)
-        tc::mbar_wait(&ctl->q_full[k % kQBufs], (k / kQBufs) & 1);
-      for (uint32_t c = (kc > (uint32_t)kKStages ? kc - kKStages : 0); c < kc; ++c) {
-        tc::mbar_wait(&ctl->k_full[c % kKStages], (c / kKStages) & 1);
-        if (PAIR) tc::mbar_wait(&ctl->k_empty[c % kKStages], (c / kKStages) & 1);
+      for (int k = (i > kQB ? i - kQB : 0); k < i; ++k)
+        tc::mbar_wait(&ctl->q_full[k % kQB], (k / kQB) & 1);
+      for (uint32_t c = (kc > (uint32_t)kKS ? kc - kKS : 0); c < kc; ++c) {
+        tc::mbar_wait(&ctl->k_full[c % kKS], (c / kKS) & 1);
+        if (PAIR) tc::mbar_wait(&ctl->k_empty[c % kKS], (c / kKS) & 1);
       }
     }
   } else if (warp == kWarpV) {
@@ -435,18 +449,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; unit_at<PAIR>(i) < n_units && ok; ++i) {
         const Unit cur = U;
         if (unit_at<PAIR>(i + 1) < n_units) U = unit_rec<PAIR>(a, unit_at<PAIR>(i + 1), rank);
-        const int qb = i % kQBufs;
-        if (!wait_or_abort(&ctl->q_full[qb], (i / kQBufs) & 1, ctl)) {
+        const int qb = i % kQB;
+        if (!wait_or_abort(&ctl->q_full[qb], (i / kQB) & 1, ctl)) {
           abort_kernel(ctl, a.err, W_Q_FULL, 0);
           break;
         }
         const uint32_t q_addr = tc::smem_u32(sQ + qb * kTile);
         for (int j = 0; j < cur.nkb; ++j, ++kc) {
-          const int st = kc % kKStages;
+          const int st = kc % kKS;
           // a stage is released only after its copies have landed, also when
           // this CTA does not use it (the next copies into it count on the
           // next phase)
-          if (!wait_or_abort(&ctl->k_full[st], (kc / kKStages) & 1, ctl)) {
+          if (!wait_or_abort(&ctl->k_full[st], (kc / kKS) & 1, ctl)) {
             abort_kernel(ctl, a.err, W_K_FULL, j);
             ok = false;
             break;
